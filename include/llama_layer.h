@@ -1,0 +1,232 @@
+/*
+ * llama_layer.h - C ABI of the GB300 (sm_103a) Llama decoder-layer forward.
+ *
+ * The library computes, over one flat batch of tokens drawn from many
+ * sequences,
+ *
+ *     hidden_states, residual = layer(positions, hidden_states, residual)
+ *
+ * for one Llama decoder layer (llama_layer_forward), for a stack of layers
+ * followed by the final norm, lm_head and greedy sampling
+ * (llama_stack_forward), and the paged KV-cache write on its own
+ * (kv_cache_write).
+ *
+ * Sources (three web pages on vLLM's llama.py), cited by tag:
+ *   [LLAMA-70B]    "LLama - DeepSeek-R1-Distill-Llama-70B" (hotelren.com
+ *                  walk-through): config.json; section 3 input_layernorm
+ *                  (RMSNorm with the residual add fused in); section 4
+ *                  LlamaAttention; LlamaMLP and SiluAndMul; the final RMSNorm;
+ *                  the Sampler.
+ *   [WALKTHROUGH]  "模型库与算子层 — 代码走读" (vllm-learning code
+ *                  walkthrough): LlamaModel, LlamaDecoderLayer, Attention
+ *                  (_update_kv_cache, attn_backend.forward with block_table),
+ *                  Linear layers (F.linear, weights stored [out, in]).
+ *   [CODE-READING] "vLLM Llama 代码解析" (yeyulingfeng.com): section 1
+ *                  LlamaForCausalLM (packed_modules_mapping, compute_logits),
+ *                  section 2.1 LlamaModel.forward (layer loop carrying the
+ *                  residual, final norm), section 4 LlamaAttention, section 5
+ *                  LlamaMLP.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; all
+ *     struct pointers (cfg, weights, batch, the per-layer arrays) are HOST
+ *     pointers read during the call only.
+ *   - Tensors are dense row-major; bf16 unless stated; 16-byte aligned.
+ *   - The caller owns all memory.  The library never allocates or frees
+ *     device memory: scratch comes from the caller's workspace, whose size
+ *     llama_workspace_size() returns.
+ *   - Work is enqueued on `stream` and runs asynchronously; nothing
+ *     synchronises the host.  Results are valid once the stream reaches them.
+ *   - A call returns LLAMA_OK, or a status code without launching anything
+ *     when its arguments are rejected.  No C++ exception crosses the ABI.
+ *   - Kernels never trap.  An out-of-range index met on the device (a cache
+ *     slot, a block-table entry, a token id, a position past seq_lens) is
+ *     recorded in a device error word and the access is skipped; a wait that
+ *     runs past its limit (2 s) is recorded and the kernel winds down.
+ *     llama_get_device_error() reports and clears the word.
+ *   - The library keeps no other state than that error word (one per device)
+ *     and cached kernel attributes.
+ */
+#ifndef LLAMA_LAYER_H_
+#define LLAMA_LAYER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers (same underlying type). */
+typedef struct CUstream_st* llama_stream_t;
+
+/* Status codes. */
+enum {
+  LLAMA_OK = 0,
+  LLAMA_ERR_ARG = 1,          /* null pointer, inconsistent or invalid size, unsupported activation */
+  LLAMA_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape or alignment */
+  LLAMA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
+  LLAMA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than llama_workspace_size() */
+  LLAMA_ERR_DEVICE_GUARD = 5, /* reported by llama_get_device_error: an index was out of range */
+  LLAMA_ERR_TIMEOUT = 6       /* reported by llama_get_device_error: a device wait gave up */
+};
+
+/* Layer shape and constants.  [LLAMA-70B] config.json: hidden_size,
+ * num_attention_heads, num_key_value_heads, head_dim, intermediate_size,
+ * rms_norm_eps, rope_theta, rope_scaling (llama3), hidden_act.
+ * Supported: head_dim 64 or 128; n_heads a multiple of n_kv_heads with
+ * n_heads / n_kv_heads <= 16; hidden, intermediate and n_heads*head_dim
+ * multiples of 8 (16-byte rows), hidden <= 16384; block_size 16;
+ * hidden_act 0 (silu).  Any other activation is rejected with LLAMA_ERR_ARG,
+ * as LlamaMLP raises for it ([LLAMA-70B] LlamaMLP). */
+typedef struct {
+  int hidden;
+  int n_heads;
+  int n_kv_heads;
+  int head_dim;
+  int intermediate;
+  int block_size;          /* tokens per KV-cache block (16) */
+  float rms_eps;
+  float rope_theta;
+  int rope_scaling;        /* 0: plain RoPE frequencies; 1: llama3 frequency rule */
+  float rs_factor;         /* llama3: factor (8) */
+  float rs_low_freq_factor;  /* llama3: low_freq_factor (1) */
+  float rs_high_freq_factor; /* llama3: high_freq_factor (4) */
+  int rs_original_max_pos;   /* llama3: original_max_position_embeddings (8192) */
+  int hidden_act;          /* 0 = silu; anything else is rejected */
+} LlamaLayerConfig;
+
+/* Weights of one layer, bf16, stored [out, in] as F.linear expects
+ * ([WALKTHROUGH] Linear layers).  The merged projections are packed in the
+ * order of [CODE-READING] section 1 packed_modules_mapping:
+ *   w_qkv     [(n_heads + 2*n_kv_heads)*head_dim, hidden]  rows q; k; v
+ *   w_o       [hidden, n_heads*head_dim]
+ *   w_gate_up [2*intermediate, hidden]                     rows gate; up
+ *   w_down    [hidden, intermediate]
+ *   ln1_w, ln2_w [hidden]  RMSNorm weights (input / post-attention). */
+typedef struct {
+  const void* ln1_w;
+  const void* w_qkv;
+  const void* w_o;
+  const void* ln2_w;
+  const void* w_gate_up;
+  const void* w_down;
+} LlamaLayerWeights;
+
+/* One flat batch ([CODE-READING] section 2.1: tokens of many sequences, with
+ * their positions).  Sequence b owns tokens [query_start_loc[b],
+ * query_start_loc[b+1]).  Its context length seq_lens[b] counts the cached
+ * tokens plus this step's; its cache blocks are block_table[b][0 ..
+ * ceil(seq_lens[b]/16)-1] ([WALKTHROUGH] Attention: kv_cache.block_table).
+ * A token at position p attends to cache positions 0..p of its sequence
+ * (this step's tokens are written first, so it sees itself).  A sequence with
+ * one new token takes the split-KV decode path, one with two or more the
+ * prefill path; both may appear in one batch.
+ * Device arrays (int32): positions [num_tokens], query_start_loc
+ * [num_seqs+1], seq_lens [num_seqs], block_table [num_seqs,
+ * max_blocks_per_seq], slot_mapping [num_tokens] or NULL (then slot =
+ * block_table[b][pos/16]*16 + pos%16 is derived on the device; a negative
+ * slot skips the token's cache write).  Host ints: max_query_len and
+ * max_seq_len bound the batch's query lengths and seq_lens (they size the
+ * launch grids; a sequence beyond them is reported as a device guard). */
+typedef struct {
+  int num_tokens;
+  int num_seqs;
+  int max_blocks_per_seq;
+  int num_blocks;          /* blocks in each cache array */
+  int max_query_len;
+  int max_seq_len;
+  const int32_t* positions;
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  const int32_t* slot_mapping;
+} LlamaBatch;
+
+/* Bytes of workspace a call needs for at most max_tokens tokens, max_seqs
+ * sequences and seq_lens up to max_seq_len; vocab > 0 adds what
+ * llama_stack_forward needs for the logits of max_seqs rows.  Returns 0 for
+ * an invalid config. */
+size_t llama_workspace_size(const LlamaLayerConfig* cfg, int max_tokens, int max_seqs, int max_seq_len, int vocab);
+
+/* One decoder layer ([CODE-READING] sections 3-5, [LLAMA-70B] sections 3-4
+ * and LlamaMLP):
+ *   h, r   = fused_add_rmsnorm(hidden_states, residual_in, ln1_w)
+ *            (residual_in NULL: r = hidden_states, [LLAMA-70B] section 3)
+ *   q,k,v  = split(h W_qkv^T); q, k rotated by RoPE at positions (v is not)
+ *   cache  : k, v stored (bf16) at each token's slot ([WALKTHROUGH] Attention)
+ *   o      = causal GQA attention of q over the paged cache
+ *   h2, r2 = fused_add_rmsnorm(o W_o^T, r, ln2_w)
+ *   out    = (silu(h2 W_gate^T) * (h2 W_up^T)) W_down^T
+ * hidden_states [num_tokens, hidden]: input x, overwritten with out.
+ * residual_in [num_tokens, hidden] or NULL; residual_out [num_tokens, hidden]
+ * receives r2 (may equal residual_in).  k_cache, v_cache [num_blocks,
+ * n_kv_heads, 16, head_dim] bf16 are updated in place. */
+int llama_layer_forward(const LlamaLayerConfig* cfg, const LlamaLayerWeights* weights, const LlamaBatch* batch,
+                        void* hidden_states, const void* residual_in, void* residual_out, void* k_cache,
+                        void* v_cache, void* workspace, size_t workspace_bytes, llama_stream_t stream);
+
+/* The model body and head over one flat batch ([CODE-READING] section 2.1;
+ * [WALKTHROUGH] LlamaModel; [LLAMA-70B] final RMSNorm and Sampler):
+ *   x = embed_w[input_ids] (if embed_w and input_ids are given; otherwise the
+ *       caller has put the input rows in hidden_states)
+ *   for each layer l: x, r = layer_l(positions, x, r), r = None at layer 0
+ *   hf = rmsnorm(x + r, final_norm_w) for the last token of every sequence
+ *   logits = hf lm_head_w^T (fp32, [num_seqs, vocab]); out_tokens = argmax
+ *   (lowest index on ties).
+ * layers, k_caches, v_caches are HOST arrays of num_layers entries (device
+ * pointers inside).  hidden_states and residual are [num_tokens, hidden]
+ * device buffers the call overwrites.  out_tokens [num_seqs] int32;
+ * out_logits [num_seqs, vocab] fp32 or NULL. */
+int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const LlamaLayerWeights* layers,
+                        const void* final_norm_w, const void* lm_head_w, int vocab, const void* embed_w,
+                        const int32_t* input_ids, const LlamaBatch* batch, void* hidden_states, void* residual,
+                        void* const* k_caches, void* const* v_caches, int32_t* out_tokens, float* out_logits,
+                        void* workspace, size_t workspace_bytes, llama_stream_t stream);
+
+/* The paged KV-cache update on its own ([WALKTHROUGH] Attention,
+ * _update_kv_cache): k, v [num_tokens, n_kv_heads, head_dim] bf16 are copied
+ * to cache[slot/16][h][slot%16][:] for every token with slot_mapping >= 0;
+ * slots >= num_blocks*16 are reported as a device guard and skipped. */
+int kv_cache_write(const void* k, const void* v, const int32_t* slot_mapping, int num_tokens, int n_kv_heads,
+                   int head_dim, int block_size, int num_blocks, void* k_cache, void* v_cache, llama_stream_t stream);
+
+/* Building blocks of the layer, exposed for tests and for callers composing
+ * their own step. */
+
+/* y[M, N] = x[M, K] W[N, K]^T ([WALKTHROUGH] Linear layers); y bf16
+ * (out_fp32 = 0) or fp32 (out_fp32 = 1).  K and N multiples of 8.
+ * The workspace holds split-K partial tiles (llama_linear_workspace_size). */
+int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int out_fp32, void* workspace,
+                 size_t workspace_bytes, llama_stream_t stream);
+size_t llama_linear_workspace_size(void);
+
+/* r = x (+ residual_in); h = r / sqrt(mean(r^2) + eps) * gamma, per row of
+ * length H ([LLAMA-70B] section 3; eps inside the square root).  residual_out
+ * may be NULL or alias x / residual_in; h may alias x. */
+int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residual_out, void* h, const void* gamma,
+                            int rows, int H, float eps, llama_stream_t stream);
+
+/* Causal GQA attention of q [num_tokens, n_heads, head_dim] (already rotated)
+ * over the paged caches, for the batch described by `batch`; writes
+ * out [num_tokens, n_heads*head_dim].  ([WALKTHROUGH] Attention.) */
+int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
+                          const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                          llama_stream_t stream);
+
+/* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
+ * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.
+ * *detail (may be NULL) receives the code of the first place that reported. */
+int llama_get_device_error(llama_stream_t stream, int* detail);
+
+/* Human-readable name of a status code (static string). */
+const char* llama_status_string(int status);
+
+/* Number of streaming multiprocessors of the current device (cached). */
+int llama_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_LAYER_H_ */

@@ -1,0 +1,262 @@
+"""Python binding of the C ABI in ``include/llama_layer.h``.
+
+Argument marshalling only: torch tensors become device pointers, Python ints
+become C ints, and a non-zero status raises :class:`LlamaError`.  Every step
+of the computation runs in the CUDA library; if the library is missing this
+module raises instead of computing anything itself.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+LLAMA_OK = 0
+LLAMA_ERR_ARG = 1
+LLAMA_ERR_UNSUPPORTED = 2
+LLAMA_ERR_CUDA = 3
+LLAMA_ERR_WORKSPACE = 4
+LLAMA_ERR_DEVICE_GUARD = 5
+LLAMA_ERR_TIMEOUT = 6
+
+
+class LlamaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class LlamaLayerConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("intermediate", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rope_scaling", ctypes.c_int),
+                ("rs_factor", ctypes.c_float), ("rs_low_freq_factor", ctypes.c_float),
+                ("rs_high_freq_factor", ctypes.c_float), ("rs_original_max_pos", ctypes.c_int),
+                ("hidden_act", ctypes.c_int)]
+
+
+class LlamaLayerWeights(ctypes.Structure):
+    _fields_ = [("ln1_w", ctypes.c_void_p), ("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("ln2_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+class LlamaBatch(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_query_len", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+                ("positions", ctypes.c_void_p), ("query_start_loc", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p)]
+
+
+# every entry point of include/llama_layer.h with its C signature
+_VP, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+_P_CFG, _P_W, _P_B = ctypes.POINTER(LlamaLayerConfig), ctypes.POINTER(LlamaLayerWeights), ctypes.POINTER(LlamaBatch)
+SIGNATURES = {
+    "llama_workspace_size": (_SZ, [_P_CFG, _I, _I, _I, _I]),
+    "llama_layer_forward": (_I, [_P_CFG, _P_W, _P_B, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "llama_stack_forward": (_I, [_P_CFG, _I, _P_W, _VP, _VP, _I, _VP, _VP, _P_B, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 _VP, _SZ, _VP]),
+    "kv_cache_write": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP]),
+    "llama_linear": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _VP, _SZ, _VP]),
+    "llama_linear_workspace_size": (_SZ, []),
+    "llama_fused_add_rmsnorm": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _F, _VP]),
+    "llama_paged_attention": (_I, [_P_CFG, _P_B, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "llama_get_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_int)]),
+    "llama_status_string": (ctypes.c_char_p, [_I]),
+    "llama_num_sms": (_I, []),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m llama_decoder_layer_gb300.build` "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().llama_status_string(int(status)).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _check(status: int, where: str) -> None:
+    if status != LLAMA_OK:
+        raise LlamaError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class LayerConfig:
+    hidden: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    intermediate: int
+    rms_eps: float
+    rope_theta: float
+    rope_scaling: Optional[dict] = None
+    block_size: int = 16
+    hidden_act: str = "silu"
+
+    def c(self) -> LlamaLayerConfig:
+        s = self.rope_scaling or {}
+        return LlamaLayerConfig(
+            self.hidden, self.n_heads, self.n_kv_heads, self.head_dim, self.intermediate, self.block_size,
+            self.rms_eps, self.rope_theta, 1 if self.rope_scaling else 0, float(s.get("factor", 1.0)),
+            float(s.get("low_freq_factor", 1.0)), float(s.get("high_freq_factor", 1.0)),
+            int(s.get("original_max_position_embeddings", 0)), 0 if self.hidden_act == "silu" else 1)
+
+    @staticmethod
+    def from_spec(spec) -> "LayerConfig":
+        return LayerConfig(spec.hidden, spec.n_heads, spec.n_kv_heads, spec.head_dim, spec.intermediate,
+                           spec.rms_eps, spec.rope_theta, spec.rope_scaling, spec.block_size)
+
+
+def make_weights(w: dict) -> LlamaLayerWeights:
+    return LlamaLayerWeights(_ptr(w["ln1"]), _ptr(w["w_qkv"]), _ptr(w["w_o"]), _ptr(w["ln2"]),
+                             _ptr(w["w_gate_up"]), _ptr(w["w_down"]))
+
+
+@dataclass
+class Batch:
+    """Device metadata of one flat batch plus the host bounds the launches need."""
+
+    positions: torch.Tensor
+    query_start_loc: torch.Tensor
+    seq_lens: torch.Tensor
+    block_table: torch.Tensor
+    num_blocks: int
+    max_query_len: int
+    max_seq_len: int
+    slot_mapping: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def from_layout(bl, slot_mapping=None) -> "Batch":
+        seq_lens = [c + q for c, q in zip(bl.ctx_lens, bl.q_lens)]
+        return Batch(bl.positions, bl.query_start_loc, bl.seq_lens, bl.block_table, bl.num_blocks,
+                     max(bl.q_lens), max(seq_lens), slot_mapping)
+
+    def c(self) -> LlamaBatch:
+        T = int(self.positions.numel())
+        B = int(self.seq_lens.numel())
+        return LlamaBatch(T, B, int(self.block_table.shape[1]), int(self.num_blocks), int(self.max_query_len),
+                          int(self.max_seq_len), _ptr(self.positions), _ptr(self.query_start_loc),
+                          _ptr(self.seq_lens), _ptr(self.block_table), _ptr(self.slot_mapping))
+
+
+def workspace_size(cfg: LayerConfig, max_tokens: int, max_seqs: int, max_seq_len: int, vocab: int = 0) -> int:
+    c = cfg.c()
+    n = lib().llama_workspace_size(ctypes.byref(c), max_tokens, max_seqs, max_seq_len, vocab)
+    if n == 0:
+        raise LlamaError(LLAMA_ERR_ARG, "llama_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def layer_forward(cfg: LayerConfig, weights: dict, batch: Batch, hidden: torch.Tensor,
+                  residual_in: Optional[torch.Tensor], residual_out: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    c, w, b = cfg.c(), make_weights(weights), batch.c()
+    st = lib().llama_layer_forward(ctypes.byref(c), ctypes.byref(w), ctypes.byref(b), _ptr(hidden),
+                                   _ptr(residual_in), _ptr(residual_out), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llama_layer_forward")
+
+
+def stack_forward(cfg: LayerConfig, layers: Sequence[dict], final_norm: torch.Tensor, lm_head: torch.Tensor,
+                  batch: Batch, hidden: torch.Tensor, residual: torch.Tensor, k_caches: Sequence[torch.Tensor],
+                  v_caches: Sequence[torch.Tensor], out_tokens: torch.Tensor, workspace: torch.Tensor,
+                  embed: Optional[torch.Tensor] = None, input_ids: Optional[torch.Tensor] = None,
+                  out_logits: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = len(layers)
+    c, b = cfg.c(), batch.c()
+    ws_arr = (LlamaLayerWeights * n)(*[make_weights(w) for w in layers])
+    kc = (ctypes.c_void_p * n)(*[_ptr(t) for t in k_caches])
+    vc = (ctypes.c_void_p * n)(*[_ptr(t) for t in v_caches])
+    st = lib().llama_stack_forward(ctypes.byref(c), n, ws_arr, _ptr(final_norm), _ptr(lm_head),
+                                   int(lm_head.shape[0]), _ptr(embed), _ptr(input_ids), ctypes.byref(b),
+                                   _ptr(hidden), _ptr(residual), kc, vc, _ptr(out_tokens), _ptr(out_logits),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llama_stack_forward")
+
+
+def kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, block_size: int = 16, stream=None) -> None:
+    T, nkv, d = k.shape
+    st = lib().kv_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, nkv, d, block_size, int(k_cache.shape[0]),
+                              _ptr(k_cache), _ptr(v_cache), _stream(stream))
+    _check(st, "kv_cache_write")
+
+
+def linear(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    M, K = x.shape
+    N = w.shape[0]
+    st = lib().llama_linear(_ptr(x), _ptr(w), M, N, K, _ptr(out), 1 if out.dtype == torch.float32 else 0,
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llama_linear")
+
+
+def linear_workspace_size() -> int:
+    return int(lib().llama_linear_workspace_size())
+
+
+def fused_add_rmsnorm(x, residual_in, residual_out, h, gamma, eps: float, stream=None) -> None:
+    rows, H = x.shape
+    st = lib().llama_fused_add_rmsnorm(_ptr(x), _ptr(residual_in), _ptr(residual_out), _ptr(h), _ptr(gamma), rows, H,
+                                       float(eps), _stream(stream))
+    _check(st, "llama_fused_add_rmsnorm")
+
+
+def paged_attention(cfg: LayerConfig, batch: Batch, q, k_cache, v_cache, out, workspace, stream=None) -> None:
+    c, b = cfg.c(), batch.c()
+    st = lib().llama_paged_attention(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llama_paged_attention")
+
+
+def get_device_error(stream=None):
+    """(status, detail) of the device error word; synchronises and clears it."""
+    d = ctypes.c_int(0)
+    st = lib().llama_get_device_error(_stream(stream), ctypes.byref(d))
+    return st, d.value
+
+
+def num_sms() -> int:
+    return int(lib().llama_num_sms())

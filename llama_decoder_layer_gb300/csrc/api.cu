@@ -1,0 +1,495 @@
+// C ABI of the library (declared in include/llama_layer.h): argument checks,
+// workspace layout and the launch sequence of a layer and of a stack.
+//
+// Layer sequence ([CODE-READING] "vLLM Llama 代码解析" §3-§5, [LLAMA-70B]
+// "LLama — DeepSeek-R1-Distill-Llama-70B" §3-§4 and LlamaMLP):
+//   slot map -> input fused add+RMSNorm -> qkv GEMM (+RoPE, +cache scatter)
+//   -> paged attention -> o_proj GEMM -> post-attention fused add+RMSNorm
+//   -> gate_up GEMM (+SiluAndMul) -> down GEMM
+// Stack ([CODE-READING] §2.1, [WALKTHROUGH] "模型库与算子层 — 代码走读" LlamaModel):
+//   embedding gather -> layers with the residual threaded (None at layer 0)
+//   -> final fused add+RMSNorm of each sequence's last token -> lm_head GEMM
+//   -> argmax.
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "llama_layer.h"
+
+namespace llama {
+
+__device__ int g_device_error[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+  return d;
+}
+
+int* device_error_word() {
+  static int* ptr[kMaxDevices] = {};
+  static std::mutex mu;
+  const int d = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) ptr[d] = static_cast<int*>(p);
+  }
+  return ptr[d];
+}
+
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int check_cfg(const LlamaLayerConfig* c) {
+  if (c == nullptr) return LLAMA_ERR_ARG;
+  if (c->hidden_act != 0) return LLAMA_ERR_ARG;  // only silu
+  if (c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->intermediate <= 0)
+    return LLAMA_ERR_ARG;
+  if (c->n_heads % c->n_kv_heads != 0) return LLAMA_ERR_ARG;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_ARG;
+  if (c->rope_scaling != 0 && c->rope_scaling != 1) return LLAMA_ERR_ARG;
+  if (c->rope_scaling == 1 &&
+      (!(c->rs_factor > 0.f) || !(c->rs_high_freq_factor > c->rs_low_freq_factor) || c->rs_original_max_pos <= 0 ||
+       !(c->rs_low_freq_factor > 0.f)))
+    return LLAMA_ERR_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return LLAMA_ERR_UNSUPPORTED;
+  if (c->n_heads / c->n_kv_heads > 16) return LLAMA_ERR_UNSUPPORTED;
+  if (c->block_size != 16) return LLAMA_ERR_UNSUPPORTED;
+  if (c->hidden % 8 || c->intermediate % 8 || c->hidden > 16384) return LLAMA_ERR_UNSUPPORTED;
+  return LLAMA_OK;
+}
+
+int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
+  if (b == nullptr) return LLAMA_ERR_ARG;
+  if (b->num_tokens < 0 || b->num_seqs < 0) return LLAMA_ERR_ARG;
+  if (b->num_tokens == 0) return LLAMA_OK;
+  if (b->num_seqs < 1 || b->num_seqs > b->num_tokens) return LLAMA_ERR_ARG;
+  if (!b->positions || !b->query_start_loc || !b->seq_lens || !b->block_table) return LLAMA_ERR_ARG;
+  if (b->max_blocks_per_seq < 1 || b->num_blocks < 1 || b->max_query_len < 1 || b->max_seq_len < 1)
+    return LLAMA_ERR_ARG;
+  if (b->max_query_len > b->num_tokens || b->max_query_len > b->max_seq_len) return LLAMA_ERR_ARG;
+  // cache rows and slots are 32-bit on the device
+  if (static_cast<long long>(b->num_blocks) * c->n_kv_heads * c->block_size > 0x7fffffffLL) return LLAMA_ERR_ARG;
+  if (static_cast<long long>(b->num_seqs) * b->max_blocks_per_seq > 0x7fffffffLL) return LLAMA_ERR_ARG;
+  if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // grid z dimension
+  return LLAMA_OK;
+}
+
+struct Layout {
+  size_t slots, h, q, o, a, gpart, apart, hf, logits, total;
+  size_t gpart_bytes, apart_bytes;
+};
+
+Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int vocab) {
+  Layout L{};
+  const size_t t = T > 0 ? T : 0;
+  const size_t qsz = static_cast<size_t>(c.n_heads) * c.head_dim;
+  size_t off = 0;
+  L.slots = off;
+  off += align256(t * 4);
+  L.h = off;
+  off += align256(t * c.hidden * 2);
+  L.q = off;
+  off += align256(t * qsz * 2);
+  L.o = off;
+  off += align256(t * qsz * 2);
+  L.a = off;
+  off += align256(t * c.intermediate * 2);
+  L.gpart = off;
+  L.gpart_bytes = gemm_partials_bytes(num_sms());
+  off += align256(L.gpart_bytes);
+  L.apart = off;
+  L.apart_bytes = attn_partials_bytes(B > 0 ? B : 1, max_seq_len > 0 ? max_seq_len : 1, c.n_heads, c.head_dim);
+  off += align256(L.apart_bytes);
+  if (vocab > 0) {
+    L.hf = off;
+    off += align256(static_cast<size_t>(B) * c.hidden * 2);
+    L.logits = off;
+    off += align256(static_cast<size_t>(B) * vocab * 4);
+  }
+  L.total = off + 256;  // slack for aligning the caller's base pointer
+  return L;
+}
+
+uint8_t* ws_base(void* ws) {
+  const uintptr_t p = reinterpret_cast<uintptr_t>(ws);
+  return reinterpret_cast<uint8_t*>((p + 255) & ~static_cast<uintptr_t>(255));
+}
+
+RopeParams rope_of(const LlamaLayerConfig& c) {
+  RopeParams r{};
+  r.theta = c.rope_theta;
+  r.llama3 = c.rope_scaling;
+  r.factor = c.rs_factor;
+  r.low_freq_factor = c.rs_low_freq_factor;
+  r.high_freq_factor = c.rs_high_freq_factor;
+  r.original_max_pos = c.rs_original_max_pos;
+  return r;
+}
+
+int cuda_status(int e) { return e == 0 ? LLAMA_OK : LLAMA_ERR_CUDA; }
+
+int check_weights(const LlamaLayerWeights* w) {
+  if (w == nullptr) return LLAMA_ERR_ARG;
+  const void* ps[6] = {w->ln1_w, w->w_qkv, w->w_o, w->ln2_w, w->w_gate_up, w->w_down};
+  for (const void* p : ps) {
+    if (p == nullptr) return LLAMA_ERR_ARG;
+    if (!a16(p)) return LLAMA_ERR_UNSUPPORTED;
+  }
+  return LLAMA_OK;
+}
+
+AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q, const void* kc, const void* vc,
+                   void* out, float* part, size_t part_bytes, int* err) {
+  AttnArgs a{};
+  a.q = q;
+  a.k_cache = kc;
+  a.v_cache = vc;
+  a.out = out;
+  a.qsl = b.query_start_loc;
+  a.seq_lens = b.seq_lens;
+  a.positions = b.positions;
+  a.block_table = b.block_table;
+  a.T = b.num_tokens;
+  a.B = b.num_seqs;
+  a.max_blocks = b.max_blocks_per_seq;
+  a.num_blocks = b.num_blocks;
+  a.nq = c.n_heads;
+  a.nkv = c.n_kv_heads;
+  a.head_dim = c.head_dim;
+  a.block_size = c.block_size;
+  a.max_query_len = b.max_query_len;
+  a.max_seq_len = b.max_seq_len;
+  a.partials = part;
+  a.partials_bytes = part_bytes;
+  a.err = err;
+  return a;
+}
+
+int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const LlamaBatch& b, void* hidden,
+               const void* res_in, void* res_out, void* kc, void* vc, uint8_t* ws, const Layout& L, cudaStream_t s) {
+  const int T = b.num_tokens;
+  if (T == 0) return LLAMA_OK;
+  int* err = device_error_word();
+  const int H = c.hidden, I = c.intermediate;
+  const int qsz = c.n_heads * c.head_dim, kvsz = c.n_kv_heads * c.head_dim;
+  int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);
+  auto h = ws + L.h;
+  auto q = ws + L.q;
+  auto o = ws + L.o;
+  auto a = ws + L.a;
+  float* gpart = reinterpret_cast<float*>(ws + L.gpart);
+  float* apart = reinterpret_cast<float*>(ws + L.apart);
+  int e;
+
+  const int32_t* slot_map = b.slot_mapping;
+  if (slot_map == nullptr) {
+    e = slot_mapping_launch(b.positions, b.query_start_loc, b.seq_lens, b.block_table, T, b.num_seqs,
+                            b.max_blocks_per_seq, c.block_size, b.num_blocks, slots, err, s);
+    if (e) return cuda_status(e);
+    slot_map = slots;
+  }
+  // input_layernorm
+  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, s);
+  if (e) return cuda_status(e);
+  // qkv_proj + RoPE + cache update
+  GemmArgs g{};
+  g.epi = kEpiQkv;
+  g.A = h;
+  g.B = w.w_qkv;
+  g.M = T;
+  g.N = qsz + 2 * kvsz;
+  g.K = H;
+  g.out = q;
+  g.ldo = qsz;
+  g.qkv.q_size = qsz;
+  g.qkv.kv_size = kvsz;
+  g.qkv.head_dim = c.head_dim;
+  g.qkv.n_kv_heads = c.n_kv_heads;
+  g.qkv.block_size = c.block_size;
+  g.qkv.num_blocks = b.num_blocks;
+  g.qkv.positions = b.positions;
+  g.qkv.slots = slot_map;
+  g.qkv.k_cache = kc;
+  g.qkv.v_cache = vc;
+  g.qkv.rope = rope_of(c);
+  g.partials = gpart;
+  g.partials_bytes = L.gpart_bytes;
+  g.err = err;
+  g.force_mode = -1;
+  e = gemm_launch(g, s);
+  if (e) return cuda_status(e);
+  // attention
+  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, err), s);
+  if (e) return cuda_status(e);
+  // o_proj -> y (in the h buffer)
+  GemmArgs go{};
+  go.epi = kEpiBf16;
+  go.A = o;
+  go.B = w.w_o;
+  go.M = T;
+  go.N = H;
+  go.K = qsz;
+  go.out = h;
+  go.ldo = H;
+  go.partials = gpart;
+  go.partials_bytes = L.gpart_bytes;
+  go.err = err;
+  go.force_mode = -1;
+  e = gemm_launch(go, s);
+  if (e) return cuda_status(e);
+  // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
+  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, s);
+  if (e) return cuda_status(e);
+  // gate_up_proj + SiluAndMul
+  GemmArgs gu{};
+  gu.epi = kEpiSwiGlu;
+  gu.A = h;
+  gu.B = w.w_gate_up;
+  gu.M = T;
+  gu.N = 2 * I;
+  gu.K = H;
+  gu.out = a;
+  gu.ldo = I;
+  gu.partials = gpart;
+  gu.partials_bytes = L.gpart_bytes;
+  gu.err = err;
+  gu.force_mode = -1;
+  e = gemm_launch(gu, s);
+  if (e) return cuda_status(e);
+  // down_proj -> hidden_states
+  GemmArgs gd{};
+  gd.epi = kEpiBf16;
+  gd.A = a;
+  gd.B = w.w_down;
+  gd.M = T;
+  gd.N = H;
+  gd.K = I;
+  gd.out = hidden;
+  gd.ldo = H;
+  gd.partials = gpart;
+  gd.partials_bytes = L.gpart_bytes;
+  gd.err = err;
+  gd.force_mode = -1;
+  e = gemm_launch(gd, s);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+int num_sms() {
+  static int sms[kMaxDevices] = {};
+  const int d = current_device();
+  if (sms[d] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 1;
+    sms[d] = v;
+  }
+  return sms[d];
+}
+
+}  // namespace llama
+
+using namespace llama;
+
+extern "C" {
+
+size_t llama_workspace_size(const LlamaLayerConfig* cfg, int max_tokens, int max_seqs, int max_seq_len, int vocab) {
+  if (check_cfg(cfg) != LLAMA_OK || max_tokens < 0 || max_seqs < 0 || vocab < 0) return 0;
+  return make_layout(*cfg, max_tokens, max_seqs, max_seq_len, vocab).total;
+}
+
+int llama_layer_forward(const LlamaLayerConfig* cfg, const LlamaLayerWeights* weights, const LlamaBatch* batch,
+                        void* hidden_states, const void* residual_in, void* residual_out, void* k_cache,
+                        void* v_cache, void* workspace, size_t workspace_bytes, llama_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st) return st;
+  if ((st = check_weights(weights))) return st;
+  if ((st = check_batch(batch, cfg))) return st;
+  if (batch->num_tokens == 0) return LLAMA_OK;
+  if (!hidden_states || !residual_out || !k_cache || !v_cache) return LLAMA_ERR_ARG;
+  if (residual_out == hidden_states) return LLAMA_ERR_ARG;
+  if (!a16(hidden_states) || !a16(residual_out) || !a16(k_cache) || !a16(v_cache) ||
+      (residual_in && !a16(residual_in)))
+    return LLAMA_ERR_UNSUPPORTED;
+  const Layout L = make_layout(*cfg, batch->num_tokens, batch->num_seqs, batch->max_seq_len, 0);
+  if (workspace == nullptr || workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
+  return layer_impl(*cfg, *weights, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache,
+                    ws_base(workspace), L, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const LlamaLayerWeights* layers,
+                        const void* final_norm_w, const void* lm_head_w, int vocab, const void* embed_w,
+                        const int32_t* input_ids, const LlamaBatch* batch, void* hidden_states, void* residual,
+                        void* const* k_caches, void* const* v_caches, int32_t* out_tokens, float* out_logits,
+                        void* workspace, size_t workspace_bytes, llama_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st) return st;
+  if (num_layers < 1 || layers == nullptr || k_caches == nullptr || v_caches == nullptr) return LLAMA_ERR_ARG;
+  for (int l = 0; l < num_layers; ++l) {
+    if ((st = check_weights(&layers[l]))) return st;
+    if (!k_caches[l] || !v_caches[l]) return LLAMA_ERR_ARG;
+    if (!a16(k_caches[l]) || !a16(v_caches[l])) return LLAMA_ERR_UNSUPPORTED;
+  }
+  if ((st = check_batch(batch, cfg))) return st;
+  if (!final_norm_w || !lm_head_w || vocab < 1 || !hidden_states || !residual || !out_tokens) return LLAMA_ERR_ARG;
+  if ((embed_w == nullptr) != (input_ids == nullptr)) return LLAMA_ERR_ARG;
+  if (vocab % 8) return LLAMA_ERR_UNSUPPORTED;
+  if (!a16(final_norm_w) || !a16(lm_head_w) || !a16(hidden_states) || !a16(residual) ||
+      (embed_w && !a16(embed_w)) || (out_logits && !a16(out_logits)))
+    return LLAMA_ERR_UNSUPPORTED;
+  if (batch->num_tokens == 0) return LLAMA_OK;
+  const Layout L = make_layout(*cfg, batch->num_tokens, batch->num_seqs, batch->max_seq_len, vocab);
+  if (workspace == nullptr || workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = ws_base(workspace);
+  int* err = device_error_word();
+  const int T = batch->num_tokens, B = batch->num_seqs, H = cfg->hidden;
+  int e;
+  if (embed_w) {
+    e = embed_launch(embed_w, input_ids, T, H, vocab, hidden_states, err, s);
+    if (e) return LLAMA_ERR_CUDA;
+  }
+  for (int l = 0; l < num_layers; ++l) {
+    st = layer_impl(*cfg, layers[l], *batch, hidden_states, l == 0 ? nullptr : residual, residual, k_caches[l],
+                    v_caches[l], ws, L, s);
+    if (st) return st;
+  }
+  // final norm over the last token of every sequence
+  void* hf = ws + L.hf;
+  e = add_rmsnorm_launch(hidden_states, residual, nullptr, hf, final_norm_w, B, H, cfg->rms_eps,
+                         batch->query_start_loc, s);
+  if (e) return LLAMA_ERR_CUDA;
+  float* logits = out_logits ? out_logits : reinterpret_cast<float*>(ws + L.logits);
+  GemmArgs g{};
+  g.epi = kEpiF32;
+  g.A = hf;
+  g.B = lm_head_w;
+  g.M = B;
+  g.N = vocab;
+  g.K = H;
+  g.out = logits;
+  g.ldo = vocab;
+  g.partials = reinterpret_cast<float*>(ws + L.gpart);
+  g.partials_bytes = L.gpart_bytes;
+  g.err = err;
+  g.force_mode = -1;
+  e = gemm_launch(g, s);
+  if (e) return LLAMA_ERR_CUDA;
+  e = argmax_launch(logits, B, vocab, out_tokens, s);
+  return e ? LLAMA_ERR_CUDA : LLAMA_OK;
+}
+
+int kv_cache_write(const void* k, const void* v, const int32_t* slot_mapping, int num_tokens, int n_kv_heads,
+                   int head_dim, int block_size, int num_blocks, void* k_cache, void* v_cache, llama_stream_t stream) {
+  if (num_tokens < 0 || n_kv_heads < 1 || head_dim < 8 || head_dim % 8 || block_size < 1 || num_blocks < 1)
+    return LLAMA_ERR_ARG;
+  if (num_tokens == 0) return LLAMA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return LLAMA_ERR_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return LLAMA_ERR_ARG;
+  if (!a16(k) || !a16(v) || !a16(k_cache) || !a16(v_cache)) return LLAMA_ERR_UNSUPPORTED;
+  const int e = kv_write_launch(k, v, slot_mapping, num_tokens, n_kv_heads, head_dim, block_size, num_blocks, k_cache,
+                                v_cache, device_error_word(), reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+size_t llama_linear_workspace_size(void) { return gemm_partials_bytes(num_sms()) + 256; }
+
+int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int out_fp32, void* workspace,
+                 size_t workspace_bytes, llama_stream_t stream) {
+  if (M < 0 || N < 1 || K < 1) return LLAMA_ERR_ARG;
+  if (M == 0) return LLAMA_OK;
+  if (!x || !w || !y) return LLAMA_ERR_ARG;
+  if (N % 8 || K % 8) return LLAMA_ERR_UNSUPPORTED;
+  if (!a16(x) || !a16(w) || !a16(y)) return LLAMA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < llama_linear_workspace_size()) return LLAMA_ERR_WORKSPACE;
+  GemmArgs g{};
+  g.epi = out_fp32 ? kEpiF32 : kEpiBf16;
+  g.A = x;
+  g.B = w;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = y;
+  g.ldo = N;
+  g.partials = reinterpret_cast<float*>(ws_base(workspace));
+  g.partials_bytes = gemm_partials_bytes(num_sms());
+  g.err = device_error_word();
+  g.force_mode = -1;
+  return cuda_status(gemm_launch(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residual_out, void* h, const void* gamma,
+                            int rows, int H, float eps, llama_stream_t stream) {
+  if (rows < 0 || H < 8 || H % 8 || H > 16384 || !(eps >= 0.f)) return LLAMA_ERR_ARG;
+  if (rows == 0) return LLAMA_OK;
+  if (!x || !h || !gamma) return LLAMA_ERR_ARG;
+  if (!a16(x) || !a16(h) || !a16(gamma) || (residual_in && !a16(residual_in)) ||
+      (residual_out && !a16(residual_out)))
+    return LLAMA_ERR_UNSUPPORTED;
+  return cuda_status(add_rmsnorm_launch(x, residual_in, residual_out, h, gamma, rows, H, eps, nullptr,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
+                          const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                          llama_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st) return st;
+  if ((st = check_batch(batch, cfg))) return st;
+  if (batch->num_tokens == 0) return LLAMA_OK;
+  if (!q || !k_cache || !v_cache || !out) return LLAMA_ERR_ARG;
+  if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return LLAMA_ERR_UNSUPPORTED;
+  const size_t need = attn_partials_bytes(batch->num_seqs, batch->max_seq_len, cfg->n_heads, cfg->head_dim) + 256;
+  if (workspace == nullptr || workspace_bytes < need) return LLAMA_ERR_WORKSPACE;
+  AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws_base(workspace)),
+                         need - 256, device_error_word());
+  return cuda_status(attention_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int llama_get_device_error(llama_stream_t stream, int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LLAMA_ERR_CUDA;
+  int* w = device_error_word();
+  if (w == nullptr) return LLAMA_ERR_CUDA;
+  int host[2] = {0, 0};
+  if (cudaMemcpy(host, w, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (cudaMemset(w, 0, sizeof(host)) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (detail) *detail = host[1];
+  if (host[0] & kErrTimeout) return LLAMA_ERR_TIMEOUT;
+  if (host[0] & kErrGuard) return LLAMA_ERR_DEVICE_GUARD;
+  return LLAMA_OK;
+}
+
+const char* llama_status_string(int status) {
+  switch (status) {
+    case LLAMA_OK:
+      return "ok";
+    case LLAMA_ERR_ARG:
+      return "invalid argument";
+    case LLAMA_ERR_UNSUPPORTED:
+      return "unsupported shape or alignment";
+    case LLAMA_ERR_CUDA:
+      return "CUDA error";
+    case LLAMA_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case LLAMA_ERR_DEVICE_GUARD:
+      return "device guard: an index was out of range";
+    case LLAMA_ERR_TIMEOUT:
+      return "device wait timed out";
+    default:
+      return "unknown status";
+  }
+}
+
+int llama_num_sms(void) { return num_sms(); }
+
+}  // extern "C"

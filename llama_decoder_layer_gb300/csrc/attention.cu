@@ -1,0 +1,702 @@
+// Paged, causal, grouped-query attention over the block-paged KV cache.
+//
+//   o[t, h] = sum_j softmax_j(q[t, h] . K[b, h / g, j] / sqrt(d)) V[b, h / g, j],
+//   j = 0 .. position(t)  (the current tokens are already in the cache)
+//
+// The q heads sharing one KV head (g = n_heads / n_kv_heads of them) are
+// processed together, so every K/V block is loaded from memory once per group.
+// K/V blocks (16 tokens x head_dim of one KV head, contiguous in the cache) are
+// fetched by TMA with 128-byte swizzle and consumed with ldmatrix + mma.sync
+// (bf16 in, fp32 accumulate); softmax is online, in the exp2 domain.
+//
+// * decode (query length 1): split-KV.  One CTA per (sequence, KV head, chunk
+//   of the context); its 4 warps stream disjoint blocks of the chunk through
+//   their own 3-stage TMA rings with the group's q heads as the 16 MMA rows,
+//   merge in shared memory, and either write the output (one chunk) or a
+//   partial (unnormalised o, running max, sum) that k_attn_combine merges.
+// * prefill (query length >= 2): one CTA per (sequence, KV head, 16 query
+//   tokens); warp w owns q head w of the group; a producer warp streams
+//   64-key K/V tiles through a 2-stage ring; fully masked tiles are skipped.
+//
+// Sources: [WALKTHROUGH] "模型库与算子层 — 代码走读", Attention
+// (attn_backend.forward(q, k, v, kv_cache.block_table) after _update_kv_cache);
+// [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", config.json and §4
+// (grouped-query attention, 64 q heads over 8 kv heads).
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace llama {
+
+namespace {
+
+constexpr int kBS = 16;             // tokens per cache block
+constexpr int kDecWarps = 4;
+constexpr int kDecStages = 3;
+constexpr int kChunkBlocks = 32;    // at most 512 keys per split-KV chunk
+constexpr int kPreStages = 2;
+constexpr int kPreKeys = 64;        // keys per prefill K/V tile (4 blocks)
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* positions;
+  const int32_t* block_table;
+  int max_blocks, num_blocks, nq, nkv, group, max_chunks;
+  float scale_log2;
+  float* part_o;
+  float2* part_ml;
+  int* err;
+};
+
+__host__ __device__ constexpr int tile_bytes(int D) { return kBS * D * 2; }
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// zero the bf16 halves of a V fragment register whose key is >= n_keys
+__device__ __forceinline__ uint32_t mask_pair(uint32_t r, int key_lo, int n_keys) {
+  if (key_lo >= n_keys) return 0u;
+  if (key_lo + 1 >= n_keys) return r & 0x0000FFFFu;
+  return r;
+}
+
+// number of context chunks of a decode sequence with nblk cache blocks
+__host__ __device__ __forceinline__ int num_chunks(int nblk) { return (nblk + kChunkBlocks - 1) / kChunkBlocks; }
+
+// Online-softmax update of one 16-key block for the two rows (g, g+8) this
+// thread holds; s[n][c] are scores already scaled to the log2 domain and
+// masked (-inf).  Returns the P fragment as an m16k16 A operand.
+__device__ __forceinline__ void softmax_block(float (&s)[2][4], float& m0, float& m1, float& l0, float& l1,
+                                              float& alpha0, float& alpha1, uint32_t (&pa)[4]) {
+  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx0 = quad_max(mx0);
+  mx1 = quad_max(mx1);
+  const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+  const float b0 = n0 == -INFINITY ? 0.f : n0;
+  const float b1 = n1 == -INFINITY ? 0.f : n1;
+  alpha0 = exp2f(m0 - b0);
+  alpha1 = exp2f(m1 - b1);
+  m0 = n0;
+  m1 = n1;
+  float p[2][4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    p[n][0] = exp2f(s[n][0] - b0);
+    p[n][1] = exp2f(s[n][1] - b0);
+    p[n][2] = exp2f(s[n][2] - b1);
+    p[n][3] = exp2f(s[n][3] - b1);
+  }
+  l0 = l0 * alpha0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+  l1 = l1 * alpha1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+  pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+  pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+}
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kDecWarps * 32)
+    k_attn_decode(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnParams p) {
+  constexpr int TB = tile_bytes(D);
+  constexpr int QS = (D + 8) * 2;  // padded row stride of the q tile (bytes)
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t ring = raw + pad;                                   // [warp][stage][K | V]
+  uint8_t* qtile = smem + kDecWarps * kDecStages * 2 * TB;           // [16][D + 8] bf16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qtile + 16 * QS);     // [warp][stage]
+
+  const int b = blockIdx.z, kvh = blockIdx.y, chunk = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = p.qsl[b];
+  if (p.qsl[b + 1] - t0 != 1) return;
+  const int pos = p.positions[t0];
+  const int n_keys = pos + 1;
+  if (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) {
+    if (chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+    return;
+  }
+  const int nblk = (n_keys + kBS - 1) / kBS;
+  const int nch = num_chunks(nblk);
+  if (nch > p.max_chunks) {  // context longer than the launch's max_seq_len
+    if (chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+    return;
+  }
+  if (chunk >= nch) return;
+  const int blk0 = chunk * nblk / nch, blk1 = (chunk + 1) * nblk / nch;
+  const int G = p.group;
+
+  // q rows of the group (rows >= G are zero padding)
+  for (int i = threadIdx.x; i < 16 * (D / 8); i += blockDim.x) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < G) v = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(t0) * p.nq + kvh * G + r) * D)[c];
+    *reinterpret_cast<uint4*>(qtile + r * QS + c * 16) = v;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(smem_u32(bars + i), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // A fragments of q for all head_dim/16 k-steps
+  uint32_t qa[D / 16][4];
+  {
+    const int m = lane >> 3;
+    const int row = (m & 1) * 8 + (lane & 7);
+    const uint32_t base = smem_u32(qtile) + row * QS + (m >> 1) * 16;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) ldsm_x4(base + kk * 32, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  }
+
+  const int nb_w = blk0 + warp < blk1 ? (blk1 - blk0 - warp + kDecWarps - 1) / kDecWarps : 0;
+  const uint32_t wring = ring + warp * kDecStages * 2 * TB;
+  const uint32_t wbar = smem_u32(bars + warp * kDecStages);
+  const uint64_t pol = policy_evict_first();
+  const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+
+  auto issue = [&](int i) {
+    const int jb = blk0 + warp + kDecWarps * i;
+    int blk = bt[jb];
+    if (blk < 0 || blk >= p.num_blocks) {
+      report_error(p.err, kErrGuard, kWhereBlockTable);
+      blk = 0;
+    }
+    const int row = (blk * p.nkv + kvh) * kBS;
+    const int st = i % kDecStages;
+    const uint32_t dst = wring + st * 2 * TB;
+    const uint32_t bar = wbar + 8 * st;
+    mbar_arrive_expect_tx(bar, 2 * TB);
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx) {
+      tma_load_2d(dst + bx * 2048, &tmK, bar, bx * 64, row, pol);
+      tma_load_2d(dst + TB + bx * 2048, &tmV, bar, bx * 64, row, pol);
+    }
+  };
+
+  if (lane == 0)
+    for (int i = 0; i < kDecStages && i < nb_w; ++i) issue(i);
+  __syncwarp();
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool ok = true;
+  int done = 0;
+
+  for (int i = 0; i < nb_w; ++i) {
+    const int st = i % kDecStages;
+    if (!mbar_wait(wbar + 8 * st, (i / kDecStages) & 1, nullptr)) {
+      ok = false;
+      break;
+    }
+    done = i + 1;
+    const uint32_t kt = wring + st * 2 * TB;
+    const uint32_t vt = kt + TB;
+    const int key0 = (blk0 + warp + kDecWarps * i) * kBS;
+
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int krow = (lane >> 4) * 8 + (lane & 7);
+      const int csel = (lane >> 3) & 1;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int ch = 2 * kk + csel;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(kt + (ch >> 3) * 2048 + sw128_offset(krow, ch & 7), r0, r1, r2, r3);
+        mma_bf16_16816(s[0], qa[kk], r0, r1);
+        mma_bf16_16816(s[1], qa[kk], r2, r3);
+      }
+    }
+    const int kq = key0 + 2 * (lane & 3);
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = kq + n * 8 + (c & 1);
+        s[n][c] = key < n_keys ? s[n][c] * p.scale_log2 : -INFINITY;
+      }
+    float a0, a1;
+    uint32_t pa[4];
+    softmax_block(s, m0, m1, l0, l1, a0, a1, pa);
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= a0;
+      o[n][1] *= a0;
+      o[n][2] *= a1;
+      o[n][3] *= a1;
+    }
+    {
+      const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+      const int csel = lane >> 4;
+      const bool tail = key0 + kBS > n_keys;
+#pragma unroll
+      for (int nd = 0; nd < D / 16; ++nd) {
+        const int ch = 2 * nd + csel;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vt + (ch >> 3) * 2048 + sw128_offset(vrow, ch & 7), r0, r1, r2, r3);
+        if (tail) {
+          r0 = mask_pair(r0, kq, n_keys);
+          r1 = mask_pair(r1, kq + 8, n_keys);
+          r2 = mask_pair(r2, kq, n_keys);
+          r3 = mask_pair(r3, kq + 8, n_keys);
+        }
+        mma_bf16_16816(o[2 * nd], pa, r0, r1);
+        mma_bf16_16816(o[2 * nd + 1], pa, r2, r3);
+      }
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (lane == 0 && i + kDecStages < nb_w) issue(i + kDecStages);
+    __syncwarp();
+  }
+  if (!ok) {
+    if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnDecode);
+    // let the loads still in flight land before the shared memory is reused
+    for (int i = done; i < nb_w && i < done + kDecStages; ++i)
+      mbar_wait(wbar + 8 * (i % kDecStages), (i / kDecStages) & 1, nullptr);
+  }
+  l0 = quad_sum(l0);
+  l1 = quad_sum(l1);
+
+  // merge the warps' partial softmax states in shared memory (ring reused)
+  __syncthreads();
+  float* mbuf = reinterpret_cast<float*>(smem);           // [warp][16]
+  float* lbuf = mbuf + kDecWarps * 16;                     // [warp][16]
+  float* obuf = lbuf + kDecWarps * 16;                     // [warp][16][D]
+  {
+    const int g = lane >> 2;
+    if ((lane & 3) == 0) {
+      mbuf[warp * 16 + g] = ok ? m0 : -INFINITY;
+      mbuf[warp * 16 + g + 8] = ok ? m1 : -INFINITY;
+      lbuf[warp * 16 + g] = l0;
+      lbuf[warp * 16 + g + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int col = n * 8 + 2 * (lane & 3);
+      obuf[(warp * 16 + g) * D + col] = o[n][0];
+      obuf[(warp * 16 + g) * D + col + 1] = o[n][1];
+      obuf[(warp * 16 + g + 8) * D + col] = o[n][2];
+      obuf[(warp * 16 + g + 8) * D + col + 1] = o[n][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int r = idx / D, col = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mbuf[w * 16 + r]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float f = exp2f(mbuf[w * 16 + r] - M);
+        L += lbuf[w * 16 + r] * f;
+        O += obuf[(w * 16 + r) * D + col] * f;
+      }
+    }
+    const int h = kvh * G + r;
+    if (nch == 1) {
+      p.out[static_cast<size_t>(t0) * p.nq * D + h * D + col] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    } else {
+      const size_t pi = (static_cast<size_t>(b) * p.max_chunks + chunk) * p.nq + h;
+      p.part_o[pi * D + col] = O;
+      if (col == 0) p.part_ml[pi] = make_float2(M, L);
+    }
+  }
+}
+
+template <int D>
+__global__ void k_attn_combine(AttnParams p) {
+  const int b = blockIdx.y, h = blockIdx.x, col = threadIdx.x;
+  const int t0 = p.qsl[b];
+  if (p.qsl[b + 1] - t0 != 1) return;
+  const int pos = p.positions[t0];
+  const int n_keys = pos + 1;
+  if (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) return;
+  const int nch = num_chunks((n_keys + kBS - 1) / kBS);
+  if (nch <= 1 || nch > p.max_chunks) return;
+  const size_t base = static_cast<size_t>(b) * p.max_chunks * p.nq + h;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(c) * p.nq].x);
+  float L = 0.f, O = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < nch; ++c) {
+      const size_t pi = base + static_cast<size_t>(c) * p.nq;
+      const float2 ml = p.part_ml[pi];
+      const float f = exp2f(ml.x - M);
+      L += ml.y * f;
+      O += p.part_o[pi * D + col] * f;
+    }
+  }
+  p.out[static_cast<size_t>(t0) * p.nq * D + h * D + col] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// prefill
+// ---------------------------------------------------------------------------
+constexpr int kPreMaxHeads = 8;  // q heads (consumer warps) per prefill CTA
+
+template <int D>
+__global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
+    k_attn_prefill(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnParams p) {
+  constexpr int TB = tile_bytes(D);      // one 16-key block of K (or V)
+  constexpr int STB = 4 * TB;            // 64 keys
+  constexpr int QS = (D + 8) * 2;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t ring = raw + pad;                               // [stage][K 64 keys | V 64 keys]
+  uint8_t* qtiles = smem + kPreStages * 2 * STB;                 // [warp][16][D + 8]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qtiles + kPreMaxHeads * 16 * QS);  // full[S], empty[S]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kPreStages);
+
+  const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;  // head chunks per KV head
+  const int b = blockIdx.z, kvh = blockIdx.y / n_hc, hc = blockIdx.y % n_hc;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = min(kPreMaxHeads, p.group - hc * kPreMaxHeads);  // q heads of this CTA
+  const int h_first = kvh * p.group + hc * kPreMaxHeads;
+  if (warp > G) return;
+  const int t0 = p.qsl[b];
+  const int qlen = p.qsl[b + 1] - t0;
+  if (qlen < 2) return;
+  if ((qlen + 15) / 16 > static_cast<int>(gridDim.x)) {  // longer than the launch's max_query_len
+    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+    return;
+  }
+  if (qt * 16 >= qlen) return;
+  const int tq = t0 + qt * 16;              // first token of this q tile
+  const int nrows = min(16, qlen - qt * 16);
+
+  // largest position of the tile (keys needed: 0 .. p_hi)
+  int p_hi = -1;
+  for (int r = 0; r < nrows; ++r) p_hi = max(p_hi, p.positions[tq + r]);
+  const int n_keys = p_hi + 1;
+  if (n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) {
+    if (kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+    return;
+  }
+  const int ntiles = (n_keys + kPreKeys - 1) / kPreKeys;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kPreStages;
+
+  if (warp < G) {
+    uint8_t* qs = qtiles + warp * 16 * QS;
+    const int h = h_first + warp;
+    for (int i = lane; i < 16 * (D / 8); i += 32) {
+      const int r = i / (D / 8), c = i % (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < nrows) v = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(tq + r) * p.nq + h) * D)[c];
+      *reinterpret_cast<uint4*>(qs + r * QS + c * 16) = v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPreStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, G);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == G) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+      const int nblk = (n_keys + kBS - 1) / kBS;
+      uint32_t uses[kPreStages] = {};
+      bool ok = true;
+      for (int kt = 0; kt < ntiles && ok; ++kt) {
+        const int st = kt % kPreStages;
+        if (!mbar_wait(empty0 + 8 * st, ((kt / kPreStages) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        int nload = min(4, nblk - kt * 4);
+        mbar_arrive_expect_tx(full0 + 8 * st, nload * 2 * TB);
+        for (int i = 0; i < nload; ++i) {
+          int blk = bt[kt * 4 + i];
+          if (blk < 0 || blk >= p.num_blocks) {
+            report_error(p.err, kErrGuard, kWhereBlockTable);
+            blk = 0;
+          }
+          const int row = (blk * p.nkv + kvh) * kBS;
+          const uint32_t dst = ring + st * 2 * STB + i * TB;
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx) {
+            tma_load_2d(dst + bx * 2048, &tmK, full0 + 8 * st, bx * 64, row, pol);
+            tma_load_2d(dst + STB + bx * 2048, &tmV, full0 + 8 * st, bx * 64, row, pol);
+          }
+        }
+        uses[st]++;
+      }
+      if (!ok) {
+        report_error(p.err, kErrTimeout, kWhereAttnPrefill);
+        *abort_flag = 1;
+      }
+      for (int s = 0; s < kPreStages; ++s)
+        if (uses[s] > 0) mbar_wait(full0 + 8 * s, (uses[s] - 1) & 1u, nullptr);
+    }
+    return;
+  }
+  if (warp >= G) return;
+
+  // ---------------- consumer warps: q head kvh*G + warp ----------------
+  uint32_t qa[D / 16][4];
+  {
+    const int m = lane >> 3;
+    const int row = (m & 1) * 8 + (lane & 7);
+    const uint32_t base = smem_u32(qtiles + warp * 16 * QS) + row * QS + (m >> 1) * 16;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) ldsm_x4(base + kk * 32, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  }
+  const int g = lane >> 2;
+  const int pos0 = g < nrows ? p.positions[tq + g] : -1;      // row g
+  const int pos1 = g + 8 < nrows ? p.positions[tq + g + 8] : -1;  // row g + 8
+  int p_lo = p_hi;
+  for (int r = 0; r < nrows; ++r) p_lo = min(p_lo, p.positions[tq + r]);
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool ok = true;
+
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const int st = kt % kPreStages;
+    if (!mbar_wait(full0 + 8 * st, (kt / kPreStages) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const uint32_t ks = ring + st * 2 * STB;
+    const uint32_t vs = ks + STB;
+    const int kbase = kt * kPreKeys;
+    const bool need_mask = kbase + kPreKeys - 1 > p_lo;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      // one 16-key block: S = q K^T, online softmax, O += P V
+      const int key0 = kbase + blk * kBS;
+      if (key0 >= n_keys) break;  // warp-uniform
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int krow = (lane >> 4) * 8 + (lane & 7);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int ch = 2 * kk + csel;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(ks + blk * TB + (ch >> 3) * 2048 + sw128_offset(krow, ch & 7), r0, r1, r2, r3);
+          mma_bf16_16816(s[0], qa[kk], r0, r1);
+          mma_bf16_16816(s[1], qa[kk], r2, r3);
+        }
+      }
+      const int kq = key0 + 2 * (lane & 3);
+      if (need_mask) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int key = kq + n * 8 + (c & 1);
+            const int lim = c < 2 ? pos0 : pos1;
+            s[n][c] = key <= lim ? s[n][c] * p.scale_log2 : -INFINITY;
+          }
+      } else {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) s[n][c] *= p.scale_log2;
+      }
+      float a0, a1;
+      uint32_t pa[4];
+      softmax_block(s, m0, m1, l0, l1, a0, a1, pa);
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
+      const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+      const int csel = lane >> 4;
+      const bool tail = key0 + kBS > n_keys;
+#pragma unroll
+      for (int nd = 0; nd < D / 16; ++nd) {
+        const int ch = 2 * nd + csel;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(vs + blk * TB + (ch >> 3) * 2048 + sw128_offset(vrow, ch & 7), r0, r1, r2, r3);
+        if (tail) {
+          r0 = mask_pair(r0, kq, n_keys);
+          r1 = mask_pair(r1, kq + 8, n_keys);
+          r2 = mask_pair(r2, kq, n_keys);
+          r3 = mask_pair(r3, kq + 8, n_keys);
+        }
+        mma_bf16_16816(o[2 * nd], pa, r0, r1);
+        mma_bf16_16816(o[2 * nd + 1], pa, r2, r3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+  }
+  if (!ok) {
+    if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
+    *abort_flag = 1;
+    return;
+  }
+  l0 = quad_sum(l0);
+  l1 = quad_sum(l1);
+  const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
+  const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int h = h_first + warp;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    const int col = n * 8 + 2 * (lane & 3);
+    if (g < nrows)
+      *reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(tq + g) * p.nq + h) * D + col) =
+          pack_bf16x2(o[n][0] * i0, o[n][1] * i0);
+    if (g + 8 < nrows)
+      *reinterpret_cast<uint32_t*>(p.out + (static_cast<size_t>(tq + g + 8) * p.nq + h) * D + col) =
+          pack_bf16x2(o[n][2] * i1, o[n][3] * i1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// cache [num_blocks * nkv * 16 rows, D] with a 16 x 64 box, 128-byte swizzle
+bool make_cache_tmap(CUtensorMap* m, const void* base, long long rows, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBS)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+size_t decode_smem() {
+  return 1024 + kDecWarps * kDecStages * 2 * tile_bytes(D) + 16 * (D + 8) * 2 + 8 * kDecWarps * kDecStages;
+}
+
+template <int D>
+size_t prefill_smem() {
+  return 1024 + kPreStages * 2 * 4 * tile_bytes(D) + kPreMaxHeads * 16 * (D + 8) * 2 + 8 * 2 * kPreStages + 16;
+}
+
+template <int D>
+int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams& p, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(k_attn_decode<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(decode_smem<D>()));
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(k_attn_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(prefill_smem<D>()));
+  });
+  if (attr != cudaSuccess) return attr;
+  const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
+  p.max_chunks = num_chunks(max_blk);
+  if (p.max_chunks < 1) p.max_chunks = 1;
+  dim3 gd(p.max_chunks, a.nkv, a.B);
+  k_attn_decode<D><<<gd, kDecWarps * 32, decode_smem<D>(), s>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.max_chunks > 1) {
+    k_attn_combine<D><<<dim3(a.nq, a.B), D, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (a.max_query_len >= 2) {
+    const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
+    const int warps = (p.group < kPreMaxHeads ? p.group : kPreMaxHeads) + 1;
+    dim3 gp((a.max_query_len + 15) / 16, a.nkv * n_hc, a.B);
+    k_attn_prefill<D><<<gp, warps * 32, prefill_smem<D>(), s>>>(tk, tv, p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+size_t attn_partials_bytes(int B, int max_seq_len, int nq, int head_dim) {
+  const int nch = num_chunks((max_seq_len + kBS - 1) / kBS);
+  const size_t n = static_cast<size_t>(B) * (nch < 1 ? 1 : nch) * nq;
+  return n * head_dim * sizeof(float) + n * sizeof(float2) + 256;
+}
+
+int attention_launch(const AttnArgs& a, cudaStream_t s) {
+  if (a.T <= 0 || a.B <= 0) return 0;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.nkv * kBS;
+  CUtensorMap tk, tv;
+  if (!make_cache_tmap(&tk, a.k_cache, rows, a.head_dim)) return cudaErrorInvalidValue;
+  if (!make_cache_tmap(&tv, a.v_cache, rows, a.head_dim)) return cudaErrorInvalidValue;
+  AttnParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.qsl = a.qsl;
+  p.seq_lens = a.seq_lens;
+  p.positions = a.positions;
+  p.block_table = a.block_table;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.nq = a.nq;
+  p.nkv = a.nkv;
+  p.group = a.nq / a.nkv;
+  p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.head_dim));
+  p.err = a.err;
+  const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
+  const size_t n = static_cast<size_t>(a.B) * (num_chunks(max_blk) < 1 ? 1 : num_chunks(max_blk)) * a.nq;
+  if (attn_partials_bytes(a.B, a.max_seq_len, a.nq, a.head_dim) > a.partials_bytes) return cudaErrorInvalidValue;
+  p.part_o = a.partials;
+  p.part_ml = reinterpret_cast<float2*>(a.partials + n * a.head_dim);
+  if (a.head_dim == 128) return launch_d<128>(a, tk, tv, p, s);
+  if (a.head_dim == 64) return launch_d<64>(a, tk, tv, p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace llama

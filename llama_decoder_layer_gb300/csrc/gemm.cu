@@ -1,0 +1,667 @@
+// Tensor-core GEMM y = x * W^T for the four projections (and lm_head), on the
+// 5th-generation tensor cores: TMA loads 128-byte-swizzled K-major tiles into
+// a shared-memory ring, one thread issues tcgen05.mma (M=128, N=256, K=16)
+// into a double-buffered fp32 accumulator in tensor memory, and four epilogue
+// warps drain it with tcgen05.ld and apply the fused epilogue:
+//   * plain bf16 store                         (o_proj, down_proj)
+//   * RoPE on q/k + q store + paged K/V scatter (qkv_proj; the cache update
+//     precedes attention, as LlamaAttention.forward does)
+//   * SiluAndMul: silu(x[:d]) * x[d:]          (gate_up_proj; a tile loads 128
+//     gate rows and the matching 128 up rows, so both halves meet in one
+//     thread)
+//   * fp32 store                               (lm_head logits)
+// The kernel is persistent (one CTA per SM).  Large problems are scheduled
+// data-parallel (whole tiles, grouped raster for L2 reuse); problems with few
+// tiles (decode) are split stream-K: every CTA gets an equal share of the
+// (tile, k-block) units, partial tiles go to a workspace and a fixup kernel
+// sums them in a fixed order and applies the same epilogue.
+//
+// Sources: [WALKTHROUGH] "模型库与算子层 — 代码走读", Linear layers (F.linear with
+// Parameter(out, in)); [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", §4
+// LlamaAttention and LlamaMLP (merged qkv / gate_up projections, SiluAndMul);
+// [CODE-READING] "vLLM Llama 代码解析", §4 (RoPE on q and k only).
+#include <cuda.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace llama {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;  // accumulator columns per tile
+constexpr int BK = 64;   // one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2048;  // + barriers, rope table, alignment slack
+
+struct GemmParams {
+  int M, N, K;
+  int tiles_m, tiles_n, kb, tiles;
+  int sk, grid, group_m;
+  long long units;
+  int b_row_step;    // row offset of the second 128-row B box (128, or I for SwiGLU)
+  int b_tile_rows;   // B rows advanced per output tile (256, or 128 for SwiGLU)
+  int b_evict_first;
+  void* out;
+  int ldo, n_out;
+  float* partials;
+  int* err;
+  QkvEpilogueArgs qkv;
+};
+
+struct Work {
+  int tile, kb0, kb1;
+};
+
+__device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor, long long end, Work& w) {
+  if (p.sk) {
+    if (cursor >= end) return false;
+    w.tile = static_cast<int>(cursor / p.kb);
+    w.kb0 = static_cast<int>(cursor % p.kb);
+    long long tile_end = static_cast<long long>(w.tile + 1) * p.kb;
+    long long e = end < tile_end ? end : tile_end;
+    w.kb1 = w.kb0 + static_cast<int>(e - cursor);
+    cursor = e;
+    return true;
+  }
+  if (cursor >= p.tiles) return false;
+  w.tile = static_cast<int>(cursor);
+  w.kb0 = 0;
+  w.kb1 = p.kb;
+  cursor += p.grid;
+  return true;
+}
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& tm, int& tn) {
+  const int group = p.group_m * p.tiles_n;
+  const int g = tile / group;
+  const int first_m = g * p.group_m;
+  int gm = p.tiles_m - first_m;
+  if (gm > p.group_m) gm = p.group_m;
+  const int r = tile - g * group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__host__ __device__ __forceinline__ long long sk_start(long long units, int grid, int c) {
+  return units * c / grid;
+}
+
+// ---------------------------------------------------------------------------
+// RoPE frequency table: per pair i, the rotation rate in revolutions per
+// position, r_i = inv_freq'_i / (2 pi), split into a float pair (hi, lo) so
+// that the angle of a large position can be reduced exactly.
+// inv_freq_i = theta^(-2i/d); llama3: wavelengths shorter than
+// orig/high_freq_factor keep their frequency, longer than orig/low_freq_factor
+// are divided by factor, in between they blend linearly in orig/wavelength.
+// ---------------------------------------------------------------------------
+__device__ void build_rope_table(const RopeParams& rp, int head_dim, float2* tab, int tid, int nthreads) {
+  const int half = head_dim / 2;
+  for (int i = tid; i < half; i += nthreads) {
+    double inv = pow(static_cast<double>(rp.theta), -2.0 * i / head_dim);
+    if (rp.llama3) {
+      const double two_pi = 6.283185307179586476925287;
+      const double lam = two_pi / inv;
+      const double orig = static_cast<double>(rp.original_max_pos);
+      const double lo = rp.low_freq_factor, hi = rp.high_freq_factor, f = rp.factor;
+      if (lam < orig / hi) {
+      } else if (lam > orig / lo) {
+        inv = inv / f;
+      } else {
+        const double s = (orig / lam - lo) / (hi - lo);
+        inv = (1.0 - s) * inv / f + s * inv;
+      }
+    }
+    const double r = inv * 0.15915494309189533576888;  // 1 / (2 pi)
+    const float rh = static_cast<float>(r);
+    const float rl = static_cast<float>(r - static_cast<double>(rh));
+    tab[i] = make_float2(rh, rl);
+  }
+}
+
+// sin/cos of 2*pi*pos*r with r = (hi + lo): the product pos*hi is split into
+// its rounded value and exact error, the integer revolutions are dropped and
+// the remaining fraction goes to sincospif.
+__device__ __forceinline__ void rope_sincos(int pos, float2 r, float& s, float& c) {
+  const float fp = static_cast<float>(pos);
+  const float ph = fp * r.x;
+  const float pe = fmaf(fp, r.x, -ph);
+  const float fr = ph - floorf(ph);
+  const float t = fr + (pe + fp * r.y);
+  sincospif(2.0f * t, &s, &c);
+}
+
+__device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = u;
+  }
+}
+
+// The fused epilogue of one output tile for the row `row` (one thread per
+// row).  `ld(col, v)` returns accumulator columns [col, col+32) of this row; it
+// may be warp-collective, so every call is made under tile-uniform control.
+template <int EPI, class Loader>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int tn, int row_in_tile, Loader& ld,
+                                              const float2* rope_tab) {
+  const int row = tm * BM + row_in_tile;
+  const bool valid = row < p.M;
+  if constexpr (EPI == kEpiBf16 || EPI == kEpiF32) {
+    const int n_base = tn * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n_base + c >= p.n_out) break;  // tile-uniform
+      float v[32];
+      ld(c, v);
+      if (!valid) continue;
+      const int n = n_base + c;
+      if constexpr (EPI == kEpiBf16) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
+        if (n + 32 <= p.n_out) {
+          store_bf16x32(o, v);
+        } else {
+          for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = __float2bfloat16_rn(v[e]);
+        }
+      } else {
+        float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
+        if (n + 32 <= p.n_out) {
+          float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = v[e];
+        }
+      }
+    }
+  } else if constexpr (EPI == kEpiSwiGlu) {
+    const int n_base = tn * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      if (n_base + c >= p.n_out) break;
+      float g[32], u[32];
+      ld(c, g);
+      ld(BN / 2 + c, u);
+      if (!valid) continue;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float sg = g[e] / (1.0f + __expf(-g[e]));
+        g[e] = sg * u[e];
+      }
+      const int n = n_base + c;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
+      if (n + 32 <= p.n_out) {
+        store_bf16x32(o, g);
+      } else {
+        for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = __float2bfloat16_rn(g[e]);
+      }
+    }
+  } else {  // kEpiQkv
+    const QkvEpilogueArgs& q = p.qkv;
+    const int d = q.head_dim;
+    const int half = d >> 1;
+    const int n0 = tn * BN;
+    const int pos = valid ? q.positions[row] : 0;
+    int slot = valid ? q.slots[row] : -1;
+    if (slot >= q.num_blocks * q.block_size) {
+      report_error(p.err, kErrGuard, kWhereSlot);
+      slot = -1;
+    }
+    const int blk = slot >= 0 ? slot / q.block_size : 0;
+    const int off = slot >= 0 ? slot % q.block_size : 0;
+    // rotated heads (q and k): j-chunks outer so sin/cos are shared by the
+    // heads of the tile
+#pragma unroll 1
+    for (int j = 0; j < half; j += 32) {
+      if (n0 >= q.q_size + q.kv_size) break;  // tile holds only v heads
+      float sn[32], cs[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) rope_sincos(pos, rope_tab[j + e], sn[e], cs[e]);
+#pragma unroll 1
+      for (int hc = 0; hc < BN; hc += d) {
+        const int col = n0 + hc;
+        if (col >= q.q_size + q.kv_size) break;
+        float lo[32], hi[32];
+        ld(hc + j, lo);
+        ld(hc + half + j, hi);
+        if (!valid) continue;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x1 = lo[e], x2 = hi[e];
+          lo[e] = x1 * cs[e] - x2 * sn[e];
+          hi[e] = x2 * cs[e] + x1 * sn[e];
+        }
+        if (col < q.q_size) {
+          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + col + j;
+          store_bf16x32(o, lo);
+          store_bf16x32(o + half, hi);
+        } else if (slot >= 0) {
+          const int kh = (col - q.q_size) / d;
+          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.k_cache) +
+                             ((static_cast<size_t>(blk) * q.n_kv_heads + kh) * q.block_size + off) * d + j;
+          store_bf16x32(o, lo);
+          store_bf16x32(o + half, hi);
+        }
+      }
+    }
+    // v heads: plain copy into the cache
+#pragma unroll 1
+    for (int hc = 0; hc < BN; hc += d) {
+      const int col = n0 + hc;
+      if (col >= p.N) break;
+      if (col < q.q_size + q.kv_size) continue;
+      const int vh = (col - q.q_size - q.kv_size) / d;
+#pragma unroll 1
+      for (int j = 0; j < d; j += 32) {
+        float v[32];
+        ld(hc + j, v);
+        if (!valid || slot < 0) continue;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.v_cache) +
+                           ((static_cast<size_t>(blk) * q.n_kv_heads + vh) * q.block_size + off) * d + j;
+        store_bf16x32(o, v);
+      }
+    }
+  }
+}
+
+struct TmemLoader {
+  uint32_t taddr;
+  __device__ __forceinline__ void operator()(int col, float (&v)[32]) const { tmem_ld32(taddr + col, v); }
+};
+
+// Sum of the partial tiles that the CTAs covering part of a split tile left
+// in the workspace, in CTA order.
+struct PartialLoader {
+  const float* partials;
+  long long units, t0, t1;
+  int grid, c_first, row;
+  __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+    for (int c = c_first; c < grid; ++c) {
+      const long long s = sk_start(units, grid, c), e = sk_start(units, grid, c + 1);
+      if (s >= t1) break;
+      if (e <= t0 || s == e) continue;
+      const int slot = s >= t0 ? 0 : 1;
+      const float4* src = reinterpret_cast<const float4*>(partials + (static_cast<size_t>(c) * 2 + slot) * (BM * BN) +
+                                                          static_cast<size_t>(row) * BN + col);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 t = src[q];
+        v[4 * q] += t.x;
+        v[4 * q + 1] += t.y;
+        v[4 * q + 2] += t.z;
+        v[4 * q + 3] += t.w;
+      }
+    }
+  }
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+
+  uint8_t* meta = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* rope_tab = reinterpret_cast<float2*>(meta + 512);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if constexpr (EPI == kEpiQkv) {
+    if (warp >= 2) build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  long long cursor, end;
+  if (p.sk) {
+    cursor = sk_start(p.units, p.grid, blockIdx.x);
+    end = sk_start(p.units, p.grid, blockIdx.x + 1);
+  } else {
+    cursor = blockIdx.x;
+    end = 0;
+  }
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    const uint64_t pol_a = policy_evict_last();
+    const uint64_t pol_b = p.b_evict_first ? policy_evict_first() : policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t uses[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+    Work w;
+    bool ok = true;
+    while (ok && next_work(p, cursor, end, w)) {
+      int tm, tn;
+      tile_coords(p, w.tile, tm, tn);
+      const int arow = tm * BM;
+      const int brow0 = tn * p.b_tile_rows;
+      const int brow1 = brow0 + p.b_row_step;
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
+          tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
+          tma_load_2d(sb + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow1, pol_b);
+        }
+        __syncwarp();
+        uses[stage]++;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmProducer);
+      *abort_flag = 1;
+    }
+    // wait for every load this warp issued to land before the CTA can exit
+    for (int s = 0; s < STAGES; ++s)
+      if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true, issued = false;
+    Work w;
+    while (ok && next_work(p, cursor, end, w)) {
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k), idesc,
+                       (kb > w.kb0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          issued = true;
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(tfull_bar(acc));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmMma);
+      *abort_flag = 1;
+    }
+    // all MMAs this thread issued must finish before tensor memory is freed
+    if (lane == 0 && issued) tc_commit(drain_bar);
+    __syncwarp();
+    if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain_bar, 0, nullptr);
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int quad = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int nseg = 0;
+    Work w;
+    bool ok = true;
+    while (next_work(p, cursor, end, w)) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(p, w.tile, tm, tn);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      if (w.kb0 == 0 && w.kb1 == p.kb) {
+        TmemLoader ld{taddr};
+        epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab);
+      } else {
+        const int slot = nseg == 0 ? 0 : 1;
+        float* dst = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) +
+                     static_cast<size_t>(row_in_tile) * BN;
+        const bool valid = tm * BM + row_in_tile < p.M;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
+        }
+      }
+      ++nseg;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmEpilogue);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// Sums the stream-K partial tiles of every tile that was split across CTAs
+// (fixed CTA order, so the result is deterministic) and applies the epilogue.
+template <int EPI>
+__global__ void __launch_bounds__(128) k_gemm_fixup(GemmParams p) {
+  __shared__ float2 rope_tab[64];
+  const int tile = blockIdx.x;
+  const long long t0 = static_cast<long long>(tile) * p.kb, t1 = t0 + p.kb;
+  // first CTA whose range contains unit t0
+  int c = static_cast<int>((t0 * p.grid) / p.units);
+  while (c + 1 < p.grid && sk_start(p.units, p.grid, c + 1) <= t0) ++c;
+  while (c > 0 && sk_start(p.units, p.grid, c) > t0) --c;
+  if (sk_start(p.units, p.grid, c) <= t0 && sk_start(p.units, p.grid, c + 1) >= t1) return;  // whole tile in one CTA
+  if constexpr (EPI == kEpiQkv) build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x, 128);
+  __syncthreads();
+  PartialLoader ld{p.partials, p.units, t0, t1, p.grid, c, static_cast<int>(threadIdx.x)};
+  int tm, tn;
+  tile_coords(p, tile, tm, tn);
+  epilogue_tile<EPI>(p, tm, tn, threadIdx.x, ld, rope_tab);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous) with a box of box_rows x 64
+// columns and 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI>
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  k_gemm_tc<EPI><<<p.grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.sk) {
+    k_gemm_fixup<EPI><<<p.tiles, 128, 0, s>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+size_t gemm_partials_bytes(int sms) { return static_cast<size_t>(sms) * 2 * BM * BN * sizeof(float); }
+
+int gemm_launch(const GemmArgs& a, cudaStream_t s) {
+  if (a.M <= 0) return 0;
+  GemmParams p{};
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.out = a.out;
+  p.ldo = a.ldo;
+  p.err = a.err;
+  p.qkv = a.qkv;
+  p.partials = a.partials;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.kb = (a.K + BK - 1) / BK;
+  if (a.epi == kEpiSwiGlu) {
+    const int I = a.N / 2;
+    p.tiles_n = (I + BN / 2 - 1) / (BN / 2);
+    p.b_tile_rows = BN / 2;
+    p.b_row_step = I;
+    p.n_out = I;
+  } else {
+    p.tiles_n = (a.N + BN - 1) / BN;
+    p.b_tile_rows = BN;
+    p.b_row_step = BN / 2;
+    p.n_out = a.N;
+  }
+  p.tiles = p.tiles_m * p.tiles_n;
+  p.b_evict_first = p.tiles_m <= 2 ? 1 : 0;
+  p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
+  const int sms = num_sms();
+  bool sk = p.tiles < 2 * sms;
+  if (a.force_mode == 0) sk = false;
+  if (a.force_mode == 1) sk = true;
+  p.units = static_cast<long long>(p.tiles) * p.kb;
+  if (sk) {
+    long long g = p.units < sms ? p.units : sms;
+    if (g < 1) g = 1;
+    p.grid = static_cast<int>(g);
+    if (gemm_partials_bytes(p.grid) > a.partials_bytes || a.partials == nullptr) return cudaErrorInvalidValue;
+  } else {
+    p.grid = p.tiles < sms ? p.tiles : sms;
+  }
+  p.sk = sk ? 1 : 0;
+
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, a.A, a.M, a.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, a.B, a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
+  switch (a.epi) {
+    case kEpiBf16:
+      return launch_typed<kEpiBf16>(ta, tb, p, s);
+    case kEpiQkv:
+      return launch_typed<kEpiQkv>(ta, tb, p, s);
+    case kEpiSwiGlu:
+      return launch_typed<kEpiSwiGlu>(ta, tb, p, s);
+    case kEpiF32:
+      return launch_typed<kEpiF32>(ta, tb, p, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace llama

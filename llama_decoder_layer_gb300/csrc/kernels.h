@@ -1,0 +1,92 @@
+// Host-side launch interface of the kernels (internal to the library; the
+// public C ABI is include/llama_layer.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace llama {
+
+enum GemmEpilogue : int {
+  kEpiBf16 = 0,    // out[m, n] = bf16(acc)
+  kEpiQkv = 1,     // RoPE on q/k columns, q -> q buffer, k/v -> paged caches
+  kEpiSwiGlu = 2,  // out[m, j] = bf16(silu(gate_j) * up_j)
+  kEpiF32 = 3,     // out[m, n] = acc (fp32)
+};
+
+struct RopeParams {
+  float theta;
+  int llama3;  // 0: plain frequencies, 1: llama3 frequency rule
+  float factor, low_freq_factor, high_freq_factor;
+  int original_max_pos;
+};
+
+struct QkvEpilogueArgs {
+  int q_size, kv_size, head_dim, n_kv_heads, block_size, num_blocks;
+  const int32_t* positions;  // [M]
+  const int32_t* slots;      // [M], < 0 = skip
+  void* k_cache;             // [num_blocks, n_kv, block, head_dim] bf16
+  void* v_cache;
+  RopeParams rope;
+};
+
+struct GemmArgs {
+  int epi;
+  const void* A;  // [M, K] bf16 row-major (activations)
+  const void* B;  // [N, K] bf16 row-major (weights, [out, in]); SwiGLU: rows [gate(I); up(I)]
+  int M, N, K;    // for SwiGLU, N = 2 * I
+  void* out;      // bf16 or f32 [M, ldo]
+  int ldo;
+  QkvEpilogueArgs qkv;
+  float* partials;  // stream-K partial tiles (see gemm_partials_bytes)
+  size_t partials_bytes;
+  int* err;
+  int force_mode;  // -1 auto, 0 data-parallel, 1 stream-K (tests)
+};
+
+size_t gemm_partials_bytes(int num_sms);
+int gemm_launch(const GemmArgs& a, cudaStream_t s);  // returns 0 or a CUDA error code
+
+// fused residual add + RMSNorm over rows of length H
+//   r = x (+ res_in); h = r * rsqrt(mean(r^2) + eps) * gamma
+// row_index_qsl != nullptr: output row b reads input row qsl[b+1]-1 (last
+// token of sequence b), otherwise row b reads row b.
+int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma,
+                       int rows, int H, float eps, const int32_t* row_index_qsl, cudaStream_t s);
+
+int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
+                        const int32_t* block_table, int T, int B,
+                        int max_blocks, int block_size, int num_blocks, int32_t* slots, int* err, cudaStream_t s);
+
+int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, int n_kv, int head_dim,
+                    int block_size, int num_blocks, void* k_cache, void* v_cache, int* err, cudaStream_t s);
+
+int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab, void* out, int* err,
+                 cudaStream_t s);
+
+int argmax_launch(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;        // [T, nq, d] bf16 (rotated)
+  const void* k_cache;  // [num_blocks, nkv, bs, d]
+  const void* v_cache;
+  void* out;            // [T, nq * d] bf16
+  const int32_t* qsl;   // [B+1]
+  const int32_t* seq_lens;
+  const int32_t* positions;
+  const int32_t* block_table;  // [B, max_blocks]
+  int T, B, max_blocks, num_blocks;
+  int nq, nkv, head_dim, block_size;
+  int max_query_len, max_seq_len;
+  float* partials;  // decode split-KV partials
+  size_t partials_bytes;
+  int* err;
+};
+
+size_t attn_partials_bytes(int B, int max_seq_len, int nq, int head_dim);
+int attention_launch(const AttnArgs& a, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace llama
