@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the Llama decoder-layer forward on GB300.
+
+Default workload: the 70B-shaped 8-layer stack (32 decode sequences with
+contexts uniform in [1024, 16384] + 2 prefill chunks of 2048 tokens, 4128
+tokens, final norm, lm_head over vocab 128256, greedy argmax).  One step is one
+call of ``llama_stack_forward``: every row of the hot path.  The metric is
+tokens/s per 70B-shape decoder layer (tokens x layers / step time).  The same
+line carries the single-layer 70B decode (128 sequences, context U[512, 8192])
+and 70B prefill (8 x 4096) results with their roofline fractions.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run: each rank runs an independent
+replica of the workload (sequences are independent, nothing is exchanged);
+the reported time is the maximum over ranks and the value counts all ranks.
+``--impl reference`` times the CPU oracle (test infrastructure, fp32) on a
+bounded sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workloads
+
+
+class Workload:
+    """A device-resident workload and its step function."""
+
+
+def setup_stack(lb, I, seed, dev):
+    spec = I.SPECS["stack_70b"]
+    bl = I.make_batch(spec, seed, dev)
+    layers = [I.make_layer_weights(spec, seed, l, dev) for l in range(spec.num_layers)]
+    emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, seed, dev)
+    caches = [I.make_kv_cache(spec, bl.num_blocks, seed, l, dev) for l in range(spec.num_layers)]
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T, B = bl.num_tokens, bl.num_seqs
+    W = Workload()
+    W.spec, W.bl, W.cfg, W.batch = spec, bl, cfg, batch
+    W.layers, W.emb, W.ids, W.lm, W.fn, W.caches = layers, emb, ids, lm, fn, caches
+    W.hidden = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device=dev)
+    W.residual = torch.empty_like(W.hidden)
+    W.tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    W.ws = lb.alloc_workspace(lb.workspace_size(cfg, T, B, batch.max_seq_len, spec.vocab), dev)
+    kcs = [c[0] for c in caches]
+    vcs = [c[1] for c in caches]
+
+    def step(stream=None, batch=None, ids=None, tokens=None):
+        lb.stack_forward(cfg, layers, fn, lm, batch or W.batch, W.hidden, W.residual, kcs, vcs,
+                         W.tokens if tokens is None else tokens, W.ws, embed=emb,
+                         input_ids=W.ids if ids is None else ids, stream=stream)
+
+    W.step = step
+    W.tokens_per_step = T
+    W.layers_n = spec.num_layers
+    return W
+
+
+def setup_layer(lb, I, name, seed, dev, weights=None):
+    spec = I.SPECS[name]
+    bl = I.make_batch(spec, seed, dev)
+    w = weights if weights is not None else I.make_layer_weights(spec, seed, 0, dev)
+    x, r = I.make_activations(spec, bl.num_tokens, seed, dev)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, dev)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    W = Workload()
+    W.spec, W.bl, W.cfg, W.batch, W.w, W.x, W.r, W.kc, W.vc = spec, bl, cfg, batch, w, x, r, kc, vc
+    W.hidden = x.clone()
+    W.res_out = torch.empty_like(x)
+    W.ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), dev)
+
+    def step(stream=None):
+        lb.layer_forward(cfg, w, batch, W.hidden, r, W.res_out, kc, vc, W.ws, stream=stream)
+
+    W.step = step
+    W.tokens_per_step = bl.num_tokens
+    W.layers_n = 1
+    return W
+
+
+def layer_algorithmic(spec, bl):
+    """Algorithmic bytes and flops of one layer step: every weight read once,
+    KV read once per KV head, the new K/V written once, activations read or
+    written once per materialised tensor; attention flops 4*d per visible
+    (query, key, q-head) pair."""
+    H, I, d, nq, nkv = spec.hidden, spec.intermediate, spec.head_dim, spec.n_heads, spec.n_kv_heads
+    T = bl.num_tokens
+    w_elems = (nq + 2 * nkv) * d * H + H * nq * d + 2 * I * H + H * I + 2 * H
+    pairs = 0
+    kv_read = 0
+    for c, q in zip(bl.ctx_lens, bl.q_lens):
+        kv_read += c + q
+        for j in range(q):
+            pairs += c + j + 1
+    kv_bytes = kv_read * nkv * d * 2 * 2 + T * nkv * d * 2 * 2
+    act_bytes = T * H * 2 * 2 * 3 + T * nq * d * 2 * 2 + T * I * 2 * 2 + T * 2 * I * 0
+    flops = 2 * T * w_elems + 4 * d * pairs * nq
+    return {"weight_bytes": w_elems * 2, "kv_bytes": kv_bytes, "act_bytes": act_bytes,
+            "bytes": w_elems * 2 + kv_bytes + act_bytes, "flops": flops}
+
+
+def time_steps(step, steps, warmup, world, sampler=None):
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, world), clocks
+
+
+def time_e2e(lb, W, steps, warmup, world, dev):
+    """Same stack step through the public API with the step's inputs copied
+    from pinned host memory and the sampled tokens copied back, every step."""
+    bl = W.bl
+    host = {
+        "ids": W.ids.cpu().pin_memory(), "positions": bl.positions.cpu().pin_memory(),
+        "qsl": bl.query_start_loc.cpu().pin_memory(), "seq_lens": bl.seq_lens.cpu().pin_memory(),
+        "block_table": bl.block_table.cpu().pin_memory(),
+    }
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(bl.num_seqs, dtype=torch.int32).pin_memory()
+    batch = lb.Batch(dev_in["positions"], dev_in["qsl"], dev_in["seq_lens"], dev_in["block_table"],
+                     W.batch.num_blocks, W.batch.max_query_len, W.batch.max_seq_len)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        W.step(batch=batch, ids=dev_in["ids"])
+        out_host.copy_(W.tokens, non_blocking=True)
+
+    ms, _ = time_steps(step, steps, warmup, world)
+    return ms, h2d, d2h
+
+
+def time_kernel(fn, reps, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+# --------------------------------------------------------------------------- CPU oracle sample
+
+
+class OracleSample:
+    """The CPU oracle on the first ``n_seqs`` decode sequences of the stack
+    workload, through all layers, the final norm and lm_head.  Preparing the
+    inputs (device->host copies, bf16->fp32 widening, compacting the sample's
+    cache blocks) happens once, outside the timed calls."""
+
+    def __init__(self, W, n_seqs=2, dtype=np.float32):
+        from oracle import llama_oracle as O
+        self.O, self.dtype = O, dtype
+        spec, bl = W.spec, W.bl
+        self.sh = O.LayerShape(spec.hidden, spec.n_heads, spec.n_kv_heads, spec.head_dim, spec.intermediate,
+                               spec.rms_eps, spec.rope_theta, spec.rope_scaling, spec.block_size)
+        qsl = bl.query_start_loc.cpu().numpy()
+        seqs = list(range(n_seqs))
+        rows = np.concatenate([np.arange(qsl[b], qsl[b + 1]) for b in seqs])
+        bt_full = bl.block_table.cpu().numpy()
+        nblk = [(bl.ctx_lens[b] + bl.q_lens[b] + 15) // 16 for b in seqs]
+        used = np.concatenate([bt_full[b, :nblk[b]] for b in seqs]).astype(np.int64)
+        bt = -np.ones((len(seqs), max(nblk)), np.int64)
+        cur = 0
+        for i in range(len(seqs)):
+            bt[i, :nblk[i]] = np.arange(cur, cur + nblk[i])
+            cur += nblk[i]
+        q_lens = [bl.q_lens[b] for b in seqs]
+        self.sqsl = np.concatenate([[0], np.cumsum(q_lens)])
+        self.batch = O.Batch(bl.positions.cpu().numpy()[rows], self.sqsl, bl.seq_lens.cpu().numpy()[seqs], bt)
+        used_t = torch.as_tensor(used, device=W.layers[0]["w_qkv"].device)
+
+        def f(t):
+            return t.float().cpu().numpy()
+
+        def b16(t):
+            return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+        self.x0 = f(W.emb[W.ids[torch.as_tensor(rows, device=W.ids.device)].long()])
+        self.layers = [O.LayerWeights(f(w["ln1"]), f(w["w_qkv"]), f(w["w_o"]), f(w["ln2"]), f(w["w_gate_up"]),
+                                      f(w["w_down"])) for w in W.layers]
+        self.caches = [(b16(kc.index_select(0, used_t)), b16(vc.index_select(0, used_t))) for kc, vc in W.caches]
+        self.fn, self.lm = f(W.fn), f(W.lm)
+        self.ntok = len(rows)
+        self.ctx = [bl.ctx_lens[b] for b in seqs]
+
+    def run(self):
+        """One timed pass; returns the seconds spent inside oracle calls."""
+        O, sh, dtype = self.O, self.sh, self.dtype
+        x, r = self.x0, None
+        elapsed = 0.0
+        for ow, (kc, vc) in zip(self.layers, self.caches):
+            kc, vc = kc.copy(), vc.copy()
+            t0 = time.perf_counter()
+            x, r = O.decoder_layer(sh, ow, self.batch, x, r, kc, vc, dtype=dtype)
+            elapsed += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        sel = O.last_token_rows(self.sqsl)
+        hf, _ = O.fused_add_rms_norm(x[sel], r[sel], self.fn, sh.rms_eps, dtype)
+        O.greedy_argmax(O.linear(hf, self.lm, dtype))
+        return elapsed + time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- main
+
+
+def run_ours(args, world, rank, local):
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    from llama_decoder_layer_gb300 import inputs as I
+
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    seed = rank  # independent replicas: each rank its own sequences
+    W = setup_stack(lb, I, seed, dev)
+
+    # main line: the stack step
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(W.step, args.steps, args.warmup, world, sampler)
+    st, detail = lb.get_device_error()
+    if st != lb.LLAMA_OK:
+        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+    tok_layers = W.tokens_per_step * W.layers_n
+    value = tok_layers * world / (ms / 1e3)
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = time_e2e(lb, W, args.steps, args.warmup, world, dev)
+    e2e_value = tok_layers * world / (e2e_ms / 1e3)
+
+    # dominant kernel: the gate_up GEMM with SiluAndMul (one layer's worth), timed alone
+    spec, T = W.spec, W.tokens_per_step
+    xin = I.normal_bf16((T, spec.hidden), 1.0, 0.0, 77, dev)
+    aout = torch.empty((T, spec.intermediate), dtype=torch.bfloat16, device=dev)
+    gws = lb.alloc_workspace(lb.linear_workspace_size(), dev)
+    wgu = W.layers[0]["w_gate_up"]
+    k_ms = time_kernel(lambda: lb.gate_up_silu(xin, wgu, aout, gws), reps=max(args.steps, 10))
+    k_flops = 2.0 * T * 2 * spec.intermediate * spec.hidden
+    k_tflops = k_flops / (k_ms / 1e3) / 1e12
+    roofline = {"kernel": "k_gemm_tc<SwiGLU> (gate_up_proj + SiluAndMul)", "bound": "tensor",
+                "achieved": round(k_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(k_tflops / peaks["bf16_tflops"], 4), "peak_source": f"bf16_tflops ({peak_src}, burst)",
+                "flops_per_launch": k_flops, "launch_ms": round(k_ms, 4), "traffic": None}
+    del xin, aout, gws
+
+    extra = {}
+    if not args.no_extra:
+        # single-layer 70B decode and prefill (weights of the stack's layer 0; their own batches/caches)
+        for name in ("decode_70b", "prefill_70b"):
+            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0])
+            steps = max(args.steps, 30) if name.startswith("decode") else args.steps
+            lms, _ = time_steps(L.step, steps, args.warmup, world)
+            alg = layer_algorithmic(L.spec, L.bl)
+            tps = L.tokens_per_step * world / (lms / 1e3)
+            if name.startswith("decode"):
+                gbs = alg["bytes"] / (lms / 1e3) / 1e9
+                extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
+                               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                            "algorithmic_bytes": alg["bytes"]}}
+            else:
+                tf = alg["flops"] / (lms / 1e3) / 1e12
+                extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 3),
+                               "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                                            "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
+                                            "algorithmic_flops": alg["flops"]}}
+            st, detail = lb.get_device_error()
+            if st != lb.LLAMA_OK:
+                raise RuntimeError(f"device error in {name}: {lb.status_string(st)}")
+            del L
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        osmp = OracleSample(W, n_seqs=2)
+        secs = osmp.run()
+        cpu = {"value": round(osmp.ntok * W.layers_n / secs, 4), "unit": "tokens/s per layer", "cores": cpu_cores(),
+               "kind": "oracle", "seconds": round(secs, 2),
+               "sample": f"{osmp.ntok} decode sequences (1 token each, contexts {osmp.ctx}) through all "
+                         f"{W.layers_n} layers + final norm + lm_head, oracle in fp32 on the host"}
+        del osmp
+
+    # algorithmic totals of the stack step
+    alg_layers = [layer_algorithmic(W.spec, W.bl) for _ in range(1)][0]
+    stack_flops = alg_layers["flops"] * W.layers_n + 2.0 * W.bl.num_seqs * W.spec.hidden * W.spec.vocab
+    # per layer: slot map, 2 norms, 4 GEMMs, decode attention + combine + prefill attention;
+    # per step: embedding, final norm, lm_head GEMM + stream-K fixup, argmax
+    launches = W.layers_n * 10 + 5
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(value, 1), "unit": "tokens/s per layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights of the 70B shape)",
+        "config": {"workload": "stack_70b: 8 x 70B-shaped layers + final norm + lm_head(128256) + greedy argmax; "
+                               "32 decode seqs (ctx U[1024,16384]) + 2 prefill chunks x 2048; 4128 tokens",
+                   "tokens_per_step": W.tokens_per_step, "layers": W.layers_n,
+                   "l2": "inputs larger than L2 (13.7 GB of weights per step)", "parallelism": f"replicas x{world}"},
+        "stack_tflops_per_s": round(stack_flops / (ms / 1e3) / 1e12, 1),
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches * args.steps,
+        "cpu_baseline": cpu,
+    }
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank):
+    """Times the CPU oracle (fp32) on a bounded sample of the stack workload:
+    each step runs one decode sequence through all layers + head."""
+    if rank != 0:
+        return
+    from llama_decoder_layer_gb300 import inputs as I
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    # inputs come from the seeded generator (device only holds them; no kernel of this library runs)
+    import types
+    spec = I.SPECS["stack_70b"]
+    bl = I.make_batch(spec, 0, dev)
+    W = types.SimpleNamespace(spec=spec, bl=bl, layers_n=spec.num_layers)
+    W.layers = [I.make_layer_weights(spec, 0, l, dev) for l in range(spec.num_layers)]
+    W.emb, W.ids, W.lm, W.fn = I.make_stack_extras(spec, bl.num_tokens, 0, dev)
+    W.caches = [I.make_kv_cache(spec, bl.num_blocks, 0, l, dev) for l in range(spec.num_layers)]
+    W.hidden = W.emb
+    osmp = OracleSample(W, n_seqs=1)
+    del W.layers, W.caches, W.emb, W.lm
+    times = []
+    for i in range(args.warmup + args.steps):
+        secs = osmp.run()
+        if i >= args.warmup:
+            times.append(secs)
+    total = sum(times)
+    value = osmp.ntok * W.layers_n * len(times) / total
+    line = {
+        "impl": "reference",
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(value, 4), "unit": "tokens/s per layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "stack_70b (sample: 1 decode sequence through 8 layers + final norm + lm_head)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s per layer", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": "1 decode sequence per step through all 8 layers + head, fp32"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s per layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

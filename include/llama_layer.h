@@ -201,6 +201,13 @@ int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int
                  size_t workspace_bytes, llama_stream_t stream);
 size_t llama_linear_workspace_size(void);
 
+/* a[M, I] = silu(x W_gate^T) * (x W_up^T) with w_gate_up [2I, K] holding the
+ * gate rows then the up rows: the merged gate_up projection with SiluAndMul
+ * in its epilogue ([LLAMA-70B] LlamaMLP; [CODE-READING] section 5).  a bf16.
+ * I and K multiples of 8; workspace as for llama_linear. */
+int llama_gate_up_silu(const void* x, const void* w_gate_up, int M, int I, int K, void* a, void* workspace,
+                       size_t workspace_bytes, llama_stream_t stream);
+
 /* r = x (+ residual_in); h = r / sqrt(mean(r^2) + eps) * gamma, per row of
  * length H ([LLAMA-70B] section 3; eps inside the square root).  residual_out
  * may be NULL or alias x / residual_in; h may alias x. */

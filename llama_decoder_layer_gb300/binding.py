@@ -64,6 +64,7 @@ SIGNATURES = {
     "kv_cache_write": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _VP, _VP]),
     "llama_linear": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _VP, _SZ, _VP]),
     "llama_linear_workspace_size": (_SZ, []),
+    "llama_gate_up_silu": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "llama_fused_add_rmsnorm": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _F, _VP]),
     "llama_paged_attention": (_I, [_P_CFG, _P_B, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "llama_get_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_int)]),
@@ -231,6 +232,15 @@ def linear(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor, workspace: torch
     st = lib().llama_linear(_ptr(x), _ptr(w), M, N, K, _ptr(out), 1 if out.dtype == torch.float32 else 0,
                             _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "llama_linear")
+
+
+def gate_up_silu(x: torch.Tensor, w_gate_up: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                 stream=None) -> None:
+    M, K = x.shape
+    I = w_gate_up.shape[0] // 2
+    st = lib().llama_gate_up_silu(_ptr(x), _ptr(w_gate_up), M, I, K, _ptr(out), _ptr(workspace), workspace.numel(),
+                                  _stream(stream))
+    _check(st, "llama_gate_up_silu")
 
 
 def linear_workspace_size() -> int:

@@ -427,6 +427,30 @@ int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int
   return cuda_status(gemm_launch(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int llama_gate_up_silu(const void* x, const void* w_gate_up, int M, int I, int K, void* a, void* workspace,
+                       size_t workspace_bytes, llama_stream_t stream) {
+  if (M < 0 || I < 1 || K < 1) return LLAMA_ERR_ARG;
+  if (M == 0) return LLAMA_OK;
+  if (!x || !w_gate_up || !a) return LLAMA_ERR_ARG;
+  if (I % 8 || K % 8) return LLAMA_ERR_UNSUPPORTED;
+  if (!a16(x) || !a16(w_gate_up) || !a16(a)) return LLAMA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < llama_linear_workspace_size()) return LLAMA_ERR_WORKSPACE;
+  GemmArgs g{};
+  g.epi = kEpiSwiGlu;
+  g.A = x;
+  g.B = w_gate_up;
+  g.M = M;
+  g.N = 2 * I;
+  g.K = K;
+  g.out = a;
+  g.ldo = I;
+  g.partials = reinterpret_cast<float*>(ws_base(workspace));
+  g.partials_bytes = gemm_partials_bytes(num_sms());
+  g.err = device_error_word();
+  g.force_mode = -1;
+  return cuda_status(gemm_launch(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residual_out, void* h, const void* gamma,
                             int rows, int H, float eps, llama_stream_t stream) {
   if (rows < 0 || H < 8 || H % 8 || H > 16384 || !(eps >= 0.f)) return LLAMA_ERR_ARG;

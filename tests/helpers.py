@@ -73,3 +73,49 @@ def check_cache(gpu_bits: np.ndarray, ref_bits: np.ndarray, before_bits: np.ndar
     g = O.bf16_bits_to_float(gpu_bits[sel])
     r = O.bf16_bits_to_float(ref_bits[sel])
     return assert_close(g, r, f"{name} (written slots)")
+
+
+class SubBatch:
+    """A subset of the sequences of a batch, re-indexed with a compact cache:
+    the oracle runs on it alone (sequences are independent, so the result is
+    the same as on the full batch)."""
+
+    def __init__(self, bl, seqs, kc_dev, vc_dev):
+        qsl = bl.query_start_loc.cpu().numpy().astype(np.int64)
+        bt = bl.block_table.cpu().numpy().astype(np.int64)
+        self.seqs = list(seqs)
+        self.rows = np.concatenate([np.arange(qsl[b], qsl[b + 1]) for b in self.seqs]).astype(np.int64)
+        nblk = [(bl.ctx_lens[b] + bl.q_lens[b] + 15) // 16 for b in self.seqs]
+        self.orig_blocks = np.concatenate([bt[b, :n] for b, n in zip(self.seqs, nblk)]).astype(np.int64)
+        cbt = -np.ones((len(self.seqs), max(nblk)), np.int64)
+        cur = 0
+        for i, n in enumerate(nblk):
+            cbt[i, :n] = np.arange(cur, cur + n)
+            cur += n
+        q_lens = [bl.q_lens[b] for b in self.seqs]
+        cqsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int64)
+        pos = bl.positions.cpu().numpy().astype(np.int64)[self.rows]
+        sl = bl.seq_lens.cpu().numpy().astype(np.int64)[self.seqs]
+        self.batch = O.Batch(pos, cqsl, sl, cbt)
+        idx = torch.as_tensor(self.orig_blocks, device=kc_dev.device)
+        self.kc = bits(kc_dev.index_select(0, idx))
+        self.vc = bits(vc_dev.index_select(0, idx))
+
+    def gpu_written(self, cache_bits_after: np.ndarray) -> np.ndarray:
+        """GPU cache rows [n_rows, nkv, d] at the slots of the subset's tokens."""
+        out = []
+        for i, p in zip(O.token_sequence(self.batch.query_start_loc), self.batch.positions):
+            blk = self.orig_blocks[self.batch.block_table[i, p // 16]]
+            out.append(cache_bits_after[blk, :, p % 16, :])
+        return np.stack(out)
+
+    def oracle_written(self, compact_bits: np.ndarray) -> np.ndarray:
+        out = []
+        for i, p in zip(O.token_sequence(self.batch.query_start_loc), self.batch.positions):
+            out.append(compact_bits[self.batch.block_table[i, p // 16], :, p % 16, :])
+        return np.stack(out)
+
+
+def untouched_equal(after_bits: np.ndarray, before_bits: np.ndarray, written: np.ndarray) -> bool:
+    keep = ~written
+    return bool(np.array_equal(after_bits.transpose(0, 2, 1, 3)[keep], before_bits.transpose(0, 2, 1, 3)[keep]))
