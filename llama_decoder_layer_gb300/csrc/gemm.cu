@@ -9,6 +9,9 @@
 //   * SiluAndMul: silu(x[:d]) * x[d:]          (gate_up_proj; a tile loads 128
 //     gate rows and the matching 128 up rows, so both halves meet in one
 //     thread)
+// Every tensor a module of the layer returns is bf16 (the model's dtype), so
+// the fused epilogues round the projection output to bf16 before RoPE and
+// before SiluAndMul, exactly where the unfused modules would store it.
 //   * fp32 store                               (lm_head logits)
 // The kernel is persistent (one CTA per SM).  Large problems are scheduled
 // data-parallel (whole tiles, grouped raster for L2 reuse); problems with few
@@ -197,10 +200,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
       ld(c, g);
       ld(BN / 2 + c, u);
       if (!valid) continue;
+      // gate_up_proj's output is a bf16 tensor that SiluAndMul then reads
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float sg = g[e] / (1.0f + __expf(-g[e]));
-        g[e] = sg * u[e];
+        const float gv = round_bf16(g[e]);
+        const float sg = gv / (1.0f + __expf(-gv));
+        g[e] = sg * round_bf16(u[e]);
       }
       const int n = n_base + c;
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
@@ -239,9 +244,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
         ld(hc + j, lo);
         ld(hc + half + j, hi);
         if (!valid) continue;
+        // qkv_proj's output is a bf16 tensor that rotary_emb then reads
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float x1 = lo[e], x2 = hi[e];
+          const float x1 = round_bf16(lo[e]), x2 = round_bf16(hi[e]);
           lo[e] = x1 * cs[e] - x2 * sn[e];
           hi[e] = x2 * cs[e] + x1 * sn[e];
         }

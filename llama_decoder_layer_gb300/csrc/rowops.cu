@@ -77,8 +77,12 @@ __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __res
         v[c][6] += bf16_lo(r.w);
         v[c][7] += bf16_hi(r.w);
       }
+      // the new residual is a bf16 tensor; the norm is taken of that tensor
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss += v[c][e] * v[c][e];
+      for (int e = 0; e < 8; ++e) {
+        v[c][e] = round_bf16(v[c][e]);
+        ss += v[c][e] * v[c][e];
+      }
     }
   }
   ss = block_sum(ss, red);

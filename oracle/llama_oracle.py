@@ -10,8 +10,11 @@ It is deliberately plain and slow: NumPy arrays, one library matmul per
 projection, explicit loops over sequences, tokens and heads for attention, and
 no blocking, fusion or reordering beyond what the definitions state.  Floating
 point runs in ``dtype`` (float64 by default, float32 for the large subsets)
-over the exact bf16 input values.  The only rounding the oracle performs is the
-one the method itself prescribes: K and V are stored into a bf16 cache.
+over the exact bf16 input values.  The layer-level functions model the pages'
+modules in the model's dtype (R3): every tensor a module returns is stored in
+bf16 (``bf16_tensors=True``, the default there), while the arithmetic inside a
+module is exact in ``dtype``.  ``bf16_tensors=False`` gives exact arithmetic
+end to end (used by the pins of the mathematics).
 
 Sources (three web pages on vLLM's ``llama.py``), cited below by tag:
 
@@ -82,6 +85,19 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return bf16_bits_to_float(float_to_bf16_bits(np.asarray(x, dtype=np.float32)))
 
 
+def store(x, bf16_tensors: bool, dtype=np.float64):
+    """A module's output tensor as the next module sees it.
+
+    R3: [LLAMA-70B] config.json gives torch_dtype bfloat16, and in the pages'
+    code each module call (the fused RMSNorm, qkv_proj, rotary_emb, attn,
+    o_proj, gate_up_proj, the SiluAndMul act_fn, down_proj) returns a tensor of
+    the model's dtype; so every module output is stored in bf16 (round to
+    nearest even, through fp32)."""
+    if not bf16_tensors:
+        return x
+    return round_to_bf16(np.asarray(x)).astype(dtype)
+
+
 # ---------------------------------------------------------------------------
 # Configuration
 # ---------------------------------------------------------------------------
@@ -139,7 +155,7 @@ def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float, dtype=np.float64) -> 
     return x / np.sqrt(ms + dtype(eps)) * np.asarray(gamma, dtype=dtype)
 
 
-def fused_add_rms_norm(x, residual, gamma, eps, dtype=np.float64):
+def fused_add_rms_norm(x, residual, gamma, eps, dtype=np.float64, bf16_tensors=False):
     """The residual-fused RMSNorm of vLLM's decoder layer.
 
     [LLAMA-70B] §3 input_layernorm: when residual is None the residual becomes
@@ -147,6 +163,8 @@ def fused_add_rms_norm(x, residual, gamma, eps, dtype=np.float64):
     sum hidden + residual becomes the new residual and is normalised (R2).
     [CODE-READING] §4 uses the same call after attention
     (post_attention_layernorm) and §2.1 for the final norm.
+    With ``bf16_tensors`` both outputs are stored in bf16 and the norm is taken
+    of the stored residual (R3: the residual is a module output).
     Returns (normed, new_residual).
     """
     x = np.asarray(x, dtype=dtype)
@@ -154,7 +172,8 @@ def fused_add_rms_norm(x, residual, gamma, eps, dtype=np.float64):
         r = x.copy()
     else:
         r = x + np.asarray(residual, dtype=dtype)
-    return rms_norm(r, gamma, eps, dtype), r
+    r = store(r, bf16_tensors, dtype)
+    return store(rms_norm(r, gamma, eps, dtype), bf16_tensors, dtype), r
 
 
 # ---------------------------------------------------------------------------
@@ -391,22 +410,24 @@ class Batch:
 
 
 def attention_block(shape: LayerShape, w: LayerWeights, batch: Batch, h, k_cache_bits, v_cache_bits,
-                    rows=None, dtype=np.float64):
+                    rows=None, dtype=np.float64, bf16_tensors=True):
     """LlamaAttention.forward: qkv_proj -> split -> rotary_emb -> attn -> o_proj.
 
     [LLAMA-70B] §4 / [CODE-READING] §4: one merged projection, split into
     [q_size, kv_size, kv_size]; RoPE on q and k; v untouched; the cache update
     precedes attention ([WALKTHROUGH] Attention).  K/V for every token are
     written; attention and o_proj are evaluated on ``rows`` (all if None).
+    Module outputs (qkv, rotated q and k, attention output, o_proj output) are
+    stored in bf16 when ``bf16_tensors`` (R3).
     Returns y [T, hidden] (zero outside ``rows``).
     """
     T = h.shape[0]
-    qkv = linear(h, w.w_qkv, dtype)
+    qkv = store(linear(h, w.w_qkv, dtype), bf16_tensors, dtype)
     q = qkv[:, :shape.q_size].reshape(T, shape.n_heads, shape.head_dim)
     k = qkv[:, shape.q_size:shape.q_size + shape.kv_size].reshape(T, shape.n_kv_heads, shape.head_dim)
     v = qkv[:, shape.q_size + shape.kv_size:].reshape(T, shape.n_kv_heads, shape.head_dim)
     inv = rope_inv_freq(shape.head_dim, shape.rope_theta, shape.rope_scaling)
-    q = apply_rope(q, batch.positions, inv, dtype)
+    q = store(apply_rope(q, batch.positions, inv, dtype), bf16_tensors, dtype)
     k = apply_rope(k, batch.positions, inv, dtype)
     slots = slot_mapping(batch.positions, batch.query_start_loc, batch.block_table, shape.block_size)
     kv_cache_write(k, v, slots, k_cache_bits, v_cache_bits, shape.block_size)
@@ -415,40 +436,44 @@ def attention_block(shape: LayerShape, w: LayerWeights, batch: Batch, h, k_cache
                         rows=rows, dtype=dtype)
     y = np.zeros((T, shape.hidden), dtype=dtype)
     sel = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
-    y[sel] = linear(o[sel].reshape(len(sel), shape.q_size), w.w_o, dtype)
+    o_sel = store(o[sel].reshape(len(sel), shape.q_size), bf16_tensors, dtype)
+    y[sel] = store(linear(o_sel, w.w_o, dtype), bf16_tensors, dtype)
     return y
 
 
-def mlp_block(shape: LayerShape, w: LayerWeights, h2, dtype=np.float64):
+def mlp_block(shape: LayerShape, w: LayerWeights, h2, dtype=np.float64, bf16_tensors=True):
     """LlamaMLP.forward: gate_up_proj -> SiluAndMul -> down_proj.
 
     [LLAMA-70B] LlamaMLP: FFN(x) = down_proj(up_proj(x) * Act(gate_proj(x)))
     with Act = SiLU; any other activation is rejected.  [CODE-READING] §5.
+    The three module outputs are stored in bf16 when ``bf16_tensors`` (R3).
     """
     if shape.hidden_act != "silu":
         raise ValueError(f"unsupported activation {shape.hidden_act}: only silu")
-    gu = linear(h2, w.w_gate_up, dtype)
-    a = silu_and_mul(gu, dtype)
-    return linear(a, w.w_down, dtype)
+    gu = store(linear(h2, w.w_gate_up, dtype), bf16_tensors, dtype)
+    a = store(silu_and_mul(gu, dtype), bf16_tensors, dtype)
+    return store(linear(a, w.w_down, dtype), bf16_tensors, dtype)
 
 
 def decoder_layer(shape: LayerShape, w: LayerWeights, batch: Batch, hidden, residual,
-                  k_cache_bits, v_cache_bits, rows=None, dtype=np.float64):
+                  k_cache_bits, v_cache_bits, rows=None, dtype=np.float64, bf16_tensors=True):
     """One decoder layer: (hidden, residual) -> (hidden, residual).
 
     [CODE-READING] §2.1 / §3 / §4: input_layernorm (fused add) -> attention ->
     post_attention_layernorm (fused add) -> MLP; the residual is threaded out
     of the layer.  ``residual=None`` is the first layer ([LLAMA-70B] §3).
     The caches are updated in place for every token; the returned arrays are
-    meaningful on ``rows`` (all rows if None).
+    meaningful on ``rows`` (all rows if None).  ``bf16_tensors``: module
+    outputs stored in bf16 (R3).
     """
-    h, r = fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype)
-    y = attention_block(shape, w, batch, h, k_cache_bits, v_cache_bits, rows=rows, dtype=dtype)
+    h, r = fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype, bf16_tensors)
+    y = attention_block(shape, w, batch, h, k_cache_bits, v_cache_bits, rows=rows, dtype=dtype,
+                        bf16_tensors=bf16_tensors)
     sel = np.arange(h.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
-    h2, r2 = fused_add_rms_norm(y[sel], r[sel], w.ln2, shape.rms_eps, dtype)
+    h2, r2 = fused_add_rms_norm(y[sel], r[sel], w.ln2, shape.rms_eps, dtype, bf16_tensors)
     out = np.zeros_like(r)
     res = np.zeros_like(r)
-    out[sel] = mlp_block(shape, w, h2, dtype)
+    out[sel] = mlp_block(shape, w, h2, dtype, bf16_tensors)
     res[sel] = r2
     return out, res
 
@@ -459,14 +484,14 @@ def decoder_layer_unfused(shape: LayerShape, w: LayerWeights, batch: Batch, hidd
 
     [WALKTHROUGH] LlamaDecoderLayer: residual = h; h = norm(h); h = attn(h);
     h = residual + h; residual = h; h = norm(h); h = mlp(h); h = residual + h.
-    Used only as a cross-check of the fused form: for the same input
-    (hidden + residual of the fused form) it returns out + residual.
+    Used only as a cross-check of the fused form in exact arithmetic: for the
+    same input (hidden + residual of the fused form) it returns out + residual.
     """
     x = np.asarray(hidden, dtype=dtype)
     a_in = rms_norm(x, w.ln1, shape.rms_eps, dtype)
-    x = x + attention_block(shape, w, batch, a_in, k_cache_bits, v_cache_bits, dtype=dtype)
+    x = x + attention_block(shape, w, batch, a_in, k_cache_bits, v_cache_bits, dtype=dtype, bf16_tensors=False)
     m_in = rms_norm(x, w.ln2, shape.rms_eps, dtype)
-    return x + mlp_block(shape, w, m_in, dtype)
+    return x + mlp_block(shape, w, m_in, dtype, bf16_tensors=False)
 
 
 def last_token_rows(query_start_loc) -> np.ndarray:
@@ -489,21 +514,23 @@ def greedy_argmax(logits):
 
 
 def stack_forward(shape: LayerShape, layers: Sequence[LayerWeights], final_norm, lm_head, batch: Batch,
-                  hidden, k_caches, v_caches, dtype=np.float64):
+                  hidden, k_caches, v_caches, dtype=np.float64, bf16_tensors=True):
     """The model body and head over one flat batch.
 
     [CODE-READING] §2.1: for layer in layers: hidden, residual =
     layer(positions, hidden, residual), starting from residual None, then
     hidden, _ = norm(hidden, residual); [LLAMA-70B] final RMSNorm and Sampler;
-    R13 logits only for the last row of each sequence.
+    R13 logits only for the last row of each sequence.  Logits are kept in
+    ``dtype`` (the Sampler works on logits.float()).
     Returns (tokens, top-2 gap, logits [B, vocab], final normed rows [B, H]).
     """
     x = np.asarray(hidden, dtype=dtype)
     r = None
     for li, w in enumerate(layers):
-        x, r = decoder_layer(shape, w, batch, x, r, k_caches[li], v_caches[li], dtype=dtype)
+        x, r = decoder_layer(shape, w, batch, x, r, k_caches[li], v_caches[li], dtype=dtype,
+                             bf16_tensors=bf16_tensors)
     sel = last_token_rows(batch.query_start_loc)
-    hf, _ = fused_add_rms_norm(x[sel], r[sel], final_norm, shape.rms_eps, dtype)
+    hf, _ = fused_add_rms_norm(x[sel], r[sel], final_norm, shape.rms_eps, dtype, bf16_tensors)
     logits = linear(hf, lm_head, dtype)
     tok, gap = greedy_argmax(logits)
     return tok, gap, logits, hf

@@ -1,0 +1,179 @@
+"""Parity at the full sizes of the five workloads, in the launch configuration
+the benchmark times (GPU).  The GPU runs the whole batch; the oracle runs on a
+seeded subset of sequences (exact: sequences are independent) and, for the
+70B prefill, on a seeded subset of rows after the cache update."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from llama_decoder_layer_gb300 import binding as lb
+from llama_decoder_layer_gb300 import build as lbuild
+from llama_decoder_layer_gb300 import inputs as I
+from oracle import llama_oracle as O
+from tests.helpers import (SubBatch, assert_close, bits, f32, oracle_batch, oracle_shape, oracle_weights,
+                           written_slot_mask)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lbuild.build()
+    lb.lib()
+
+
+def _untouched_on_device(before: torch.Tensor, after: torch.Tensor, written: np.ndarray, name: str):
+    keep = torch.as_tensor(~written, device=before.device)  # [num_blocks, 16]
+    b = before.permute(0, 2, 1, 3)[keep]
+    a = after.permute(0, 2, 1, 3)[keep]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name}: slots outside the batch changed"
+
+
+def _layer_case(name, sample_seqs, rows_in_seq=None, seed=0, dtype=np.float64):
+    spec = I.SPECS[name]
+    bl = I.make_batch(spec, seed, DEV)
+    w = I.make_layer_weights(spec, seed, 0, DEV)
+    x, r = I.make_activations(spec, bl.num_tokens, seed, DEV)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, DEV)
+    kc0, vc0 = kc.clone(), vc.clone()
+    sub = SubBatch(bl, sample_seqs, kc, vc)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), DEV)
+    hid = x.clone()
+    res = torch.empty_like(x)
+    lb.layer_forward(cfg, w, batch, hid, r, res, kc, vc, ws)
+    torch.cuda.synchronize()
+    st, where = lb.get_device_error()
+    assert st == lb.LLAMA_OK, f"device error {st} at {where}"
+    # indexing: every slot outside the batch is untouched, bit for bit
+    wm = written_slot_mask(bl, bl.num_blocks)
+    _untouched_on_device(kc0, kc, wm, "k_cache")
+    _untouched_on_device(vc0, vc, wm, "v_cache")
+    del kc0, vc0
+    rows_sel = None if rows_in_seq is None else list(rows_in_seq)
+    xs = f32(x)[sub.rows]
+    rs = None if r is None else f32(r)[sub.rows]
+    kref, vref = sub.kc.copy(), sub.vc.copy()
+    out, res_ref = O.decoder_layer(oracle_shape(spec), oracle_weights(w), sub.batch, xs, rs, kref, vref,
+                                   rows=rows_sel, dtype=dtype)
+    sel = np.arange(len(sub.rows)) if rows_sel is None else np.asarray(rows_sel)
+    e1 = assert_close(f32(hid)[sub.rows][sel], out[sel], f"{name} hidden_states")
+    e2 = assert_close(f32(res)[sub.rows][sel], res_ref[sel], f"{name} residual")
+    e3 = assert_close(O.bf16_bits_to_float(sub.gpu_written(bits(kc))),
+                      O.bf16_bits_to_float(sub.oracle_written(kref)), f"{name} k written")
+    e4 = assert_close(O.bf16_bits_to_float(sub.gpu_written(bits(vc))),
+                      O.bf16_bits_to_float(sub.oracle_written(vref)), f"{name} v written")
+    print(f"{name}: rel err hidden {e1:.2e} residual {e2:.2e} k {e3:.2e} v {e4:.2e}")
+
+
+def test_tiny_full_config():
+    _layer_case("tiny", sample_seqs=range(2))
+
+
+def test_decode_8b_all_sequences():
+    _layer_case("decode_8b", sample_seqs=range(64))
+
+
+def test_decode_70b_seeded_subset():
+    rng = np.random.default_rng(2024)
+    _layer_case("decode_70b", sample_seqs=sorted(rng.choice(128, size=8, replace=False).tolist()))
+
+
+def test_prefill_70b_one_sequence_seeded_rows():
+    rng = np.random.default_rng(7)
+    seq = int(rng.integers(0, 8))
+    rows = sorted(set(rng.choice(4096, size=254, replace=False).tolist()) | {0, 4095})
+    _layer_case("prefill_70b", sample_seqs=[seq], rows_in_seq=rows)
+
+
+def test_stack_70b_subset_tokens_and_logits():
+    spec = I.SPECS["stack_70b"]
+    seed = 0
+    bl = I.make_batch(spec, seed, DEV)
+    layers = [I.make_layer_weights(spec, seed, l, DEV) for l in range(spec.num_layers)]
+    emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, seed, DEV)
+    caches = [I.make_kv_cache(spec, bl.num_blocks, seed, l, DEV) for l in range(spec.num_layers)]
+    # sample: 4 seeded decode sequences and one prefill chunk (sequence 32 or 33)
+    rng = np.random.default_rng(11)
+    sample = sorted(rng.choice(32, size=4, replace=False).tolist()) + [32 + int(rng.integers(0, 2))]
+    subs = [SubBatch(bl, sample, kc, vc) for kc, vc in caches]
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T, B = bl.num_tokens, bl.num_seqs
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, T, B, batch.max_seq_len, spec.vocab), DEV)
+    hid = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device=DEV)
+    res = torch.empty_like(hid)
+    tokens = torch.empty(B, dtype=torch.int32, device=DEV)
+    logits = torch.empty((B, spec.vocab), dtype=torch.float32, device=DEV)
+    lb.stack_forward(cfg, layers, fn, lm, batch, hid, res, [c[0] for c in caches], [c[1] for c in caches], tokens, ws,
+                     embed=emb, input_ids=ids, out_logits=logits)
+    torch.cuda.synchronize()
+    st, where = lb.get_device_error()
+    assert st == lb.LLAMA_OK, f"device error {st} at {where}"
+    # oracle in fp32 (its reading for this size) on the subset, layer by layer
+    sh = oracle_shape(spec)
+    sub0 = subs[0]
+    x = f32(emb)[ids.cpu().numpy().astype(np.int64)[sub0.rows]]
+    r = None
+    for l in range(spec.num_layers):
+        kref, vref = subs[l].kc.copy(), subs[l].vc.copy()
+        x, r = O.decoder_layer(sh, oracle_weights(layers[l]), subs[l].batch, x, r, kref, vref, dtype=np.float32)
+        ek = assert_close(O.bf16_bits_to_float(subs[l].gpu_written(bits(caches[l][0]))),
+                          O.bf16_bits_to_float(subs[l].oracle_written(kref)), f"layer {l} k written")
+        ev = assert_close(O.bf16_bits_to_float(subs[l].gpu_written(bits(caches[l][1]))),
+                          O.bf16_bits_to_float(subs[l].oracle_written(vref)), f"layer {l} v written")
+        print(f"stack layer {l}: k {ek:.2e} v {ev:.2e}")
+    last = O.last_token_rows(sub0.batch.query_start_loc)
+    hf, _ = O.fused_add_rms_norm(x[last], r[last], f32(fn), sh.rms_eps, np.float32, bf16_tensors=True)
+    ref_logits = O.linear(hf, f32(lm), np.float32)
+    ref_tok, gap = O.greedy_argmax(ref_logits)
+    e = assert_close(f32(logits)[sample], ref_logits, "logits")
+    g_tok = tokens.cpu().numpy()[sample]
+    decided = gap > 0.05
+    assert np.array_equal(g_tok[decided], ref_tok[decided]), f"greedy tokens differ: {g_tok} vs {ref_tok} gap {gap}"
+    # the argmax kernel agrees with the logits the GPU produced (all rows, exact index)
+    assert np.array_equal(tokens.cpu().numpy(), np.argmax(f32(logits), axis=-1))
+    print(f"stack: logits rel err {e:.2e}, tokens compared on {int(decided.sum())}/{len(sample)} rows, gap {gap}")
+
+
+def test_max_position_decode():
+    """One decode token at position 131071 (max_position_embeddings - 1) over a
+    131072-token context, tiny shape with llama3 RoPE."""
+    spec = dataclasses.replace(I.SPECS["tiny"], rope_theta=500000.0, rope_scaling=I.LLAMA3_SCALING,
+                               groups=(("decode", 1, 1, 131071, 131071), ("decode", 2, 1, 5, 70)))
+    bl = I.make_batch(spec, 1, DEV)
+    w = I.make_layer_weights(spec, 1, 0, DEV)
+    x, r = I.make_activations(spec, bl.num_tokens, 1, DEV)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, 1, 0, DEV)
+    kb0, vb0 = bits(kc), bits(vc)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), DEV)
+    hid = x.clone()
+    res = torch.empty_like(x)
+    lb.layer_forward(cfg, w, batch, hid, r, res, kc, vc, ws)
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
+    out, res_ref = O.decoder_layer(oracle_shape(spec), oracle_weights(w), oracle_batch(bl), f32(x),
+                                   None if r is None else f32(r), kb0.copy(), vb0.copy())
+    assert_close(f32(hid), out, "hidden at max position")
+    assert_close(f32(res), res_ref, "residual at max position")
+
+
+def test_empty_batch_is_a_no_op():
+    spec = I.SPECS["tiny"]
+    cfg = lb.LayerConfig.from_spec(spec)
+    w = I.make_layer_weights(spec, 0, 0, DEV)
+    e = torch.empty(0, dtype=torch.int32, device=DEV)
+    batch = lb.Batch(e, torch.zeros(1, dtype=torch.int32, device=DEV), e,
+                     torch.zeros((0, 1), dtype=torch.int32, device=DEV), 1, 1, 1)
+    x = torch.empty((0, spec.hidden), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((1, spec.n_kv_heads, 16, spec.head_dim), dtype=torch.bfloat16, device=DEV)
+    ws = lb.alloc_workspace(1024, DEV)
+    lb.layer_forward(cfg, w, batch, x, None, x, kc, kc.clone(), ws)
+    assert lb.get_device_error()[0] == lb.LLAMA_OK

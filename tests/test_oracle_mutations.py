@@ -121,11 +121,12 @@ def _mut_slot_off_by_one(positions, query_start_loc, block_table, block_size):
 _orig_layer = O.decoder_layer
 
 
-def _mut_layer_residual_dropped(shape, w, batch, hidden, residual, kc, vc, rows=None, dtype=np.float64):
-    h, r = O.fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype)
-    y = O.attention_block(shape, w, batch, h, kc, vc, rows=rows, dtype=dtype)
-    h2, r2 = O.fused_add_rms_norm(y, None, w.ln2, shape.rms_eps, dtype)
-    return O.mlp_block(shape, w, h2, dtype), r2
+def _mut_layer_residual_dropped(shape, w, batch, hidden, residual, kc, vc, rows=None, dtype=np.float64,
+                                bf16_tensors=True):
+    h, r = O.fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype, bf16_tensors)
+    y = O.attention_block(shape, w, batch, h, kc, vc, rows=rows, dtype=dtype, bf16_tensors=bf16_tensors)
+    h2, r2 = O.fused_add_rms_norm(y, None, w.ln2, shape.rms_eps, dtype, bf16_tensors)
+    return O.mlp_block(shape, w, h2, dtype, bf16_tensors), r2
 
 
 MUTANTS = [
@@ -146,6 +147,7 @@ MUTANTS = [
     ("rms_norm", _mut_rms_eps_outside, lambda: P.check_layer_brute_force(None, True)),
     ("silu_and_mul", _mut_silu_swapped, lambda: P.check_layer_brute_force(None, True)),
     ("apply_rope", _mut_rope_sign, lambda: P.check_layer_brute_force(None, True)),
+    ("silu_and_mul", _mut_silu_swapped, lambda: P.check_layer_brute_force(None, True, bf16=True)),
 ]
 
 

@@ -442,20 +442,20 @@ def check_fused_equals_unfused(scaling=None):
     x = rng.standard_normal((T, sh.hidden))
     res = rng.standard_normal((T, sh.hidden))
     kc1, vc1 = s["k"].copy(), s["v"].copy()
-    out, r2 = O.decoder_layer(sh, w, batch, x, res, kc1, vc1)
+    out, r2 = O.decoder_layer(sh, w, batch, x, res, kc1, vc1, bf16_tensors=False)
     kc2, vc2 = s["k"].copy(), s["v"].copy()
     want = O.decoder_layer_unfused(sh, w, batch, x + res, kc2, vc2)
     assert np.max(np.abs(out + r2 - want)) < 1e-10
     assert np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2)
     # residual None: the layer's residual output starts from the raw input
     kc3, vc3 = s["k"].copy(), s["v"].copy()
-    out3, r3 = O.decoder_layer(sh, w, batch, x, None, kc3, vc3)
+    out3, r3 = O.decoder_layer(sh, w, batch, x, None, kc3, vc3, bf16_tensors=False)
     want3 = O.decoder_layer_unfused(sh, w, batch, x, s["k"].copy(), s["v"].copy())
     assert np.max(np.abs(out3 + r3 - want3)) < 1e-10
     # rows subset gives the same rows as the full evaluation
     kc4, vc4 = s["k"].copy(), s["v"].copy()
     rows = [0, 4, 9]
-    out4, r4 = O.decoder_layer(sh, w, batch, x, res, kc4, vc4, rows=rows)
+    out4, r4 = O.decoder_layer(sh, w, batch, x, res, kc4, vc4, rows=rows, bf16_tensors=False)
     assert np.max(np.abs(out4[rows] - out[rows])) < 1e-12 and np.array_equal(r4[rows], r2[rows])
 
 
@@ -480,10 +480,21 @@ def test_merged_qkv_equals_separate_projections():
     assert np.max(np.abs(O.silu_and_mul(gu) - sep)) < 1e-12
 
 
-def brute_layer(sh, w, positions, seq_of, seq_lens, x, res, kcache, vcache, bt):
+def _bf16_scalar(v):
+    """bf16 value of a Python float (round to nearest even), by integer
+    arithmetic on the float32 bit pattern."""
+    import struct
+    u = struct.unpack("<I", struct.pack("<f", v))[0]
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return struct.unpack("<f", struct.pack("<I", u & 0xFFFFFFFF))[0]
+
+
+def brute_layer(sh, w, positions, seq_of, seq_lens, x, res, kcache, vcache, bt, bf16=False):
     """Scalar-loop restatement of the layer on tiny shapes (contiguous per-token
-    K/V lists are rebuilt from a dict of written positions)."""
+    K/V lists are rebuilt from a dict of written positions).  ``bf16`` stores
+    every module output in bf16, as the layer-level oracle does by default."""
     T, H = len(x), sh.hidden
+    rn = (lambda vec: [_bf16_scalar(e) for e in vec]) if bf16 else (lambda vec: vec)
     d, nq, nkv = sh.head_dim, sh.n_heads, sh.n_kv_heads
 
     def rms(v, g):
@@ -504,13 +515,13 @@ def brute_layer(sh, w, positions, seq_of, seq_lens, x, res, kcache, vcache, bt):
             out[i + half] = vec[i + half] * c + vec[i] * s_
         return out
 
-    r = [[x[t][i] + (res[t][i] if res is not None else 0.0) for i in range(H)] for t in range(T)]
-    hs = [rms(r[t], w.ln1.tolist()) for t in range(T)]
+    r = [rn([x[t][i] + (res[t][i] if res is not None else 0.0) for i in range(H)]) for t in range(T)]
+    hs = [rn(rms(r[t], w.ln1.tolist())) for t in range(T)]
     Wqkv, q_all = w.w_qkv.tolist(), []
     kv_new = {}
     for t in range(T):
-        qkv = mv(Wqkv, hs[t])
-        q = [rot(qkv[h * d:(h + 1) * d], positions[t]) for h in range(nq)]
+        qkv = rn(mv(Wqkv, hs[t]))
+        q = [rn(rot(qkv[h * d:(h + 1) * d], positions[t])) for h in range(nq)]
         k = [rot(qkv[sh.q_size + h * d: sh.q_size + (h + 1) * d], positions[t]) for h in range(nkv)]
         v = [qkv[sh.q_size + sh.kv_size + h * d: sh.q_size + sh.kv_size + (h + 1) * d] for h in range(nkv)]
         q_all.append(q)
@@ -533,18 +544,19 @@ def brute_layer(sh, w, positions, seq_of, seq_lens, x, res, kcache, vcache, bt):
                     K.append(O.bf16_bits_to_float(kcache[blk, kh, j % sh.block_size]).astype(float).tolist())
                     V.append(O.bf16_bits_to_float(vcache[blk, kh, j % sh.block_size]).astype(float).tolist())
             o += brute_attention(q_all[t][h], K, V, p, 1 / math.sqrt(d))
-        y = mv(w.w_o.tolist(), o)
-        r2 = [y[i] + r[t][i] for i in range(H)]
-        h2 = rms(r2, w.ln2.tolist())
-        gu = mv(w.w_gate_up.tolist(), h2)
+        o = rn(o)
+        y = rn(mv(w.w_o.tolist(), o))
+        r2 = rn([y[i] + r[t][i] for i in range(H)])
+        h2 = rn(rms(r2, w.ln2.tolist()))
+        gu = rn(mv(w.w_gate_up.tolist(), h2))
         I = sh.intermediate
-        a = [gu[i] / (1 + math.exp(-gu[i])) * gu[I + i] for i in range(I)]
-        outs.append(mv(w.w_down.tolist(), a))
+        a = rn([gu[i] / (1 + math.exp(-gu[i])) * gu[I + i] for i in range(I)])
+        outs.append(rn(mv(w.w_down.tolist(), a)))
         r2s.append(r2)
     return np.array(outs), np.array(r2s)
 
 
-def check_layer_brute_force(scaling=None, residual=True):
+def check_layer_brute_force(scaling=None, residual=True, bf16=False):
     sh = tiny_shape(hidden=32, nq=4, nkv=2, d=8, inter=24, scaling=scaling,
                     theta=500000.0 if scaling else 10000.0, bs=2)
     rng = np.random.default_rng(77)
@@ -555,17 +567,31 @@ def check_layer_brute_force(scaling=None, residual=True):
     x = rng.standard_normal((T, sh.hidden))
     res = rng.standard_normal((T, sh.hidden)) if residual else None
     kc, vc = s["k"].copy(), s["v"].copy()
-    out, r2 = O.decoder_layer(sh, w, batch, x, res, kc, vc)
+    out, r2 = O.decoder_layer(sh, w, batch, x, res, kc, vc, bf16_tensors=bf16)
     seq_of = O.token_sequence(s["qsl"]).tolist()
     bo, br = brute_layer(sh, w, s["positions"].tolist(), seq_of, s["seq_lens"].tolist(), x.tolist(),
-                         None if res is None else res.tolist(), s["k"], s["v"], s["block_table"].tolist())
-    assert np.max(np.abs(out - bo)) < 1e-9 * max(1.0, np.max(np.abs(bo)))
-    assert np.max(np.abs(r2 - br)) < 1e-12
+                         None if res is None else res.tolist(), s["k"], s["v"], s["block_table"].tolist(), bf16=bf16)
+    if bf16:
+        # both sides store module outputs in bf16; the fp64 arithmetic inside may
+        # put a value on the other side of a bf16 rounding boundary in rare
+        # cases: allow one bf16 ulp on a few elements, exact elsewhere
+        ulp = np.abs(bo) * 2.0 ** -7 + 1e-30
+        bad = np.abs(out - bo) > 1e-9 * np.maximum(1.0, np.abs(bo))
+        assert np.all(np.abs(out - bo)[bad] <= ulp[bad] * 1.01) and bad.mean() < 0.02
+        assert np.max(np.abs(r2 - br)) <= 2.0 ** -7 * np.max(np.abs(br))
+    else:
+        assert np.max(np.abs(out - bo)) < 1e-9 * max(1.0, np.max(np.abs(bo)))
+        assert np.max(np.abs(r2 - br)) < 1e-12
 
 
 def test_layer_brute_force():
     check_layer_brute_force(None, True)
     check_layer_brute_force(O_LLAMA3, False)
+
+
+def test_layer_brute_force_bf16_module_outputs():
+    check_layer_brute_force(None, True, bf16=True)
+    check_layer_brute_force(O_LLAMA3, False, bf16=True)
 
 
 def check_stack_composition():
@@ -580,7 +606,7 @@ def check_stack_composition():
     x = rng.standard_normal((T, sh.hidden))
     kcs = [s["k"].copy() for _ in range(3)]
     vcs = [s["v"].copy() for _ in range(3)]
-    tok, gap, logits, hf = O.stack_forward(sh, layers, fnorm, lm, batch, x, kcs, vcs)
+    tok, gap, logits, hf = O.stack_forward(sh, layers, fnorm, lm, batch, x, kcs, vcs, bf16_tensors=False)
     # unfused model: hidden = layer(hidden) with the residual inside, then norm(hidden)
     hid = x.copy()
     for li in range(3):
