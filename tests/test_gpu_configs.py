@@ -14,7 +14,7 @@ from llama_decoder_layer_gb300 import build as lbuild
 from llama_decoder_layer_gb300 import inputs as I
 from oracle import llama_oracle as O
 from tests.helpers import (SubBatch, assert_close, bits, f32, oracle_batch, oracle_shape, oracle_weights,
-                           written_slot_mask)
+                           rel_err, written_slot_mask)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -92,13 +92,24 @@ def test_prefill_70b_one_sequence_seeded_rows():
 
 
 def test_stack_70b_subset_tokens_and_logits():
+    """The 8-layer stack, pinned in three parts:
+    (a) the stack call equals the composition of its layer calls, the final
+        norm and lm_head, bit for bit (caches, logits, tokens);
+    (b) every layer matches the oracle given that layer's inputs (teacher
+        forcing), on 4 seeded decode sequences and one prefill chunk;
+    (c) the head matches the oracle given the final hidden/residual rows:
+        logits within tolerance, greedy tokens where the top-2 gap > 0.05.
+    The free-running difference across the 8 layers is printed, not asserted:
+    two oracles that differ only in fp32 vs fp64 accumulation drift apart by
+    the same amount (bf16 module outputs through random-init layers)."""
     spec = I.SPECS["stack_70b"]
     seed = 0
     bl = I.make_batch(spec, seed, DEV)
-    layers = [I.make_layer_weights(spec, seed, l, DEV) for l in range(spec.num_layers)]
+    NL = spec.num_layers
+    layers = [I.make_layer_weights(spec, seed, l, DEV) for l in range(NL)]
     emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, seed, DEV)
-    caches = [I.make_kv_cache(spec, bl.num_blocks, seed, l, DEV) for l in range(spec.num_layers)]
-    # sample: 4 seeded decode sequences and one prefill chunk (sequence 32 or 33)
+    caches = [I.make_kv_cache(spec, bl.num_blocks, seed, l, DEV) for l in range(NL)]
+    caches2 = [(kc.clone(), vc.clone()) for kc, vc in caches]
     rng = np.random.default_rng(11)
     sample = sorted(rng.choice(32, size=4, replace=False).tolist()) + [32 + int(rng.integers(0, 2))]
     subs = [SubBatch(bl, sample, kc, vc) for kc, vc in caches]
@@ -115,30 +126,61 @@ def test_stack_70b_subset_tokens_and_logits():
     torch.cuda.synchronize()
     st, where = lb.get_device_error()
     assert st == lb.LLAMA_OK, f"device error {st} at {where}"
-    # oracle in fp32 (its reading for this size) on the subset, layer by layer
+
+    # (a) the same step as separate layer calls; keep every layer's inputs
+    h2 = emb[ids.long()].contiguous()
+    r2 = torch.empty_like(h2)
+    layer_in = []
+    for l in range(NL):
+        layer_in.append((f32(h2)[subs[0].rows], None if l == 0 else f32(r2)[subs[0].rows]))
+        lb.layer_forward(cfg, layers[l], batch, h2, None if l == 0 else r2, r2, caches2[l][0], caches2[l][1], ws)
+    last = bl.query_start_loc[1:].long() - 1
+    hf = torch.empty((B, spec.hidden), dtype=torch.bfloat16, device=DEV)
+    lb.fused_add_rmsnorm(h2[last].contiguous(), r2[last].contiguous(), None, hf, fn, spec.rms_eps)
+    logits2 = torch.empty_like(logits)
+    lb.linear(hf, lm, logits2, lb.alloc_workspace(lb.linear_workspace_size(), DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(hid, h2) and torch.equal(res, r2), "stack hidden/residual differ from the layer composition"
+    for l in range(NL):
+        assert torch.equal(caches[l][0].view(torch.int16), caches2[l][0].view(torch.int16)), f"layer {l} k cache"
+        assert torch.equal(caches[l][1].view(torch.int16), caches2[l][1].view(torch.int16)), f"layer {l} v cache"
+    assert torch.equal(logits, logits2), "stack logits differ from norm + lm_head of the composition"
+    del caches2
+
+    # (b) every layer against the oracle on the same inputs (fp32 oracle for this size)
     sh = oracle_shape(spec)
-    sub0 = subs[0]
-    x = f32(emb)[ids.cpu().numpy().astype(np.int64)[sub0.rows]]
-    r = None
-    for l in range(spec.num_layers):
+    x_free = f32(emb)[ids.cpu().numpy().astype(np.int64)[subs[0].rows]]
+    r_free = None
+    gpu_after = [(layer_in[l + 1] if l + 1 < NL else (f32(hid)[subs[0].rows], f32(res)[subs[0].rows]))
+                 for l in range(NL)]
+    for l in range(NL):
+        ow = oracle_weights(layers[l])
         kref, vref = subs[l].kc.copy(), subs[l].vc.copy()
-        x, r = O.decoder_layer(sh, oracle_weights(layers[l]), subs[l].batch, x, r, kref, vref, dtype=np.float32)
+        xo, ro = O.decoder_layer(sh, ow, subs[l].batch, layer_in[l][0], layer_in[l][1], kref, vref,
+                                 dtype=np.float32)
+        eh = assert_close(gpu_after[l][0], xo, f"layer {l} hidden (same inputs)")
+        er = assert_close(gpu_after[l][1], ro, f"layer {l} residual (same inputs)")
         ek = assert_close(O.bf16_bits_to_float(subs[l].gpu_written(bits(caches[l][0]))),
                           O.bf16_bits_to_float(subs[l].oracle_written(kref)), f"layer {l} k written")
         ev = assert_close(O.bf16_bits_to_float(subs[l].gpu_written(bits(caches[l][1]))),
                           O.bf16_bits_to_float(subs[l].oracle_written(vref)), f"layer {l} v written")
-        print(f"stack layer {l}: k {ek:.2e} v {ev:.2e}")
-    last = O.last_token_rows(sub0.batch.query_start_loc)
-    hf, _ = O.fused_add_rms_norm(x[last], r[last], f32(fn), sh.rms_eps, np.float32, bf16_tensors=True)
-    ref_logits = O.linear(hf, f32(lm), np.float32)
+        kf, vf = subs[l].kc.copy(), subs[l].vc.copy()
+        x_free, r_free = O.decoder_layer(sh, ow, subs[l].batch, x_free, r_free, kf, vf, dtype=np.float32)
+        print(f"stack layer {l}: same-input rel err hidden {eh:.2e} residual {er:.2e} k {ek:.2e} v {ev:.2e}; "
+              f"free-running hidden {rel_err(gpu_after[l][0], x_free):.2e}")
+
+    # (c) the head on the same inputs
+    lrows = O.last_token_rows(subs[0].batch.query_start_loc)
+    hf_ref, _ = O.fused_add_rms_norm(f32(hid)[subs[0].rows][lrows], f32(res)[subs[0].rows][lrows], f32(fn),
+                                     sh.rms_eps, np.float32, bf16_tensors=True)
+    ref_logits = O.linear(hf_ref, f32(lm), np.float32)
     ref_tok, gap = O.greedy_argmax(ref_logits)
     e = assert_close(f32(logits)[sample], ref_logits, "logits")
     g_tok = tokens.cpu().numpy()[sample]
     decided = gap > 0.05
     assert np.array_equal(g_tok[decided], ref_tok[decided]), f"greedy tokens differ: {g_tok} vs {ref_tok} gap {gap}"
-    # the argmax kernel agrees with the logits the GPU produced (all rows, exact index)
     assert np.array_equal(tokens.cpu().numpy(), np.argmax(f32(logits), axis=-1))
-    print(f"stack: logits rel err {e:.2e}, tokens compared on {int(decided.sum())}/{len(sample)} rows, gap {gap}")
+    print(f"stack head: logits rel err {e:.2e}, tokens compared on {int(decided.sum())}/{len(sample)} rows")
 
 
 def test_max_position_decode():
