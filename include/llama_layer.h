@@ -68,7 +68,8 @@ enum {
   LLAMA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
   LLAMA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than llama_workspace_size() */
   LLAMA_ERR_DEVICE_GUARD = 5, /* reported by llama_get_device_error: an index was out of range */
-  LLAMA_ERR_TIMEOUT = 6       /* reported by llama_get_device_error: a device wait gave up */
+  LLAMA_ERR_TIMEOUT = 6,      /* reported by llama_get_device_error: a device wait gave up */
+  LLAMA_ERR_SCRATCH_LIMIT = 7 /* llama_paged_attention_noalloc: the batch needs more than its fixed scratch */
 };
 
 /* Layer shape and constants.  [LLAMA-70B] config.json: hidden_size,
@@ -220,6 +221,26 @@ int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residu
 int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
                           const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
                           llama_stream_t stream);
+
+/* The paged attention above, for callers that cannot allocate device memory
+ * at the point where they run attention.  Examples are a plugin that its host
+ * framework hands only input and output buffers, a process whose memory pool
+ * another runtime owns, and a loop that forbids allocation after start-up.
+ * None of these can provide the workspace llama_paged_attention needs.  The
+ * pages have no counterpart to this entry point.
+ * The split-KV scratch is a fixed array of llama_paged_attention_noalloc_limit()
+ * bytes (32 MiB) inside the library.  Every GPU that loads the library holds it
+ * until the process exits.  A batch whose partials need more than that
+ * (num_seqs * ceil(ceil(max_seq_len/16)/32) * n_heads * (head_dim+2) * 4 + 256
+ * bytes) is rejected with LLAMA_ERR_SCRATCH_LIMIT before anything is
+ * launched.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array, so calls that overlap on the GPU race on it:
+ * the caller must serialise them.  Nothing in it has to start at zero.
+ * Arguments and results are those of llama_paged_attention. */
+int llama_paged_attention_noalloc(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q,
+                                  const void* k_cache, const void* v_cache, void* out, llama_stream_t stream);
+size_t llama_paged_attention_noalloc_limit(void);
 
 /* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
  * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.

@@ -24,6 +24,7 @@ LLAMA_ERR_CUDA = 3
 LLAMA_ERR_WORKSPACE = 4
 LLAMA_ERR_DEVICE_GUARD = 5
 LLAMA_ERR_TIMEOUT = 6
+LLAMA_ERR_SCRATCH_LIMIT = 7
 
 
 class LlamaError(RuntimeError):
@@ -67,6 +68,8 @@ SIGNATURES = {
     "llama_gate_up_silu": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP, _SZ, _VP]),
     "llama_fused_add_rmsnorm": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _F, _VP]),
     "llama_paged_attention": (_I, [_P_CFG, _P_B, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "llama_paged_attention_noalloc": (_I, [_P_CFG, _P_B, _VP, _VP, _VP, _VP, _VP]),
+    "llama_paged_attention_noalloc_limit": (_SZ, []),
     "llama_get_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_int)]),
     "llama_status_string": (ctypes.c_char_p, [_I]),
     "llama_num_sms": (_I, []),
@@ -259,6 +262,15 @@ def paged_attention(cfg: LayerConfig, batch: Batch, q, k_cache, v_cache, out, wo
     st = lib().llama_paged_attention(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "llama_paged_attention")
+
+
+def paged_attention_noalloc(cfg: LayerConfig, batch: Batch, q, k_cache, v_cache, out, stream=None) -> None:
+    """Paged attention with the library's fixed scratch array instead of a
+    workspace, for callers that cannot allocate device memory."""
+    c, b = cfg.c(), batch.c()
+    st = lib().llama_paged_attention_noalloc(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(k_cache),
+                                             _ptr(v_cache), _ptr(out), _stream(stream))
+    _check(st, "llama_paged_attention_noalloc")
 
 
 def get_device_error(stream=None):

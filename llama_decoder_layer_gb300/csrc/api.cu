@@ -509,6 +509,8 @@ const char* llama_status_string(int status) {
       return "device guard: an index was out of range";
     case LLAMA_ERR_TIMEOUT:
       return "device wait timed out";
+    case LLAMA_ERR_SCRATCH_LIMIT:
+      return "batch needs more split-KV scratch than llama_paged_attention_noalloc's fixed array";
     default:
       return "unknown status";
   }
