@@ -1,0 +1,88 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/llama_layer.h declares, and rejects bad arguments on
+the host before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from llama_decoder_layer_gb300 import binding as lb
+from llama_decoder_layer_gb300 import build as lbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "llama_layer.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("typedef",)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lbuild.build()
+    return lb.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("llama_layer_forward", "llama_stack_forward", "kv_cache_write", "llama_workspace_size",
+                     "llama_status_string", "llama_get_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in llama_layer.h but not exported"
+    # and the binding knows every one of them
+    assert set(names) == set(lb.SIGNATURES), set(names) ^ set(lb.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for st in range(0, 8):
+        s = lb.status_string(st)
+        assert s and "unknown" not in s
+    assert "unknown" in lb.status_string(99)
+
+
+def test_host_argument_checks_without_a_gpu(lib):
+    L = lib
+    # null config / weights / batch
+    assert L.llama_layer_forward(None, None, None, None, None, None, None, None, None, 0, None) == lb.LLAMA_ERR_ARG
+    cfg = lb.LayerConfig(512, 8, 2, 64, 1376, 1e-5, 1e4)
+    c = cfg.c()
+    assert L.llama_layer_forward(ctypes.byref(c), None, None, None, None, None, None, None, None, 0,
+                                 None) == lb.LLAMA_ERR_ARG
+    # unsupported activation (the MLP accepts silu only)
+    bad = lb.LayerConfig(512, 8, 2, 64, 1376, 1e-5, 1e4, hidden_act="gelu").c()
+    assert L.llama_paged_attention(ctypes.byref(bad), None, None, None, None, None, None, 0,
+                                   None) == lb.LLAMA_ERR_ARG
+    # n_heads not a multiple of n_kv_heads
+    bad = lb.LayerConfig(512, 8, 3, 64, 1376, 1e-5, 1e4).c()
+    assert L.llama_paged_attention(ctypes.byref(bad), None, None, None, None, None, None, 0,
+                                   None) == lb.LLAMA_ERR_ARG
+    # head_dim outside {64, 128}
+    bad = lb.LayerConfig(512, 8, 2, 96, 1376, 1e-5, 1e4).c()
+    assert L.llama_paged_attention(ctypes.byref(bad), None, None, None, None, None, None, 0,
+                                   None) == lb.LLAMA_ERR_UNSUPPORTED
+    # GQA group above 16
+    bad = lb.LayerConfig(4096, 32, 1, 128, 1376, 1e-5, 1e4).c()
+    assert L.llama_paged_attention(ctypes.byref(bad), None, None, None, None, None, None, 0,
+                                   None) == lb.LLAMA_ERR_UNSUPPORTED
+    # the stack needs at least one layer
+    assert L.llama_stack_forward(ctypes.byref(c), 0, None, None, None, 0, None, None, None, None, None, None, None,
+                                 None, None, None, 0, None) == lb.LLAMA_ERR_ARG
+    # cache write: bad sizes
+    assert L.kv_cache_write(None, None, None, 4, 0, 128, 16, 10, None, None, None) == lb.LLAMA_ERR_ARG
+    assert L.kv_cache_write(None, None, None, 4, 8, 100, 16, 10, None, None, None) == lb.LLAMA_ERR_ARG
+    # empty problems are valid no-ops
+    assert L.kv_cache_write(None, None, None, 0, 8, 128, 16, 10, None, None, None) == lb.LLAMA_OK
+    assert L.llama_linear(None, None, 0, 256, 256, None, 0, None, 0, None) == lb.LLAMA_OK
+    assert L.llama_linear(None, None, 4, 250, 256, None, 0, None, 0, None) == lb.LLAMA_ERR_ARG  # null pointers first
+    # norm: H must be a multiple of 8 within 16384
+    assert L.llama_fused_add_rmsnorm(None, None, None, None, None, 4, 100, 1e-5, None) == lb.LLAMA_ERR_ARG
