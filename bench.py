@@ -361,6 +361,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
     seed = rank  # independent replicas: each rank its own sequences
+    if args.workload != "stack_70b":
+        return run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
     W = setup_stack(lb, I, seed, dev)
 
     # main line: the stack step
@@ -400,19 +402,8 @@ def run_ours(args, world, rank, local):
             lms, _ = time_steps(L.step, steps, args.warmup, world)
             alg = layer_algorithmic(L.spec, L.bl)
             tps = L.tokens_per_step * world / (lms / 1e3)
-            if name.startswith("decode"):
-                gbs = alg["bytes"] / (lms / 1e3) / 1e9
-                extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
-                               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                                            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                                            "algorithmic_bytes": alg["bytes"]}}
-            else:
-                tf = alg["flops"] / (lms / 1e3) / 1e12
-                extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 3),
-                               "roofline": {"bound": "tensor", "achieved": round(tf, 1),
-                                            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                                            "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
-                                            "algorithmic_flops": alg["flops"]}}
+            extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
+                           "roofline": layer_roofline(name, alg, lms, peaks, peak_src)}
             st, detail = lb.get_device_error()
             if st != lb.LLAMA_OK:
                 raise RuntimeError(f"device error in {name}: {lb.status_string(st)}")
@@ -453,6 +444,43 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
     }
     line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def layer_roofline(name, alg, ms, peaks, peak_src):
+    if name.startswith("decode") or name == "tiny":
+        gbs = alg["bytes"] / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes": alg["bytes"], "traffic": None}
+    tf = alg["flops"] / (ms / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": f"bf16_tflops_sustained ({peak_src})", "algorithmic_flops": alg["flops"], "traffic": None}
+
+
+def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
+    """One decoder layer of the named workload per step (residual in, residual out)."""
+    L = setup_layer(lb, I, args.workload, seed, dev)
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(L.step, args.steps, args.warmup, world, sampler)
+    st, detail = lb.get_device_error()
+    if st != lb.LLAMA_OK:
+        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+    alg = layer_algorithmic(L.spec, L.bl)
+    value = L.tokens_per_step * world / (ms / 1e3)
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": args.workload, "tokens_per_step": L.tokens_per_step, "layers": 1,
+                   "l2": "inputs larger than L2" if alg["bytes"] > L2_BYTES else "inputs smaller than L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": layer_roofline(args.workload, alg, ms, peaks, peak_src),
+        "clocks": clocks, "gpu_launches": None, "cpu_baseline": None, "e2e": None,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -503,6 +531,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stack_70b",
+                    choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny"],
+                    help="stack_70b (default) or one single-layer workload (then no extra results)")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
