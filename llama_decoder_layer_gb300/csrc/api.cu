@@ -79,7 +79,8 @@ int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
   // cache rows and slots are 32-bit on the device
   if (static_cast<long long>(b->num_blocks) * c->n_kv_heads * c->block_size > 0x7fffffffLL) return LLAMA_ERR_ARG;
   if (static_cast<long long>(b->num_seqs) * b->max_blocks_per_seq > 0x7fffffffLL) return LLAMA_ERR_ARG;
-  if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // grid z dimension
+  if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;                   // grid z dimension
+  if ((b->num_tokens + 15) / 16 + b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // prefill work items
   return LLAMA_OK;
 }
 
@@ -107,7 +108,8 @@ Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int
   L.gpart_bytes = gemm_partials_bytes(num_sms());
   off += align256(L.gpart_bytes);
   L.apart = off;
-  L.apart_bytes = attn_partials_bytes(B > 0 ? B : 1, max_seq_len > 0 ? max_seq_len : 1, c.n_heads, c.head_dim);
+  L.apart_bytes =
+      attn_partials_bytes(B > 0 ? B : 1, T > 0 ? T : 1, max_seq_len > 0 ? max_seq_len : 1, c.n_heads, c.head_dim);
   off += align256(L.apart_bytes);
   if (vocab > 0) {
     L.hf = off;
@@ -472,7 +474,8 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
   if (batch->num_tokens == 0) return LLAMA_OK;
   if (!q || !k_cache || !v_cache || !out) return LLAMA_ERR_ARG;
   if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return LLAMA_ERR_UNSUPPORTED;
-  const size_t need = attn_partials_bytes(batch->num_seqs, batch->max_seq_len, cfg->n_heads, cfg->head_dim) + 256;
+  const size_t need =
+      attn_partials_bytes(batch->num_seqs, batch->num_tokens, batch->max_seq_len, cfg->n_heads, cfg->head_dim) + 256;
   if (workspace == nullptr || workspace_bytes < need) return LLAMA_ERR_WORKSPACE;
   AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws_base(workspace)),
                          need - 256, device_error_word());

@@ -52,8 +52,15 @@ struct AttnParams {
   float scale_log2;
   float* part_o;
   float2* part_ml;
+  uint32_t* pre_items;  // prefill work list: (sequence << 16) | q-tile, 0xFFFFFFFF past the end
   int* err;
 };
+
+constexpr uint32_t kNoItem = 0xFFFFFFFFu;
+
+// number of prefill work items the host sizes the launch for: at most
+// ceil(q_len / 16) per sequence, so at most T / 16 + B in total
+__host__ __device__ __forceinline__ int max_prefill_items(int T, int B) { return (T + 15) / 16 + B; }
 
 __host__ __device__ constexpr int tile_bytes(int D) { return kBS * D * 2; }
 
@@ -356,6 +363,52 @@ __global__ void k_attn_combine(AttnParams p) {
 // ---------------------------------------------------------------------------
 // prefill
 // ---------------------------------------------------------------------------
+// Lists the prefill work: the 16-token query tiles of every sequence with at
+// least two new tokens, longest causal range first within a sequence, so the
+// prefill grid holds no CTAs for decode sequences.  One CTA, a block-wide
+// exclusive scan over the sequences in rounds of 1024.
+__global__ void __launch_bounds__(1024) k_attn_plan(const int32_t* __restrict__ qsl, int B, uint32_t* items,
+                                                    int max_items) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int n = 0;
+    if (b < B) {
+      const int ql = qsl[b + 1] - qsl[b];
+      n = ql >= 2 ? (ql + 15) / 16 : 0;
+    }
+    int inc = n;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < static_cast<int>(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += t;
+      }
+      warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + inc - n;
+    for (int j = 0; j < n; ++j)
+      if (excl + j < max_items) items[excl + j] = (static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(n - 1 - j);
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_tot[(blockDim.x >> 5) - 1];
+    __syncthreads();
+  }
+  for (int i = carry + threadIdx.x; i < max_items; i += blockDim.x) items[i] = kNoItem;
+}
+
 constexpr int kPreMaxHeads = 8;  // q heads (consumer warps) per prefill CTA
 
 template <int D>
@@ -374,20 +427,17 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kPreStages);
 
   const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;  // head chunks per KV head
-  const int b = blockIdx.z, kvh = blockIdx.y / n_hc, hc = blockIdx.y % n_hc;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
+  const uint32_t item = p.pre_items[blockIdx.y];
+  if (item == kNoItem) return;
+  const int b = static_cast<int>(item >> 16), qt = static_cast<int>(item & 0xFFFFu);
+  const int kvh = blockIdx.x / n_hc, hc = blockIdx.x % n_hc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = min(kPreMaxHeads, p.group - hc * kPreMaxHeads);  // q heads of this CTA
   const int h_first = kvh * p.group + hc * kPreMaxHeads;
   if (warp > G) return;
   const int t0 = p.qsl[b];
   const int qlen = p.qsl[b + 1] - t0;
-  if (qlen < 2) return;
-  if ((qlen + 15) / 16 > static_cast<int>(gridDim.x)) {  // longer than the launch's max_query_len
-    if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
-    return;
-  }
-  if (qt * 16 >= qlen) return;
+  if (qlen < 2 || qt * 16 >= qlen) return;
   const int tq = t0 + qt * 16;              // first token of this q tile
   const int nrows = min(16, qlen - qt * 16);
 
@@ -652,9 +702,13 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
     if (e != cudaSuccess) return e;
   }
   if (a.max_query_len >= 2) {
+    const int items = max_prefill_items(a.T, a.B);
+    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, p.pre_items, items);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
     const int warps = (p.group < kPreMaxHeads ? p.group : kPreMaxHeads) + 1;
-    dim3 gp((a.max_query_len + 15) / 16, a.nkv * n_hc, a.B);
+    dim3 gp(a.nkv * n_hc, items);
     k_attn_prefill<D><<<gp, warps * 32, prefill_smem<D>(), s>>>(tk, tv, p);
     e = cudaGetLastError();
   }
@@ -663,10 +717,11 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
 
 }  // namespace
 
-size_t attn_partials_bytes(int B, int max_seq_len, int nq, int head_dim) {
+size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim) {
   const int nch = num_chunks((max_seq_len + kBS - 1) / kBS);
   const size_t n = static_cast<size_t>(B) * (nch < 1 ? 1 : nch) * nq;
-  return n * head_dim * sizeof(float) + n * sizeof(float2) + 256;
+  return n * head_dim * sizeof(float) + n * sizeof(float2) +
+         static_cast<size_t>(max_prefill_items(T, B)) * sizeof(uint32_t) + 256;
 }
 
 int attention_launch(const AttnArgs& a, cudaStream_t s) {
@@ -691,9 +746,11 @@ int attention_launch(const AttnArgs& a, cudaStream_t s) {
   p.err = a.err;
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   const size_t n = static_cast<size_t>(a.B) * (num_chunks(max_blk) < 1 ? 1 : num_chunks(max_blk)) * a.nq;
-  if (attn_partials_bytes(a.B, a.max_seq_len, a.nq, a.head_dim) > a.partials_bytes) return cudaErrorInvalidValue;
+  if (attn_partials_bytes(a.B, a.T, a.max_seq_len, a.nq, a.head_dim) > a.partials_bytes) return cudaErrorInvalidValue;
+  if (a.B > 65535 || max_prefill_items(a.T, a.B) > 65535) return cudaErrorInvalidValue;  // item packing, grid y
   p.part_o = a.partials;
   p.part_ml = reinterpret_cast<float2*>(a.partials + n * a.head_dim);
+  p.pre_items = reinterpret_cast<uint32_t*>(p.part_ml + n);
   if (a.head_dim == 128) return launch_d<128>(a, tk, tv, p, s);
   if (a.head_dim == 64) return launch_d<64>(a, tk, tv, p, s);
   return cudaErrorInvalidValue;

@@ -156,9 +156,156 @@ __device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
   }
 }
 
-// The fused epilogue of one output tile for the row `row` (one thread per
-// row).  `ld(col, v)` returns accumulator columns [col, col+32) of this row; it
-// may be warp-collective, so every call is made under tile-uniform control.
+// ---------------------------------------------------------------------------
+// Epilogue.  A tile's accumulator row is split into column units that can be
+// finished independently: 8 chunks of 32 columns (bf16/f32 stores), 4 chunks
+// of 32 SwiGLU outputs (each reads gate columns c.. and up columns 128+c..), or
+// 4 (head, 32-pair chunk) units of the qkv tile.  `ld(col, v)` returns
+// accumulator columns [col, col+32) of the thread's row; the TMEM loader is
+// warp-collective, so every call is made under tile-uniform control.
+// ---------------------------------------------------------------------------
+template <int EPI>
+struct EpiUnits {
+  static constexpr int kUnits = (EPI == kEpiBf16 || EPI == kEpiF32) ? 8 : 4;
+};
+
+__device__ __forceinline__ void store_chunk(const GemmParams& p, int row, int n, const float (&v)[32], bool f32out) {
+  if (f32out) {
+    float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
+    if (n + 32 <= p.n_out) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = v[e];
+    }
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
+    if (n + 32 <= p.n_out) {
+      store_bf16x32(o, v);
+    } else {
+      for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = __float2bfloat16_rn(v[e]);
+    }
+  }
+}
+
+// Where this row's k/v go in the paged cache (slot < 0: nowhere).
+struct QkvRow {
+  int pos, slot, blk, off;
+};
+
+__device__ __forceinline__ QkvRow qkv_row(const GemmParams& p, int row, bool valid) {
+  const QkvEpilogueArgs& q = p.qkv;
+  QkvRow r;
+  r.pos = valid ? q.positions[row] : 0;
+  r.slot = valid ? q.slots[row] : -1;
+  if (r.slot >= q.num_blocks * q.block_size) {
+    report_error(p.err, kErrGuard, kWhereSlot);
+    r.slot = -1;
+  }
+  r.blk = r.slot >= 0 ? r.slot / q.block_size : 0;
+  r.off = r.slot >= 0 ? r.slot % q.block_size : 0;
+  return r;
+}
+
+// RoPE on pairs (j+e, half+j+e) of the head starting at global column col,
+// then the store: q to the q buffer, k to the cache.  qkv_proj's output is a
+// bf16 tensor that rotary_emb then reads, hence the rounding first.
+__device__ __forceinline__ void qkv_rotate_store(const GemmParams& p, int row, const QkvRow& r, int col, int j,
+                                                 float (&lo)[32], float (&hi)[32], const float (&sn)[32],
+                                                 const float (&cs)[32]) {
+  const QkvEpilogueArgs& q = p.qkv;
+  const int d = q.head_dim, half = d >> 1;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x1 = round_bf16(lo[e]), x2 = round_bf16(hi[e]);
+    lo[e] = x1 * cs[e] - x2 * sn[e];
+    hi[e] = x2 * cs[e] + x1 * sn[e];
+  }
+  if (col < q.q_size) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + col + j;
+    store_bf16x32(o, lo);
+    store_bf16x32(o + half, hi);
+  } else if (r.slot >= 0) {
+    const int kh = (col - q.q_size) / d;
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.k_cache) +
+                       ((static_cast<size_t>(r.blk) * q.n_kv_heads + kh) * q.block_size + r.off) * d + j;
+    store_bf16x32(o, lo);
+    store_bf16x32(o + half, hi);
+  }
+}
+
+__device__ __forceinline__ void qkv_v_store(const GemmParams& p, const QkvRow& r, int col, int j,
+                                            const float (&v)[32]) {
+  const QkvEpilogueArgs& q = p.qkv;
+  if (r.slot < 0) return;
+  const int vh = (col - q.q_size - q.kv_size) / q.head_dim;
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.v_cache) +
+                     ((static_cast<size_t>(r.blk) * q.n_kv_heads + vh) * q.block_size + r.off) * q.head_dim + j;
+  store_bf16x32(o, v);
+}
+
+// SiluAndMul on 32 outputs: gate_up_proj's output is a bf16 tensor that
+// SiluAndMul then reads, hence the rounding of both halves first.
+__device__ __forceinline__ void swiglu32(float (&g)[32], const float (&u)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float gv = round_bf16(g[e]);
+    const float sg = gv / (1.0f + __expf(-gv));
+    g[e] = sg * round_bf16(u[e]);
+  }
+}
+
+// One column unit of one row (used by the stream-K fixup, where every thread
+// owns a (row, unit) pair).
+template <int EPI, class Loader>
+__device__ __forceinline__ void epilogue_unit(const GemmParams& p, int tm, int tn, int row_in_tile, int unit,
+                                              Loader& ld, const float2* rope_tab) {
+  const int row = tm * BM + row_in_tile;
+  if (row >= p.M) return;
+  if constexpr (EPI == kEpiBf16 || EPI == kEpiF32) {
+    const int c = unit * 32;
+    const int n = tn * BN + c;
+    if (n >= p.n_out) return;
+    float v[32];
+    ld(c, v);
+    store_chunk(p, row, n, v, EPI == kEpiF32);
+  } else if constexpr (EPI == kEpiSwiGlu) {
+    const int c = unit * 32;
+    const int n = tn * (BN / 2) + c;
+    if (n >= p.n_out) return;
+    float g[32], u[32];
+    ld(c, g);
+    ld(BN / 2 + c, u);
+    swiglu32(g, u);
+    store_chunk(p, row, n, g, false);
+  } else {
+    const QkvEpilogueArgs& q = p.qkv;
+    const int d = q.head_dim, half = d >> 1;
+    const int per_head = half / 32;  // 32-pair chunks per head
+    const int hc = (unit / per_head) * d;
+    const int j = (unit % per_head) * 32;
+    const int col = tn * BN + hc;
+    if (col >= p.N) return;
+    const QkvRow r = qkv_row(p, row, true);
+    float lo[32], hi[32];
+    ld(hc + j, lo);
+    ld(hc + half + j, hi);
+    if (col < q.q_size + q.kv_size) {
+      float sn[32], cs[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) rope_sincos(r.pos, rope_tab[j + e], sn[e], cs[e]);
+      qkv_rotate_store(p, row, r, col, j, lo, hi, sn, cs);
+    } else {
+      qkv_v_store(p, r, col, j, lo);
+      qkv_v_store(p, r, col, half + j, hi);
+    }
+  }
+}
+
+// The whole tile for one row (one thread per row, the GEMM kernel's epilogue
+// warps).  For qkv the j-chunks are the outer loop so sin/cos are shared by
+// the heads of the tile.
 template <int EPI, class Loader>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int tn, int row_in_tile, Loader& ld,
                                               const float2* rope_tab) {
@@ -171,25 +318,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
       if (n_base + c >= p.n_out) break;  // tile-uniform
       float v[32];
       ld(c, v);
-      if (!valid) continue;
-      const int n = n_base + c;
-      if constexpr (EPI == kEpiBf16) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
-        if (n + 32 <= p.n_out) {
-          store_bf16x32(o, v);
-        } else {
-          for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = __float2bfloat16_rn(v[e]);
-        }
-      } else {
-        float* o = reinterpret_cast<float*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
-        if (n + 32 <= p.n_out) {
-          float4* o4 = reinterpret_cast<float4*>(o);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = v[e];
-        }
-      }
+      if (valid) store_chunk(p, row, n_base + c, v, EPI == kEpiF32);
     }
   } else if constexpr (EPI == kEpiSwiGlu) {
     const int n_base = tn * (BN / 2);
@@ -200,42 +329,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
       ld(c, g);
       ld(BN / 2 + c, u);
       if (!valid) continue;
-      // gate_up_proj's output is a bf16 tensor that SiluAndMul then reads
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float gv = round_bf16(g[e]);
-        const float sg = gv / (1.0f + __expf(-gv));
-        g[e] = sg * round_bf16(u[e]);
-      }
-      const int n = n_base + c;
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + n;
-      if (n + 32 <= p.n_out) {
-        store_bf16x32(o, g);
-      } else {
-        for (int e = 0; e < 32 && n + e < p.n_out; ++e) o[e] = __float2bfloat16_rn(g[e]);
-      }
+      swiglu32(g, u);
+      store_chunk(p, row, n_base + c, g, false);
     }
   } else {  // kEpiQkv
     const QkvEpilogueArgs& q = p.qkv;
     const int d = q.head_dim;
     const int half = d >> 1;
     const int n0 = tn * BN;
-    const int pos = valid ? q.positions[row] : 0;
-    int slot = valid ? q.slots[row] : -1;
-    if (slot >= q.num_blocks * q.block_size) {
-      report_error(p.err, kErrGuard, kWhereSlot);
-      slot = -1;
-    }
-    const int blk = slot >= 0 ? slot / q.block_size : 0;
-    const int off = slot >= 0 ? slot % q.block_size : 0;
-    // rotated heads (q and k): j-chunks outer so sin/cos are shared by the
-    // heads of the tile
+    const QkvRow r = qkv_row(p, row, valid);
 #pragma unroll 1
     for (int j = 0; j < half; j += 32) {
       if (n0 >= q.q_size + q.kv_size) break;  // tile holds only v heads
       float sn[32], cs[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) rope_sincos(pos, rope_tab[j + e], sn[e], cs[e]);
+      for (int e = 0; e < 32; ++e) rope_sincos(r.pos, rope_tab[j + e], sn[e], cs[e]);
 #pragma unroll 1
       for (int hc = 0; hc < BN; hc += d) {
         const int col = n0 + hc;
@@ -243,25 +351,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
         float lo[32], hi[32];
         ld(hc + j, lo);
         ld(hc + half + j, hi);
-        if (!valid) continue;
-        // qkv_proj's output is a bf16 tensor that rotary_emb then reads
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x1 = round_bf16(lo[e]), x2 = round_bf16(hi[e]);
-          lo[e] = x1 * cs[e] - x2 * sn[e];
-          hi[e] = x2 * cs[e] + x1 * sn[e];
-        }
-        if (col < q.q_size) {
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(row) * p.ldo + col + j;
-          store_bf16x32(o, lo);
-          store_bf16x32(o + half, hi);
-        } else if (slot >= 0) {
-          const int kh = (col - q.q_size) / d;
-          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.k_cache) +
-                             ((static_cast<size_t>(blk) * q.n_kv_heads + kh) * q.block_size + off) * d + j;
-          store_bf16x32(o, lo);
-          store_bf16x32(o + half, hi);
-        }
+        if (valid) qkv_rotate_store(p, row, r, col, j, lo, hi, sn, cs);
       }
     }
     // v heads: plain copy into the cache
@@ -270,15 +360,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
       const int col = n0 + hc;
       if (col >= p.N) break;
       if (col < q.q_size + q.kv_size) continue;
-      const int vh = (col - q.q_size - q.kv_size) / d;
 #pragma unroll 1
       for (int j = 0; j < d; j += 32) {
         float v[32];
         ld(hc + j, v);
-        if (!valid || slot < 0) continue;
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(q.v_cache) +
-                           ((static_cast<size_t>(blk) * q.n_kv_heads + vh) * q.block_size + off) * d + j;
-        store_bf16x32(o, v);
+        if (valid) qkv_v_store(p, r, col, j, v);
       }
     }
   }
@@ -534,8 +620,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // Sums the stream-K partial tiles of every tile that was split across CTAs
 // (fixed CTA order, so the result is deterministic) and applies the epilogue.
+// One thread per (row, column unit): a tile is spread over BM / kRows CTAs so
+// the partial reads of a decode-sized problem run on many SMs at once.
+constexpr int kFixThreads = 256;
+
 template <int EPI>
-__global__ void __launch_bounds__(128) k_gemm_fixup(GemmParams p) {
+__global__ void __launch_bounds__(kFixThreads) k_gemm_fixup(GemmParams p) {
+  constexpr int kUnits = EpiUnits<EPI>::kUnits;
+  constexpr int kRows = kFixThreads / kUnits;
   __shared__ float2 rope_tab[64];
   const int tile = blockIdx.x;
   const long long t0 = static_cast<long long>(tile) * p.kb, t1 = t0 + p.kb;
@@ -544,12 +636,17 @@ __global__ void __launch_bounds__(128) k_gemm_fixup(GemmParams p) {
   while (c + 1 < p.grid && sk_start(p.units, p.grid, c + 1) <= t0) ++c;
   while (c > 0 && sk_start(p.units, p.grid, c) > t0) --c;
   if (sk_start(p.units, p.grid, c) <= t0 && sk_start(p.units, p.grid, c + 1) >= t1) return;  // whole tile in one CTA
-  if constexpr (EPI == kEpiQkv) build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x, 128);
-  __syncthreads();
-  PartialLoader ld{p.partials, p.units, t0, t1, p.grid, c, static_cast<int>(threadIdx.x)};
   int tm, tn;
   tile_coords(p, tile, tm, tn);
-  epilogue_tile<EPI>(p, tm, tn, threadIdx.x, ld, rope_tab);
+  if (tm * BM + static_cast<int>(blockIdx.y) * kRows >= p.M) return;  // no valid row in this CTA
+  if constexpr (EPI == kEpiQkv) {
+    build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x, kFixThreads);
+    __syncthreads();
+  }
+  const int row_in_tile = blockIdx.y * kRows + threadIdx.x / kUnits;
+  const int unit = threadIdx.x % kUnits;
+  PartialLoader ld{p.partials, p.units, t0, t1, p.grid, c, row_in_tile};
+  epilogue_unit<EPI>(p, tm, tn, row_in_tile, unit, ld, rope_tab);
 }
 
 // ---------------------------------------------------------------------------
@@ -600,7 +697,8 @@ int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams&
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.sk) {
-    k_gemm_fixup<EPI><<<p.tiles, 128, 0, s>>>(p);
+    constexpr int kRows = kFixThreads / EpiUnits<EPI>::kUnits;
+    k_gemm_fixup<EPI><<<dim3(p.tiles, BM / kRows), kFixThreads, 0, s>>>(p);
     e = cudaGetLastError();
   }
   return e;

@@ -84,7 +84,8 @@ struct AttnArgs {
   int* err;
 };
 
-size_t attn_partials_bytes(int B, int max_seq_len, int nq, int head_dim);
+// split-KV partials + the prefill work list of a batch of B sequences and T tokens
+size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim);
 int attention_launch(const AttnArgs& a, cudaStream_t s);
 
 int num_sms();
