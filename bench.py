@@ -361,6 +361,10 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
     seed = rank  # independent replicas: each rank its own sequences
+    if args.workload == "gemm_gate_up":
+        return run_gate_up(args, world, rank, local, lb, I, dev, peaks, peak_src)
+    if args.workload in ("attn_prefill", "attn_decode"):
+        return run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
     if args.workload != "stack_70b":
         return run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
     W = setup_stack(lb, I, seed, dev)
@@ -460,6 +464,75 @@ def layer_roofline(name, alg, ms, peaks, peak_src):
             "peak_source": f"bf16_tflops_sustained ({peak_src})", "algorithmic_flops": alg["flops"], "traffic": None}
 
 
+def run_gate_up(args, world, rank, local, lb, I, dev, peaks, peak_src):
+    """The gate_up projection with its SiluAndMul epilogue at the stack's
+    shape (4128 tokens, 70B weights) alone: x 68 MB, W 940 MB, out 237 MB."""
+    spec = I.SPECS["stack_70b"]
+    T = sum(c * n for _, c, n, _, _ in spec.groups)
+    x = I.normal_bf16((T, spec.hidden), 1.0, 0.0, 77, dev)
+    w = I.normal_bf16((2 * spec.intermediate, spec.hidden), 0.02, 0.0, 78, dev)
+    out = torch.empty((T, spec.intermediate), dtype=torch.bfloat16, device=dev)
+    ws = lb.alloc_workspace(lb.linear_workspace_size(), dev)
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(lambda: lb.gate_up_silu(x, w, out, ws), args.steps, args.warmup, world, sampler)
+    flops = 2.0 * T * 2 * spec.intermediate * spec.hidden
+    tf = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(T * world / (ms / 1e3), 1), "unit": "tokens/s through gate_up_proj", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"gemm_gate_up: {T} x {2 * spec.intermediate} x {spec.hidden} + SiluAndMul",
+                   "l2": "inputs larger than L2 (940 MB of weights)"},
+        "roofline": {"kernel": "k_gemm_tc<SwiGLU>", "bound": "tensor", "achieved": round(tf, 1),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "peak_source": f"bf16_tflops ({peak_src}, burst)", "flops_per_launch": flops, "traffic": None},
+        "clocks": clocks, "gpu_launches": args.steps, "cpu_baseline": None, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
+    """The paged GQA attention of the 70B prefill (8 x 4096, causal) or decode
+    (128 sequences, context U[512, 8192]) batch alone, q drawn N(0,1)."""
+    spec = I.SPECS["prefill_70b" if args.workload == "attn_prefill" else "decode_70b"]
+    bl = I.make_batch(spec, seed, dev)
+    q = I.normal_bf16((bl.num_tokens, spec.n_heads, spec.head_dim), 1.0, 0.0, 5, dev)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, dev)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    out = torch.empty((bl.num_tokens, spec.n_heads * spec.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), dev)
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(lambda: lb.paged_attention(cfg, batch, q, kc, vc, out, ws), args.steps, args.warmup,
+                            world, sampler)
+    d, nq, nkv = spec.head_dim, spec.n_heads, spec.n_kv_heads
+    pairs = sum(c * q_ + q_ * (q_ + 1) // 2 for c, q_ in zip(bl.ctx_lens, bl.q_lens))
+    kv_bytes = sum(c + q_ for c, q_ in zip(bl.ctx_lens, bl.q_lens)) * nkv * d * 2 * 2
+    io_bytes = bl.num_tokens * nq * d * 2 * 2
+    if args.workload == "attn_prefill":
+        tf = 4.0 * d * pairs * nq / (ms / 1e3) / 1e12
+        roof = {"kernel": "k_attn_prefill", "bound": "tensor", "achieved": round(tf, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                "peak_source": f"bf16_tflops ({peak_src}, burst)", "traffic": None}
+    else:
+        gbs = (kv_bytes + io_bytes) / (ms / 1e3) / 1e9
+        roof = {"kernel": "k_attn_decode + k_attn_combine", "bound": "hbm", "achieved": round(gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "peak_source": f"hbm_gbs ({peak_src})", "algorithmic_bytes": kv_bytes + io_bytes, "traffic": None}
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(bl.num_tokens * world / (ms / 1e3), 1), "unit": "tokens/s through attention",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload}, "roofline": roof, "clocks": clocks, "gpu_launches": None,
+        "cpu_baseline": None, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
     """One decoder layer of the named workload per step (residual in, residual out)."""
     L = setup_layer(lb, I, args.workload, seed, dev)
@@ -532,8 +605,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stack_70b",
-                    choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny"],
-                    help="stack_70b (default) or one single-layer workload (then no extra results)")
+                    choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny", "gemm_gate_up",
+                             "attn_prefill", "attn_decode"],
+                    help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
+                         "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
+                         "attn_decode: the paged attention of the 70B prefill / decode batch alone")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

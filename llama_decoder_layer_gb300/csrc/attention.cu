@@ -546,66 +546,110 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
     const uint32_t vs = ks + STB;
     const int kbase = kt * kPreKeys;
     const bool need_mask = kbase + kPreKeys - 1 > p_lo;
+    const int nblk_t = min(4, (n_keys - kbase + kBS - 1) / kBS);  // 16-key blocks holding keys (warp-uniform)
+    // S = q K^T over the whole 64-key tile (8 n-tiles of 8 keys)
+    float s[8][4];
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-      // one 16-key block: S = q K^T, online softmax, O += P V
-      const int key0 = kbase + blk * kBS;
-      if (key0 >= n_keys) break;  // warp-uniform
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
-        const int krow = (lane >> 4) * 8 + (lane & 7);
-        const int csel = (lane >> 3) & 1;
+    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    {
+      const int krow = (lane >> 4) * 8 + (lane & 7);
+      const int csel = (lane >> 3) & 1;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int ch = 2 * kk + csel;
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(ks + blk * TB + (ch >> 3) * 2048 + sw128_offset(krow, ch & 7), r0, r1, r2, r3);
-          mma_bf16_16816(s[0], qa[kk], r0, r1);
-          mma_bf16_16816(s[1], qa[kk], r2, r3);
+      for (int blk = 0; blk < 4; ++blk) {
+        if (blk < nblk_t) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int ch = 2 * kk + csel;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(ks + blk * TB + (ch >> 3) * 2048 + sw128_offset(krow, ch & 7), r0, r1, r2, r3);
+            mma_bf16_16816(s[2 * blk], qa[kk], r0, r1);
+            mma_bf16_16816(s[2 * blk + 1], qa[kk], r2, r3);
+          }
         }
       }
-      const int kq = key0 + 2 * (lane & 3);
-      if (need_mask) {
+    }
+    // scale to the log2 domain; causal mask (keys past n_keys are past every
+    // row's position, so the same test removes them)
+    const int kq = kbase + 2 * (lane & 3);
+    if (need_mask) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 8; ++n)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int key = kq + n * 8 + (c & 1);
-            const int lim = c < 2 ? pos0 : pos1;
-            s[n][c] = key <= lim ? s[n][c] * p.scale_log2 : -INFINITY;
-          }
-      } else {
+        for (int c = 0; c < 4; ++c) {
+          const int key = kq + n * 8 + (c & 1);
+          const int lim = c < 2 ? pos0 : pos1;
+          s[n][c] = key <= lim ? s[n][c] * p.scale_log2 : -INFINITY;
+        }
+    } else {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 8; ++n)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) s[n][c] *= p.scale_log2;
-      }
-      float a0, a1;
-      uint32_t pa[4];
-      softmax_block(s, m0, m1, l0, l1, a0, a1, pa);
+        for (int c = 0; c < 4; ++c) s[n][c] *= p.scale_log2;
+    }
+    // online softmax once per tile: new row maxima, rescale of O and l
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= a0;
-        o[n][1] *= a0;
-        o[n][2] *= a1;
-        o[n][3] *= a1;
-      }
+    for (int n = 0; n < 8; ++n) {
+      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+    }
+    mx0 = quad_max(mx0);
+    mx1 = quad_max(mx1);
+    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+    const float b0 = nm0 == -INFINITY ? 0.f : nm0;
+    const float b1 = nm1 == -INFINITY ? 0.f : nm1;
+    const float a0 = exp2f(m0 - b0), a1 = exp2f(m1 - b1);
+    m0 = nm0;
+    m1 = nm1;
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      s[n][0] = exp2f(s[n][0] - b0);
+      s[n][1] = exp2f(s[n][1] - b0);
+      s[n][2] = exp2f(s[n][2] - b1);
+      s[n][3] = exp2f(s[n][3] - b1);
+      ls0 += s[n][0] + s[n][1];
+      ls1 += s[n][2] + s[n][3];
+    }
+    l0 = l0 * a0 + ls0;
+    l1 = l1 * a1 + ls1;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= a0;
+      o[n][1] *= a0;
+      o[n][2] *= a1;
+      o[n][3] *= a1;
+    }
+    // O += P V, one 16-key block per k-step
+    {
       const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
       const int csel = lane >> 4;
-      const bool tail = key0 + kBS > n_keys;
 #pragma unroll
-      for (int nd = 0; nd < D / 16; ++nd) {
-        const int ch = 2 * nd + csel;
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(vs + blk * TB + (ch >> 3) * 2048 + sw128_offset(vrow, ch & 7), r0, r1, r2, r3);
-        if (tail) {
-          r0 = mask_pair(r0, kq, n_keys);
-          r1 = mask_pair(r1, kq + 8, n_keys);
-          r2 = mask_pair(r2, kq, n_keys);
-          r3 = mask_pair(r3, kq + 8, n_keys);
+      for (int blk = 0; blk < 4; ++blk) {
+        if (blk < nblk_t) {
+          uint32_t pa[4];
+          pa[0] = pack_bf16x2(s[2 * blk][0], s[2 * blk][1]);
+          pa[1] = pack_bf16x2(s[2 * blk][2], s[2 * blk][3]);
+          pa[2] = pack_bf16x2(s[2 * blk + 1][0], s[2 * blk + 1][1]);
+          pa[3] = pack_bf16x2(s[2 * blk + 1][2], s[2 * blk + 1][3]);
+          const int key0 = kbase + blk * kBS;
+          const int kqb = key0 + 2 * (lane & 3);
+          const bool tail = key0 + kBS > n_keys;
+#pragma unroll
+          for (int nd = 0; nd < D / 16; ++nd) {
+            const int ch = 2 * nd + csel;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vs + blk * TB + (ch >> 3) * 2048 + sw128_offset(vrow, ch & 7), r0, r1, r2, r3);
+            if (tail) {
+              r0 = mask_pair(r0, kqb, n_keys);
+              r1 = mask_pair(r1, kqb + 8, n_keys);
+              r2 = mask_pair(r2, kqb, n_keys);
+              r3 = mask_pair(r3, kqb + 8, n_keys);
+            }
+            mma_bf16_16816(o[2 * nd], pa, r0, r1);
+            mma_bf16_16816(o[2 * nd + 1], pa, r2, r3);
+          }
         }
-        mma_bf16_16816(o[2 * nd], pa, r0, r1);
-        mma_bf16_16816(o[2 * nd + 1], pa, r2, r3);
       }
     }
     __syncwarp();

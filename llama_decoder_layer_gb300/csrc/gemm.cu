@@ -734,8 +734,14 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
     p.n_out = a.N;
   }
   p.tiles = p.tiles_m * p.tiles_n;
-  p.b_evict_first = p.tiles_m <= 2 ? 1 : 0;
-  p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
+  // Raster: when the activation operand fits comfortably in L2 (the decode
+  // and mixed-batch projections), walk every M-tile of a weight panel before
+  // moving on, so each weight byte comes from HBM once and the activations stay
+  // L2-resident; otherwise group 16 M-tiles (2 MB A panels, 4 MB B panels).
+  const size_t a_bytes = static_cast<size_t>(a.M) * a.K * 2;
+  const bool a_in_l2 = a_bytes <= (static_cast<size_t>(64) << 20);
+  p.b_evict_first = (p.tiles_m <= 2 || a_in_l2) ? 1 : 0;
+  p.group_m = a_in_l2 ? p.tiles_m : (p.tiles_m < 16 ? p.tiles_m : 16);
   const int sms = num_sms();
   bool sk = p.tiles < 2 * sms;
   if (a.force_mode == 0) sk = false;
