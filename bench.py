@@ -70,13 +70,22 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device=None):
+    """Maximum of a per-rank value (the step time) over all ranks."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    if device is None:
+        device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms_max, world):
+    """Units all ranks processed per second, timed by the slowest rank
+    (replicas: every rank processes its own batch of the same size)."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -376,7 +385,7 @@ def run_ours(args, world, rank, local):
     if st != lb.LLAMA_OK:
         raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
     tok_layers = W.tokens_per_step * W.layers_n
-    value = tok_layers * world / (ms / 1e3)
+    value = whole_job_rate(tok_layers, ms, world)
 
     # end to end through the public API with host buffers
     e2e_ms, h2d, d2h = time_e2e(lb, W, args.steps, args.warmup, world, dev)
