@@ -36,6 +36,10 @@ import torch  # noqa: E402
 
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the gate_up
+# GEMM at the stack's shape (4128 x 57344 x 8192), from an ncu capture of the
+# current kernel and launch parameters (None until taken).
+GATE_UP_DRAM_BYTES_PER_LAUNCH = None  # re-measure after any change to the kernel or its raster
 
 
 def load_peaks():
@@ -403,7 +407,8 @@ def run_ours(args, world, rank, local):
     roofline = {"kernel": "k_gemm_tc<SwiGLU> (gate_up_proj + SiluAndMul)", "bound": "tensor",
                 "achieved": round(k_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(k_tflops / peaks["bf16_tflops"], 4), "peak_source": f"bf16_tflops ({peak_src}, burst)",
-                "flops_per_launch": k_flops, "launch_ms": round(k_ms, 4), "traffic": None}
+                "flops_per_launch": k_flops, "launch_ms": round(k_ms, 4),
+                "traffic": GATE_UP_DRAM_BYTES_PER_LAUNCH}
     del xin, aout, gws
 
     extra = {}
@@ -474,10 +479,11 @@ def layer_roofline(name, alg, ms, peaks, peak_src):
 
 
 def run_gate_up(args, world, rank, local, lb, I, dev, peaks, peak_src):
-    """The gate_up projection with its SiluAndMul epilogue at the stack's
-    shape (4128 tokens, 70B weights) alone: x 68 MB, W 940 MB, out 237 MB."""
+    """The gate_up projection with its SiluAndMul epilogue alone, 70B weights,
+    --gemm-tokens rows (4128, the stack's batch, by default: x 68 MB, W 940 MB,
+    out 237 MB)."""
     spec = I.SPECS["stack_70b"]
-    T = sum(c * n for _, c, n, _, _ in spec.groups)
+    T = args.gemm_tokens
     x = I.normal_bf16((T, spec.hidden), 1.0, 0.0, 77, dev)
     w = I.normal_bf16((2 * spec.intermediate, spec.hidden), 0.02, 0.0, 78, dev)
     out = torch.empty((T, spec.intermediate), dtype=torch.bfloat16, device=dev)
@@ -619,6 +625,7 @@ def main():
                     help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
                          "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
                          "attn_decode: the paged attention of the 70B prefill / decode batch alone")
+    ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
