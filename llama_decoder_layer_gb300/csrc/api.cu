@@ -80,7 +80,7 @@ int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
   if (static_cast<long long>(b->num_blocks) * c->n_kv_heads * c->block_size > 0x7fffffffLL) return LLAMA_ERR_ARG;
   if (static_cast<long long>(b->num_seqs) * b->max_blocks_per_seq > 0x7fffffffLL) return LLAMA_ERR_ARG;
   if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;                   // grid z dimension
-  if ((b->num_tokens + 15) / 16 + b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // prefill work items
+  if ((b->num_tokens + 7) / 8 + b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // prefill work items
   return LLAMA_OK;
 }
 

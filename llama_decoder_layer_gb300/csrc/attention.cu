@@ -58,9 +58,9 @@ struct AttnParams {
 
 constexpr uint32_t kNoItem = 0xFFFFFFFFu;
 
-// number of prefill work items the host sizes the launch for: at most
-// ceil(q_len / 16) per sequence, so at most T / 16 + B in total
-__host__ __device__ __forceinline__ int max_prefill_items(int T, int B) { return (T + 15) / 16 + B; }
+// number of prefill work items the host sizes the list for: at most
+// ceil(q_len / tile) per sequence, tile >= 8 tokens, so at most T / 8 + B
+__host__ __device__ __forceinline__ int max_prefill_items(int T, int B) { return (T + 7) / 8 + B; }
 
 __host__ __device__ constexpr int tile_bytes(int D) { return kBS * D * 2; }
 
@@ -367,8 +367,8 @@ __global__ void k_attn_combine(AttnParams p) {
 // least two new tokens, longest causal range first within a sequence, so the
 // prefill grid holds no CTAs for decode sequences.  One CTA, a block-wide
 // exclusive scan over the sequences in rounds of 1024.
-__global__ void __launch_bounds__(1024) k_attn_plan(const int32_t* __restrict__ qsl, int B, uint32_t* items,
-                                                    int max_items) {
+__global__ void __launch_bounds__(1024) k_attn_plan(const int32_t* __restrict__ qsl, int B, int tile_tokens,
+                                                    uint32_t* items, int max_items) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const int32_t* __restrict__ 
     int n = 0;
     if (b < B) {
       const int ql = qsl[b + 1] - qsl[b];
-      n = ql >= 2 ? (ql + 15) / 16 : 0;
+      n = ql >= 2 ? (ql + tile_tokens - 1) / tile_tokens : 0;
     }
     int inc = n;  // inclusive scan within the warp
 #pragma unroll
@@ -678,6 +678,315 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 }
 
 // ---------------------------------------------------------------------------
+// prefill on the 5th-generation tensor cores (head_dim 128, 128 % group == 0)
+//
+// One CTA per (sequence, KV head, 128/G query tokens): the 128 MMA rows are
+// those tokens x the G q heads of the group (row r = token r/G, head r%G), so
+// every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
+// 64 columns) and 128-key K/V tiles (2-stage ring); one thread of warp 1 issues
+// S = Q K^T into a double-buffered TMEM accumulator and O += P V into a TMEM
+// accumulator (V is the MN-major B operand); warps 2-5 (one row each) run the
+// online softmax from TMEM, write P as bf16 into a 128-byte-swizzled tile and
+// rescale O in TMEM only when a row's running max grows by more than 2^8.
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 192;
+constexpr int kTcKeys = 128;                       // keys per K/V tile
+constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 32 KB (K or V, two 64-column halves)
+constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half (16 KB)
+constexpr int kTcSmem = 1024 + 32768 + 2 * 2 * kTcTileBytes + 32768 + 256;
+constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_attn_prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t q_s = sb;                                   // Q: two 64-column halves
+  auto k_s = [&](int st) { return sb + 32768u + st * 2u * kTcTileBytes; };
+  auto v_s = [&](int st) { return sb + 32768u + st * 2u * kTcTileBytes + kTcTileBytes; };
+  const uint32_t p_s = sb + 32768u + 4u * kTcTileBytes;      // P (bf16, K-major over keys)
+  uint8_t* p_gen = smem + 32768 + 4 * kTcTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 32768 + 4 * kTcTileBytes + 32768);
+  const uint32_t bar0 = smem_u32(bars);
+  const uint32_t q_full = bar0, kv_full0 = bar0 + 8, kv_empty0 = bar0 + 24, s_full0 = bar0 + 40, p_full = bar0 + 56,
+                 o_done = bar0 + 64, drain = bar0 + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const uint32_t item = p.pre_items[blockIdx.y];
+  if (item == kNoItem) return;
+  const int G = p.group, QT = 128 / G;
+  const int b = static_cast<int>(item >> 16), qt = static_cast<int>(item & 0xFFFFu);
+  const int kvh = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = p.qsl[b];
+  const int qlen = p.qsl[b + 1] - t0;
+  if (qlen < 2 || qt * QT >= qlen) return;
+  const int tq = t0 + qt * QT;
+  const int nrows_tok = min(QT, qlen - qt * QT);
+
+  if (threadIdx.x == 0) *p_hi_s = -1;
+  __syncthreads();
+  if (threadIdx.x < nrows_tok) atomicMax(p_hi_s, p.positions[tq + threadIdx.x]);
+  __syncthreads();
+  const int n_keys = *p_hi_s + 1;
+  if (n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks || n_keys < 1) {
+    if (kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+    return;
+  }
+  const int nblk = (n_keys + kBS - 1) / kBS;
+  const int ntiles = (n_keys + kTcKeys - 1) / kTcKeys;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kv_full0 + 8 * i, 1);
+      mbar_init(kv_empty0 + 8 * i, 1);
+      mbar_init(s_full0 + 8 * i, 1);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and 128, O at 256
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    bool ok = true;
+    uint32_t uses[2] = {0, 0};
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      mbar_arrive_expect_tx(q_full, 32768);
+      tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
+      tma_load_3d(q_s + kTcHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
+      const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(kv_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kf = kv_full0 + 8 * st;
+        mbar_arrive_expect_tx(kf, 2 * kTcTileBytes);
+        for (int i = 0; i < kTcKeys / kBS; ++i) {
+          const int jb = j * (kTcKeys / kBS) + i;
+          // blocks past the context load the first block again: finite data the mask removes
+          int blk = bt[jb < nblk ? jb : 0];
+          if (blk < 0 || blk >= p.num_blocks) {
+            report_error(p.err, kErrGuard, kWhereBlockTable);
+            blk = 0;
+          }
+          const int row = (blk * p.nkv + kvh) * kBS;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) {
+            tma_load_2d(k_s(st) + bx * kTcHalf + i * 2048, &tmK, kf, bx * 64, row, pol);
+            tma_load_2d(v_s(st) + bx * kTcHalf + i * 2048, &tmV, kf, bx * 64, row, pol);
+          }
+        }
+        uses[st]++;
+      }
+      if (!ok) {
+        report_error(p.err, kErrTimeout, kWhereAttnPrefill);
+        *abort_flag = 1;
+      }
+      mbar_wait(q_full, 0, nullptr);
+      for (int st = 0; st < 2; ++st)
+        if (uses[st] > 0) mbar_wait(kv_full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128);
+    constexpr uint32_t idPV = idesc_bf16_f32_bmn(128, 128);
+    bool ok = mbar_wait(q_full, 0, abort_flag);
+    bool issued = false;
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1;
+      if (!mbar_wait(kv_full0 + 8 * st, (j >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t d = tmem + st * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+          tc_mma_f16(d, smem_desc_sw128(q_s + off), smem_desc_sw128(k_s(st) + off), idS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full0 + 8 * st);
+        issued = true;
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < ntiles && ok; ++j) {
+      if (j + 1 < ntiles && !issue_s(j + 1)) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(p_full, j & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const int st = j & 1;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = smem_desc_sw128(p_s + (ks >> 2) * kTcHalf + (ks & 3) * 32);
+          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(st) + ks * 2048, kTcHalf, 1024);
+          tc_mma_f16(tmem + 256, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(kv_empty0 + 8 * st);
+        tc_commit(o_done);
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
+      *abort_flag = 1;
+    }
+    if (lane == 0 && issued) tc_commit(drain);
+    __syncwarp();
+    if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain, 0, nullptr);
+  } else {
+    // ---------------- softmax warps: one row each ----------------
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int tok = r / G, hq = r % G;
+    const bool row_ok = tok < nrows_tok;
+    const int pos = row_ok ? p.positions[tq + tok] : -1;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (!mbar_wait(s_full0 + 8 * st, (j >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float t[32];
+        tmem_ld32(lane_addr + st * 128 + c * 32, t);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t[e];
+      }
+      const int kbase = j * kTcKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        sv[c] = kbase + c <= pos ? sv[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[c]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      if (j > 0) {
+        // P V of the previous tile must be done: the P tile is reused and O may be rescaled
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool need = m_new > m_run + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(lane_addr + 256 + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(lane_addr + 256 + c * 32, o);
+          }
+          l *= alpha;
+          m_run = m_new;
+        }
+      } else {
+        m_run = m_new;
+      }
+      const float base = m_run == -INFINITY ? 0.f : m_run;
+      // P row (bf16) into the swizzled K-major tile
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        float e8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          e8[e] = exp2f(sv[ch * 8 + e] - base);
+          l += e8[e];
+        }
+        uint4 u;
+        u.x = pack_bf16x2(e8[0], e8[1]);
+        u.y = pack_bf16x2(e8[2], e8[3]);
+        u.z = pack_bf16x2(e8[4], e8[5]);
+        u.w = pack_bf16x2(e8[6], e8[7]);
+        const int half = ch >> 3, c8 = ch & 7;
+        *reinterpret_cast<uint4*>(p_gen + half * kTcHalf + r * 128 + ((c8 ^ (r & 7)) << 4)) = u;
+      }
+      // keys past the context inside the last loaded block: zero their V rows
+      // (P is zero there, but stale cache contents must not reach the MMA)
+      if (j == ntiles - 1) {
+        const int valid = n_keys - kbase;
+        uint8_t* vg = smem + (v_s(st) - sb);
+        for (int i = threadIdx.x - 64; i < (kTcKeys - valid) * 2 * 8; i += 128) {
+          const int rowv = valid + i / 16, hf = (i / 8) & 1, c16 = i & 7;
+          *reinterpret_cast<uint4*>(vg + hf * kTcHalf + rowv * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok && !mbar_wait(o_done, (ntiles - 1) & 1, abort_flag)) ok = false;
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = p.out + (static_cast<size_t>(tq + tok) * p.nq + kvh * G + hq) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(lane_addr + 256 + c * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= inv;
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
+            u.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
+            u.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
+            u.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
+            d4[q] = u;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -707,6 +1016,20 @@ bool make_cache_tmap(CUtensorMap* m, const void* base, long long rows, int D) {
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBS)};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [T, nq, 128] as a 3-D tensor (d, head, token) with a box of 64 columns x
+// `group` heads x `tokens` tokens: one box is 128 rows of the prefill tile
+bool make_q_tmap(CUtensorMap* m, const void* base, int T, int nq, int group, int tokens) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(nq), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(nq) * 128 * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tokens)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -745,9 +1068,27 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (a.max_query_len >= 2 && D == 128 && 128 % p.group == 0) {
+    // tensor-core prefill: 128 / group tokens per tile
+    const int qt_tokens = 128 / p.group;
+    const int items = (a.T + qt_tokens - 1) / qt_tokens + a.B;
+    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, qt_tokens, p.pre_items, items);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    static std::once_flag tc_once;
+    static cudaError_t tc_attr = cudaSuccess;
+    std::call_once(tc_once, [] {
+      tc_attr = cudaFuncSetAttribute(k_attn_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    });
+    if (tc_attr != cudaSuccess) return tc_attr;
+    CUtensorMap tq;
+    if (!make_q_tmap(&tq, a.q, a.T, a.nq, p.group, qt_tokens)) return cudaErrorInvalidValue;
+    k_attn_prefill_tc<<<dim3(a.nkv, items), kTcThreads, kTcSmem, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
   if (a.max_query_len >= 2) {
-    const int items = max_prefill_items(a.T, a.B);
-    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, p.pre_items, items);
+    const int items = (a.T + 15) / 16 + a.B;
+    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, 16, p.pre_items, items);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
