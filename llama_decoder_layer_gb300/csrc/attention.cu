@@ -690,30 +690,40 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // rescale O in TMEM only when a row's running max grows by more than 2^8.
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 192;
-constexpr int kTcKeys = 128;                       // keys per K/V tile
-constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 32 KB (K or V, two 64-column halves)
-constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half (16 KB)
-constexpr int kTcSmem = 1024 + 32768 + 2 * 2 * kTcTileBytes + 32768 + 256;
+constexpr int kTcKeys = 64;                        // keys per K/V tile
+constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-column halves)
+constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
+constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
+constexpr int kTcPBytes = 128 * kTcKeys * 2;       // P tile (16 KB)
+constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
+constexpr int kTcSmem = 2 * kTcQHalf + 2 * 2 * kTcTileBytes + kTcPBytes + 256 + kTcSlack;
 constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     k_attn_prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  if (pad > kTcSlack) {  // the dynamic shared memory base is 1024-aligned in practice
+    if (threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereAttnPrefill);
+    return;
+  }
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t q_s = sb;                                   // Q: two 64-column halves
-  auto k_s = [&](int st) { return sb + 32768u + st * 2u * kTcTileBytes; };
-  auto v_s = [&](int st) { return sb + 32768u + st * 2u * kTcTileBytes + kTcTileBytes; };
-  const uint32_t p_s = sb + 32768u + 4u * kTcTileBytes;      // P (bf16, K-major over keys)
-  uint8_t* p_gen = smem + 32768 + 4 * kTcTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 32768 + 4 * kTcTileBytes + 32768);
+  auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes; };
+  auto v_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes + kTcTileBytes; };
+  const uint32_t p_s = sb + 2u * kTcQHalf + 4u * kTcTileBytes;      // P (bf16, K-major over keys)
+  uint8_t* p_gen = smem + 2 * kTcQHalf + 4 * kTcTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + 4 * kTcTileBytes + kTcPBytes);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, kv_full0 = bar0 + 8, kv_empty0 = bar0 + 24, s_full0 = bar0 + 40, p_full = bar0 + 56,
-                 o_done = bar0 + 64, drain = bar0 + 72;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  // K and V have their own 2-stage rings: a K stage is free as soon as its
+  // S = Q K^T is done, so the next K tile is fetched while P V still runs
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
+                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full = bar0 + 88, o_done = bar0 + 96,
+                 drain = bar0 + 104;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -744,8 +754,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(kv_full0 + 8 * i, 1);
-      mbar_init(kv_empty0 + 8 * i, 1);
+      mbar_init(k_full0 + 8 * i, 1);
+      mbar_init(k_empty0 + 8 * i, 1);
+      mbar_init(v_full0 + 8 * i, 1);
+      mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
     }
     mbar_init(p_full, 4);
@@ -755,32 +767,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and 128, O at 256
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and kTcKeys, O at 2 * kTcKeys
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     bool ok = true;
-    uint32_t uses[2] = {0, 0};
+    uint32_t k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
     if (lane == 0) {
       const uint64_t pol = policy_evict_normal();
       mbar_arrive_expect_tx(q_full, 32768);
       tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
-      tma_load_3d(q_s + kTcHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
+      tma_load_3d(q_s + kTcQHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
       const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(kv_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t kf = kv_full0 + 8 * st;
-        mbar_arrive_expect_tx(kf, 2 * kTcTileBytes);
+      auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int j) {
+        mbar_arrive_expect_tx(bar, kTcTileBytes);
         for (int i = 0; i < kTcKeys / kBS; ++i) {
           const int jb = j * (kTcKeys / kBS) + i;
           // blocks past the context load the first block again: finite data the mask removes
@@ -790,41 +796,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             blk = 0;
           }
           const int row = (blk * p.nkv + kvh) * kBS;
-#pragma unroll
-          for (int bx = 0; bx < 2; ++bx) {
-            tma_load_2d(k_s(st) + bx * kTcHalf + i * 2048, &tmK, kf, bx * 64, row, pol);
-            tma_load_2d(v_s(st) + bx * kTcHalf + i * 2048, &tmV, kf, bx * 64, row, pol);
-          }
+          tma_load_2d(dst + i * 2048, tm, bar, 0, row, pol);
+          tma_load_2d(dst + kTcHalf + i * 2048, tm, bar, 64, row, pol);
         }
-        uses[st]++;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        if (!mbar_wait(k_empty0 + 8 * st, par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        load_tile(&tmK, k_s(st), k_full0 + 8 * st, j);
+        k_uses[st]++;
+        if (!mbar_wait(v_empty0 + 8 * st, par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        load_tile(&tmV, v_s(st), v_full0 + 8 * st, j);
+        v_uses[st]++;
       }
       if (!ok) {
         report_error(p.err, kErrTimeout, kWhereAttnPrefill);
         *abort_flag = 1;
       }
       mbar_wait(q_full, 0, nullptr);
-      for (int st = 0; st < 2; ++st)
-        if (uses[st] > 0) mbar_wait(kv_full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
+      for (int st = 0; st < 2; ++st) {
+        if (k_uses[st] > 0) mbar_wait(k_full0 + 8 * st, (k_uses[st] - 1) & 1u, nullptr);
+        if (v_uses[st] > 0) mbar_wait(v_full0 + 8 * st, (v_uses[st] - 1) & 1u, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t idS = idesc_bf16_f32(128, 128);
+    constexpr uint32_t idS = idesc_bf16_f32(128, kTcKeys);
     constexpr uint32_t idPV = idesc_bf16_f32_bmn(128, 128);
     bool ok = mbar_wait(q_full, 0, abort_flag);
     bool issued = false;
     auto issue_s = [&](int j) -> bool {
       const int st = j & 1;
-      if (!mbar_wait(kv_full0 + 8 * st, (j >> 1) & 1, abort_flag)) return false;
+      if (!mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t d = tmem + st * 128;
+        const uint32_t d = tmem + st * kTcKeys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-          tc_mma_f16(d, smem_desc_sw128(q_s + off), smem_desc_sw128(k_s(st) + off), idS, kk > 0 ? 1u : 0u);
+          const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
+          const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(st) + ck), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full0 + 8 * st);
+        tc_commit(k_empty0 + 8 * st);
         issued = true;
       }
       __syncwarp();
@@ -836,7 +858,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = false;
         break;
       }
-      if (!mbar_wait(p_full, j & 1, abort_flag)) {
+      if (!mbar_wait(p_full, j & 1, abort_flag) || !mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -844,12 +866,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) {
         const int st = j & 1;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = smem_desc_sw128(p_s + (ks >> 2) * kTcHalf + (ks & 3) * 32);
+        for (int ks = 0; ks < kTcKeys / 16; ++ks) {
+          const uint64_t a = smem_desc_sw128(p_s + ks * 32);
           const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(st) + ks * 2048, kTcHalf, 1024);
-          tc_mma_f16(tmem + 256, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_f16(tmem + 2 * kTcKeys, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(kv_empty0 + 8 * st);
+        tc_commit(v_empty0 + 8 * st);
         tc_commit(o_done);
       }
       __syncwarp();
@@ -878,22 +900,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float t[32];
-        tmem_ld32(lane_addr + st * 128 + c * 32, t);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t[e];
-      }
+      // pass 1: masked, scaled row maximum of S (TMEM read in 64-column chunks,
+      // eight independent max chains)
       const int kbase = j * kTcKeys;
-      float mx = -INFINITY;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        sv[c] = kbase + c <= pos ? sv[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kTcKeys / 64; ++c) {
+        float t[64];
+        tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
+        const int lim = pos - kbase - c * 64;  // column e is visible when e <= lim
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
       }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      mx = mx == -INFINITY ? -INFINITY : mx * p.scale_log2;
       const float m_new = fmaxf(m_run, mx);
+      // Rescale (rare): only when some row of the warp gains more than 2^8.
+      const bool need = j > 0 && m_new > m_run + kRescaleLog2;
+      const bool warp_rescale = __any_sync(0xffffffffu, need);
+      if (j == 0) m_run = m_new;
       if (j > 0) {
         // P V of the previous tile must be done: the P tile is reused and O may be rescaled
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag)) {
@@ -901,41 +930,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const bool need = m_new > m_run + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+      }
+      if (warp_rescale) {
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tmem_ld32(lane_addr + 256 + c * 32, o);
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(lane_addr + 2 * kTcKeys + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(lane_addr + 256 + c * 32, o);
-          }
-          l *= alpha;
-          m_run = m_new;
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(lane_addr + 2 * kTcKeys + c * 32, o);
         }
-      } else {
+        l *= alpha;
         m_run = m_new;
       }
       const float base = m_run == -INFINITY ? 0.f : m_run;
-      // P row (bf16) into the swizzled K-major tile
+      // pass 2: P = exp2(S - max) as bf16 into the swizzled K-major tile
+      float ls8[8];
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        float e8[8];
+      for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kTcKeys / 64; ++c) {
+        float t[64];
+        tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
+        const int lim = pos - kbase - c * 64;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          e8[e] = exp2f(sv[ch * 8 + e] - base);
-          l += e8[e];
+        for (int q4 = 0; q4 < 8; ++q4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int e = q4 * 8 + e2 * 2;
+            const float x0 = e <= lim ? exp2f(fmaf(t[e], p.scale_log2, -base)) : 0.f;
+            const float x1 = e + 1 <= lim ? exp2f(fmaf(t[e + 1], p.scale_log2, -base)) : 0.f;
+            ls8[e2 * 2] += x0;
+            ls8[e2 * 2 + 1] += x1;
+            w[e2] = pack_bf16x2(x0, x1);
+          }
+          const int ch = c * 8 + q4;  // 16-byte chunk of the P row (64 keys = one 128-byte row)
+          *reinterpret_cast<uint4*>(p_gen + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        uint4 u;
-        u.x = pack_bf16x2(e8[0], e8[1]);
-        u.y = pack_bf16x2(e8[2], e8[3]);
-        u.z = pack_bf16x2(e8[4], e8[5]);
-        u.w = pack_bf16x2(e8[6], e8[7]);
-        const int half = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(p_gen + half * kTcHalf + r * 128 + ((c8 ^ (r & 7)) << 4)) = u;
       }
+      l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       // keys past the context inside the last loaded block: zero their V rows
       // (P is zero there, but stale cache contents must not reach the MMA)
       if (j == ntiles - 1) {
@@ -962,7 +997,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
-        tmem_ld32(lane_addr + 256 + c * 32, o);
+        tmem_ld32(lane_addr + 2 * kTcKeys + c * 32, o);
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= inv;
@@ -983,7 +1018,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
