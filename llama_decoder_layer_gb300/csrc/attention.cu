@@ -25,6 +25,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -726,6 +727,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
+  int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
 
   const uint32_t item = p.pre_items[blockIdx.y];
   if (item == kNoItem) return;
@@ -739,11 +741,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int tq = t0 + qt * QT;
   const int nrows_tok = min(QT, qlen - qt * QT);
 
-  if (threadIdx.x == 0) *p_hi_s = -1;
+  if (threadIdx.x == 0) {
+    *p_hi_s = -1;
+    *p_lo_s = 0x7fffffff;
+  }
   __syncthreads();
-  if (threadIdx.x < nrows_tok) atomicMax(p_hi_s, p.positions[tq + threadIdx.x]);
+  if (threadIdx.x < nrows_tok) {
+    const int ps = p.positions[tq + threadIdx.x];
+    atomicMax(p_hi_s, ps);
+    atomicMin(p_lo_s, ps);
+  }
   __syncthreads();
   const int n_keys = *p_hi_s + 1;
+  const int pos_lo = *p_lo_s;  // tiles ending at or below it need no causal mask
   if (n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks || n_keys < 1) {
     if (kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
     return;
@@ -903,6 +913,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // pass 1: masked, scaled row maximum of S (TMEM read in 64-column chunks,
       // eight independent max chains)
       const int kbase = j * kTcKeys;
+      const bool full_tile = kbase + kTcKeys - 1 <= pos_lo;  // CTA-uniform
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
@@ -911,9 +922,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float t[64];
         tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
         const int lim = pos - kbase - c * 64;  // column e is visible when e <= lim
+        if (full_tile) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+          for (int e = 0; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+        }
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -954,21 +970,31 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float t[64];
         tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
         const int lim = pos - kbase - c * 64;
+        auto emit = [&](auto masked) {
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          uint32_t w[4];
+          for (int q4 = 0; q4 < 8; ++q4) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int e = q4 * 8 + e2 * 2;
-            const float x0 = e <= lim ? exp2f(fmaf(t[e], p.scale_log2, -base)) : 0.f;
-            const float x1 = e + 1 <= lim ? exp2f(fmaf(t[e + 1], p.scale_log2, -base)) : 0.f;
-            ls8[e2 * 2] += x0;
-            ls8[e2 * 2 + 1] += x1;
-            w[e2] = pack_bf16x2(x0, x1);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = q4 * 8 + e2 * 2;
+              float x0 = fast_exp2(fmaf(t[e], p.scale_log2, -base));
+              float x1 = fast_exp2(fmaf(t[e + 1], p.scale_log2, -base));
+              if (decltype(masked)::value) {
+                x0 = e <= lim ? x0 : 0.f;
+                x1 = e + 1 <= lim ? x1 : 0.f;
+              }
+              ls8[e2 * 2] += x0;
+              ls8[e2 * 2 + 1] += x1;
+              w[e2] = pack_bf16x2(x0, x1);
+            }
+            const int ch = c * 8 + q4;  // 16-byte chunk of the P row (64 keys = one 128-byte row)
+            *reinterpret_cast<uint4*>(p_gen + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          const int ch = c * 8 + q4;  // 16-byte chunk of the P row (64 keys = one 128-byte row)
-          *reinterpret_cast<uint4*>(p_gen + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        };
+        if (full_tile)
+          emit(std::false_type{});
+        else
+          emit(std::true_type{});
       }
       l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       // keys past the context inside the last loaded block: zero their V rows

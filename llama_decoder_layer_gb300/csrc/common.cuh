@@ -65,6 +65,14 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // value of x after storage as bf16 (round to nearest even)
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
+// 2^x by the hardware approximation instruction (relative error ~2^-22,
+// subnormal results flushed to zero): the softmax weights are stored as bf16
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory addresses and mbarriers
 // ---------------------------------------------------------------------------
