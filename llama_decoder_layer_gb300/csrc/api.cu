@@ -81,12 +81,14 @@ int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
   if (static_cast<long long>(b->num_seqs) * b->max_blocks_per_seq > 0x7fffffffLL) return LLAMA_ERR_ARG;
   if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;                   // grid z dimension
   if ((b->num_tokens + 7) / 8 + b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // prefill work items
+  if (b->max_seq_len > kMaxSeqLen) return LLAMA_ERR_UNSUPPORTED;  // split-KV merge scratch
   return LLAMA_OK;
 }
 
 struct Layout {
-  size_t slots, h, q, o, a, gpart, apart, hf, logits, total;
+  size_t slots, h, q, o, a, gpart, apart, cnt, hf, logits, total;
   size_t gpart_bytes, apart_bytes;
+  int cnt_attn;  // split-KV arrival counters, one per (sequence, KV head)
 };
 
 Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int vocab) {
@@ -111,6 +113,9 @@ Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int
   L.apart_bytes =
       attn_partials_bytes(B > 0 ? B : 1, T > 0 ? T : 1, max_seq_len > 0 ? max_seq_len : 1, c.n_heads, c.head_dim);
   off += align256(L.apart_bytes);
+  L.cnt = off;
+  L.cnt_attn = static_cast<int>(attn_counter_count(B, c.n_kv_heads));
+  off += align256(static_cast<size_t>(L.cnt_attn) * sizeof(int));
   if (vocab > 0) {
     L.hf = off;
     off += align256(static_cast<size_t>(B) * c.hidden * 2);
@@ -150,7 +155,7 @@ int check_weights(const LlamaLayerWeights* w) {
 }
 
 AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q, const void* kc, const void* vc,
-                   void* out, float* part, size_t part_bytes, int* err) {
+                   void* out, float* part, size_t part_bytes, int* counters, int* err, bool pdl) {
   AttnArgs a{};
   a.q = q;
   a.k_cache = kc;
@@ -172,12 +177,18 @@ AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q
   a.max_seq_len = b.max_seq_len;
   a.partials = part;
   a.partials_bytes = part_bytes;
+  a.counters = counters;
   a.err = err;
+  a.pdl = pdl ? 1 : 0;
   return a;
 }
 
+// The kernels of one layer, in order.  chain: the first kernel may overlap the
+// kernel before it on the stream (one of this library's, inside a stack call);
+// every later kernel overlaps its predecessor in the layer.
 int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const LlamaBatch& b, void* hidden,
-               const void* res_in, void* res_out, void* kc, void* vc, uint8_t* ws, const Layout& L, cudaStream_t s) {
+               const void* res_in, void* res_out, void* kc, void* vc, uint8_t* ws, const Layout& L, bool chain,
+               cudaStream_t s) {
   const int T = b.num_tokens;
   if (T == 0) return LLAMA_OK;
   int* err = device_error_word();
@@ -190,28 +201,40 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   auto a = ws + L.a;
   float* gpart = reinterpret_cast<float*>(ws + L.gpart);
   float* apart = reinterpret_cast<float*>(ws + L.apart);
+  int* acnt = reinterpret_cast<int*>(ws + L.cnt);
   int e;
 
   const int32_t* slot_map = b.slot_mapping;
   if (slot_map == nullptr) {
     e = slot_mapping_launch(b.positions, b.query_start_loc, b.seq_lens, b.block_table, T, b.num_seqs,
-                            b.max_blocks_per_seq, c.block_size, b.num_blocks, slots, err, s);
+                            b.max_blocks_per_seq, c.block_size, b.num_blocks, slots, err, chain, s);
     if (e) return cuda_status(e);
     slot_map = slots;
+    chain = true;
   }
-  // input_layernorm
-  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, s);
+  // input_layernorm; it also clears the attention's arrival counters
+  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, acnt, L.cnt_attn, chain,
+                         s);
   if (e) return cuda_status(e);
+  auto gemm = [&](int epi, const void* A, const void* B, int N, int K, void* out, int ldo) {
+    GemmArgs g{};
+    g.epi = epi;
+    g.A = A;
+    g.B = B;
+    g.M = T;
+    g.N = N;
+    g.K = K;
+    g.out = out;
+    g.ldo = ldo;
+    g.partials = gpart;
+    g.partials_bytes = L.gpart_bytes;
+    g.err = err;
+    g.force_mode = -1;
+    g.pdl = 1;
+    return g;
+  };
   // qkv_proj + RoPE + cache update
-  GemmArgs g{};
-  g.epi = kEpiQkv;
-  g.A = h;
-  g.B = w.w_qkv;
-  g.M = T;
-  g.N = qsz + 2 * kvsz;
-  g.K = H;
-  g.out = q;
-  g.ldo = qsz;
+  GemmArgs g = gemm(kEpiQkv, h, w.w_qkv, qsz + 2 * kvsz, H, q, qsz);
   g.qkv.q_size = qsz;
   g.qkv.kv_size = kvsz;
   g.qkv.head_dim = c.head_dim;
@@ -223,65 +246,22 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   g.qkv.k_cache = kc;
   g.qkv.v_cache = vc;
   g.qkv.rope = rope_of(c);
-  g.partials = gpart;
-  g.partials_bytes = L.gpart_bytes;
-  g.err = err;
-  g.force_mode = -1;
   e = gemm_launch(g, s);
   if (e) return cuda_status(e);
   // attention
-  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, err), s);
+  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, acnt, err, true), s);
   if (e) return cuda_status(e);
   // o_proj -> y (in the h buffer)
-  GemmArgs go{};
-  go.epi = kEpiBf16;
-  go.A = o;
-  go.B = w.w_o;
-  go.M = T;
-  go.N = H;
-  go.K = qsz;
-  go.out = h;
-  go.ldo = H;
-  go.partials = gpart;
-  go.partials_bytes = L.gpart_bytes;
-  go.err = err;
-  go.force_mode = -1;
-  e = gemm_launch(go, s);
+  e = gemm_launch(gemm(kEpiBf16, o, w.w_o, H, qsz, h, H), s);
   if (e) return cuda_status(e);
   // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
-  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, s);
+  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, nullptr, 0, true, s);
   if (e) return cuda_status(e);
   // gate_up_proj + SiluAndMul
-  GemmArgs gu{};
-  gu.epi = kEpiSwiGlu;
-  gu.A = h;
-  gu.B = w.w_gate_up;
-  gu.M = T;
-  gu.N = 2 * I;
-  gu.K = H;
-  gu.out = a;
-  gu.ldo = I;
-  gu.partials = gpart;
-  gu.partials_bytes = L.gpart_bytes;
-  gu.err = err;
-  gu.force_mode = -1;
-  e = gemm_launch(gu, s);
+  e = gemm_launch(gemm(kEpiSwiGlu, h, w.w_gate_up, 2 * I, H, a, I), s);
   if (e) return cuda_status(e);
   // down_proj -> hidden_states
-  GemmArgs gd{};
-  gd.epi = kEpiBf16;
-  gd.A = a;
-  gd.B = w.w_down;
-  gd.M = T;
-  gd.N = H;
-  gd.K = I;
-  gd.out = hidden;
-  gd.ldo = H;
-  gd.partials = gpart;
-  gd.partials_bytes = L.gpart_bytes;
-  gd.err = err;
-  gd.force_mode = -1;
-  e = gemm_launch(gd, s);
+  e = gemm_launch(gemm(kEpiBf16, a, w.w_down, H, I, hidden, H), s);
   return cuda_status(e);
 }
 
@@ -325,7 +305,7 @@ int llama_layer_forward(const LlamaLayerConfig* cfg, const LlamaLayerWeights* we
   const Layout L = make_layout(*cfg, batch->num_tokens, batch->num_seqs, batch->max_seq_len, 0);
   if (workspace == nullptr || workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
   return layer_impl(*cfg, *weights, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache,
-                    ws_base(workspace), L, reinterpret_cast<cudaStream_t>(stream));
+                    ws_base(workspace), L, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const LlamaLayerWeights* layers,
@@ -357,18 +337,18 @@ int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const Llama
   const int T = batch->num_tokens, B = batch->num_seqs, H = cfg->hidden;
   int e;
   if (embed_w) {
-    e = embed_launch(embed_w, input_ids, T, H, vocab, hidden_states, err, s);
+    e = embed_launch(embed_w, input_ids, T, H, vocab, hidden_states, err, false, s);
     if (e) return LLAMA_ERR_CUDA;
   }
   for (int l = 0; l < num_layers; ++l) {
     st = layer_impl(*cfg, layers[l], *batch, hidden_states, l == 0 ? nullptr : residual, residual, k_caches[l],
-                    v_caches[l], ws, L, s);
+                    v_caches[l], ws, L, l > 0 || embed_w != nullptr, s);
     if (st) return st;
   }
   // final norm over the last token of every sequence
   void* hf = ws + L.hf;
   e = add_rmsnorm_launch(hidden_states, residual, nullptr, hf, final_norm_w, B, H, cfg->rms_eps,
-                         batch->query_start_loc, s);
+                         batch->query_start_loc, nullptr, 0, true, s);
   if (e) return LLAMA_ERR_CUDA;
   float* logits = out_logits ? out_logits : reinterpret_cast<float*>(ws + L.logits);
   GemmArgs g{};
@@ -384,9 +364,10 @@ int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const Llama
   g.partials_bytes = L.gpart_bytes;
   g.err = err;
   g.force_mode = -1;
+  g.pdl = 1;
   e = gemm_launch(g, s);
   if (e) return LLAMA_ERR_CUDA;
-  e = argmax_launch(logits, B, vocab, out_tokens, s);
+  e = argmax_launch(logits, B, vocab, out_tokens, true, s);
   return e ? LLAMA_ERR_CUDA : LLAMA_OK;
 }
 
@@ -403,7 +384,27 @@ int kv_cache_write(const void* k, const void* v, const int32_t* slot_mapping, in
   return cuda_status(e);
 }
 
-size_t llama_linear_workspace_size(void) { return gemm_partials_bytes(num_sms()) + 256; }
+}  // extern "C"
+
+namespace {
+
+// A GEMM on its own, with its partial tiles in the caller's workspace.
+int standalone_gemm(GemmArgs& g, void* workspace, cudaStream_t s) {
+  g.partials = reinterpret_cast<float*>(ws_base(workspace));
+  g.partials_bytes = gemm_partials_bytes(num_sms());
+  g.err = device_error_word();
+  g.force_mode = -1;
+  g.pdl = 0;
+  return gemm_launch(g, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t llama_linear_workspace_size(void) {
+  return gemm_partials_bytes(num_sms()) + 256;
+}
 
 int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int out_fp32, void* workspace,
                  size_t workspace_bytes, llama_stream_t stream) {
@@ -422,11 +423,7 @@ int llama_linear(const void* x, const void* w, int M, int N, int K, void* y, int
   g.K = K;
   g.out = y;
   g.ldo = N;
-  g.partials = reinterpret_cast<float*>(ws_base(workspace));
-  g.partials_bytes = gemm_partials_bytes(num_sms());
-  g.err = device_error_word();
-  g.force_mode = -1;
-  return cuda_status(gemm_launch(g, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(standalone_gemm(g, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_gate_up_silu(const void* x, const void* w_gate_up, int M, int I, int K, void* a, void* workspace,
@@ -446,11 +443,7 @@ int llama_gate_up_silu(const void* x, const void* w_gate_up, int M, int I, int K
   g.K = K;
   g.out = a;
   g.ldo = I;
-  g.partials = reinterpret_cast<float*>(ws_base(workspace));
-  g.partials_bytes = gemm_partials_bytes(num_sms());
-  g.err = device_error_word();
-  g.force_mode = -1;
-  return cuda_status(gemm_launch(g, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(standalone_gemm(g, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residual_out, void* h, const void* gamma,
@@ -461,8 +454,8 @@ int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residu
   if (!a16(x) || !a16(h) || !a16(gamma) || (residual_in && !a16(residual_in)) ||
       (residual_out && !a16(residual_out)))
     return LLAMA_ERR_UNSUPPORTED;
-  return cuda_status(add_rmsnorm_launch(x, residual_in, residual_out, h, gamma, rows, H, eps, nullptr,
-                                        reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(add_rmsnorm_launch(x, residual_in, residual_out, h, gamma, rows, H, eps, nullptr, nullptr, 0,
+                                        false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
@@ -474,12 +467,19 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
   if (batch->num_tokens == 0) return LLAMA_OK;
   if (!q || !k_cache || !v_cache || !out) return LLAMA_ERR_ARG;
   if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return LLAMA_ERR_UNSUPPORTED;
-  const size_t need =
-      attn_partials_bytes(batch->num_seqs, batch->num_tokens, batch->max_seq_len, cfg->n_heads, cfg->head_dim) + 256;
-  if (workspace == nullptr || workspace_bytes < need) return LLAMA_ERR_WORKSPACE;
-  AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws_base(workspace)),
-                         need - 256, device_error_word());
-  return cuda_status(attention_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+  const int B = batch->num_seqs, T = batch->num_tokens, S = batch->max_seq_len;
+  const size_t part = attn_partials_bytes(B, T, S, cfg->n_heads, cfg->head_dim);
+  const size_t ncnt = attn_counter_count(B, cfg->n_kv_heads);
+  if (workspace == nullptr ||
+      workspace_bytes < attn_workspace_bytes(B, T, S, cfg->n_heads, cfg->n_kv_heads, cfg->head_dim))
+    return LLAMA_ERR_WORKSPACE;
+  uint8_t* ws = ws_base(workspace);
+  int* counters = reinterpret_cast<int*>(ws + attn_workspace_counter_offset(B, T, S, cfg->n_heads, cfg->head_dim));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(counters, 0, ncnt * sizeof(int), s) != cudaSuccess) return LLAMA_ERR_CUDA;
+  AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws), part, counters,
+                         device_error_word(), false);
+  return cuda_status(attention_launch(a, s));
 }
 
 int llama_get_device_error(llama_stream_t stream, int* detail) {

@@ -13,7 +13,8 @@
 //   of the context); its 4 warps stream disjoint blocks of the chunk through
 //   their own 3-stage TMA rings with the group's q heads as the 16 MMA rows,
 //   merge in shared memory, and either write the output (one chunk) or a
-//   partial (unnormalised o, running max, sum) that k_attn_combine merges.
+//   partial (unnormalised o, running max, sum).  The chunk CTA that completes
+//   the (sequence, KV head) arrival count merges the partials, in chunk order.
 // * prefill (query length >= 2): one CTA per (sequence, KV head, 16 query
 //   tokens); warp w owns q head w of the group; a producer warp streams
 //   64-key K/V tiles through a 2-stage ring; fully masked tiles are skipped.
@@ -29,6 +30,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace llama {
 
@@ -54,6 +56,7 @@ struct AttnParams {
   float* part_o;
   float2* part_ml;
   uint32_t* pre_items;  // prefill work list: (sequence << 16) | q-tile, 0xFFFFFFFF past the end
+  int* counters;        // [B][nkv] split-KV arrival counts
   int* err;
 };
 
@@ -132,7 +135,10 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   const uint32_t ring = raw + pad;                                   // [warp][stage][K | V]
   uint8_t* qtile = smem + kDecWarps * kDecStages * 2 * TB;           // [16][D + 8] bf16
   uint64_t* bars = reinterpret_cast<uint64_t*>(qtile + 16 * QS);     // [warp][stage]
+  __shared__ int merge_here;
 
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.z, kvh = blockIdx.y, chunk = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = p.qsl[b];
@@ -333,32 +339,85 @@ __global__ void __launch_bounds__(kDecWarps * 32)
       if (col == 0) p.part_ml[pi] = make_float2(M, L);
     }
   }
-}
+  if (nch == 1) return;
 
-template <int D>
-__global__ void k_attn_combine(AttnParams p) {
-  const int b = blockIdx.y, h = blockIdx.x, col = threadIdx.x;
-  const int t0 = p.qsl[b];
-  if (p.qsl[b + 1] - t0 != 1) return;
-  const int pos = p.positions[t0];
-  const int n_keys = pos + 1;
-  if (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) return;
-  const int nch = num_chunks((n_keys + kBS - 1) / kBS);
-  if (nch <= 1 || nch > p.max_chunks) return;
-  const size_t base = static_cast<size_t>(b) * p.max_chunks * p.nq + h;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(c) * p.nq].x);
-  float L = 0.f, O = 0.f;
-  if (M != -INFINITY) {
+  // Count this chunk in; the CTA that completes the count merges all chunks
+  // of the group's heads in chunk order (the same result whichever CTA it is).
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* cnt = p.counters + b * p.nkv + kvh;
+    const int last = atomicAdd(cnt, 1) == nch - 1;
+    if (last) atomicExch(cnt, 0);  // every chunk is in: ready for the next launch
+    merge_here = last;
+  }
+  __syncthreads();
+  if (!merge_here) return;
+  __threadfence();
+  // chunk weights f = 2^(m_c - M) and the normaliser L per head, in shared
+  // memory (the ring is free again); the sums run in chunk order
+  // (4 * G * (2 * nch + 1) bytes: within the ring and q tile for every
+  // G <= 16 and nch <= kMaxSeqLen / 512)
+  float* fw = reinterpret_cast<float*>(smem);  // [G][nch] running maxima, then weights
+  float* lsum = fw + G * nch;                  // [G][nch] partial sums
+  float* ltot = lsum + G * nch;                // [G]
+  const size_t sb = static_cast<size_t>(b) * p.max_chunks * p.nq + kvh * G;  // (chunk 0, head kvh*G)
+  for (int i = threadIdx.x; i < G * nch; i += blockDim.x) {
+    const int r = i / nch, c = i % nch;
+    const float2 ml = __ldcg(p.part_ml + sb + static_cast<size_t>(c) * p.nq + r);
+    fw[i] = ml.x;
+    lsum[i] = ml.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int r = threadIdx.x;
+    float M = -INFINITY;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, fw[r * nch + c]);
+    float L = 0.f;
     for (int c = 0; c < nch; ++c) {
-      const size_t pi = base + static_cast<size_t>(c) * p.nq;
-      const float2 ml = p.part_ml[pi];
-      const float f = exp2f(ml.x - M);
-      L += ml.y * f;
-      O += p.part_o[pi * D + col] * f;
+      const float f = M == -INFINITY ? 0.f : exp2f(fw[r * nch + c] - M);
+      fw[r * nch + c] = f;
+      L += lsum[r * nch + c] * f;
+    }
+    ltot[r] = L;
+  }
+  __syncthreads();
+  constexpr int kPer = 16 * D / (kDecWarps * 32);  // elements per thread, 16 rows x D
+  constexpr int kU = 4;                             // chunks whose loads are in flight together
+  float O[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) O[k] = 0.f;
+  const float* po = p.part_o + sb * D;
+  for (int c0 = 0; c0 < nch; c0 += kU) {
+    float v[kU][kPer];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = threadIdx.x + k * kDecWarps * 32;
+        const int r = idx / D;
+        v[u][k] = (c0 + u < nch && r < G) ? __ldcg(po + (static_cast<size_t>(c0 + u) * p.nq + r) * D + idx % D)
+                                          : 0.f;
+      }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (c0 + u >= nch) break;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int r = (threadIdx.x + k * kDecWarps * 32) / D;
+        if (r < G) O[k] += v[u][k] * fw[r * nch + c0 + u];
+      }
     }
   }
-  p.out[static_cast<size_t>(t0) * p.nq * D + h * D + col] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int idx = threadIdx.x + k * kDecWarps * 32;
+    const int r = idx / D, col = idx % D;
+    if (r < G) {
+      const float L = ltot[r];
+      p.out[static_cast<size_t>(t0) * p.nq * D + (kvh * G + r) * D + col] = __float2bfloat16_rn(L > 0.f ? O[k] / L : 0.f);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -372,6 +431,8 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const int32_t* __restrict__ 
                                                     uint32_t* items, int max_items) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
@@ -427,6 +488,8 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
   uint64_t* bars = reinterpret_cast<uint64_t*>(qtiles + kPreMaxHeads * 16 * QS);  // full[S], empty[S]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kPreStages);
 
+  pdl_wait();
+  pdl_trigger();
   const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;  // head chunks per KV head
   const uint32_t item = p.pre_items[blockIdx.y];
   if (item == kNoItem) return;
@@ -704,6 +767,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     k_attn_prefill_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
+  pdl_wait();
+  pdl_trigger();
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   if (pad > kTcSlack) {  // the dynamic shared memory base is 1024-aligned in practice
@@ -1120,22 +1185,28 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   p.max_chunks = num_chunks(max_blk);
   if (p.max_chunks < 1) p.max_chunks = 1;
-  dim3 gd(p.max_chunks, a.nkv, a.B);
-  k_attn_decode<D><<<gd, kDecWarps * 32, decode_smem<D>(), s>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.max_chunks > 1) {
-    k_attn_combine<D><<<dim3(a.nq, a.B), D, 0, s>>>(p);
-    e = cudaGetLastError();
+  if (p.max_chunks > 1 && p.counters == nullptr) return cudaErrorInvalidValue;
+  if (a.max_seq_len > kMaxSeqLen) return cudaErrorInvalidValue;
+  // the first kernel takes the caller's dependency mode, the others follow it
+  bool pdl = a.pdl != 0;
+  auto next_pdl = [&]() {
+    const bool r = pdl;
+    pdl = true;
+    return r;
+  };
+  const bool tc = a.max_query_len >= 2 && D == 128 && 128 % p.group == 0;
+  const int tile_tokens = tc ? 128 / p.group : 16;  // tensor-core prefill: 128 rows = tokens x group heads
+  const int items = (a.T + tile_tokens - 1) / tile_tokens + a.B;
+  cudaError_t e;
+  if (a.max_query_len >= 2) {
+    e = launch_kernel(k_attn_plan, dim3(1), dim3(1024), 0, s, next_pdl(), a.qsl, a.B, tile_tokens, p.pre_items,
+                      items);
     if (e != cudaSuccess) return e;
   }
-  if (a.max_query_len >= 2 && D == 128 && 128 % p.group == 0) {
-    // tensor-core prefill: 128 / group tokens per tile
-    const int qt_tokens = 128 / p.group;
-    const int items = (a.T + qt_tokens - 1) / qt_tokens + a.B;
-    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, qt_tokens, p.pre_items, items);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  dim3 gd(p.max_chunks, a.nkv, a.B);
+  e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), s, next_pdl(), tk, tv, p);
+  if (e != cudaSuccess || a.max_query_len < 2) return e;
+  if (tc) {
     static std::once_flag tc_once;
     static cudaError_t tc_attr = cudaSuccess;
     std::call_once(tc_once, [] {
@@ -1143,31 +1214,34 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
     });
     if (tc_attr != cudaSuccess) return tc_attr;
     CUtensorMap tq;
-    if (!make_q_tmap(&tq, a.q, a.T, a.nq, p.group, qt_tokens)) return cudaErrorInvalidValue;
-    k_attn_prefill_tc<<<dim3(a.nkv, items), kTcThreads, kTcSmem, s>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    if (!make_q_tmap(&tq, a.q, a.T, a.nq, p.group, tile_tokens)) return cudaErrorInvalidValue;
+    return launch_kernel(k_attn_prefill_tc, dim3(a.nkv, items), dim3(kTcThreads), kTcSmem, s, next_pdl(), tq, tk,
+                         tv, p);
   }
-  if (a.max_query_len >= 2) {
-    const int items = (a.T + 15) / 16 + a.B;
-    k_attn_plan<<<1, 1024, 0, s>>>(a.qsl, a.B, 16, p.pre_items, items);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
-    const int warps = (p.group < kPreMaxHeads ? p.group : kPreMaxHeads) + 1;
-    dim3 gp(a.nkv * n_hc, items);
-    k_attn_prefill<D><<<gp, warps * 32, prefill_smem<D>(), s>>>(tk, tv, p);
-    e = cudaGetLastError();
-  }
-  return e;
+  const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
+  const int warps = (p.group < kPreMaxHeads ? p.group : kPreMaxHeads) + 1;
+  return launch_kernel(k_attn_prefill<D>, dim3(a.nkv * n_hc, items), dim3(warps * 32), prefill_smem<D>(), s,
+                       next_pdl(), tk, tv, p);
 }
 
 }  // namespace
+
+size_t attn_counter_count(int B, int nkv) { return static_cast<size_t>(B > 0 ? B : 1) * nkv; }
 
 size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim) {
   const int nch = num_chunks((max_seq_len + kBS - 1) / kBS);
   const size_t n = static_cast<size_t>(B) * (nch < 1 ? 1 : nch) * nq;
   return n * head_dim * sizeof(float) + n * sizeof(float2) +
          static_cast<size_t>(max_prefill_items(T, B)) * sizeof(uint32_t) + 256;
+}
+
+size_t attn_workspace_counter_offset(int B, int T, int max_seq_len, int nq, int head_dim) {
+  return (attn_partials_bytes(B, T, max_seq_len, nq, head_dim) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t attn_workspace_bytes(int B, int T, int max_seq_len, int nq, int nkv, int head_dim) {
+  const size_t cnt = (attn_counter_count(B, nkv) * sizeof(int) + 255) & ~static_cast<size_t>(255);
+  return attn_workspace_counter_offset(B, T, max_seq_len, nq, head_dim) + cnt + 256;
 }
 
 int attention_launch(const AttnArgs& a, cudaStream_t s) {
@@ -1190,6 +1264,7 @@ int attention_launch(const AttnArgs& a, cudaStream_t s) {
   p.group = a.nq / a.nkv;
   p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.head_dim));
   p.err = a.err;
+  p.counters = a.counters;
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   const size_t n = static_cast<size_t>(a.B) * (num_chunks(max_blk) < 1 ? 1 : num_chunks(max_blk)) * a.nq;
   if (attn_partials_bytes(a.B, a.T, a.max_seq_len, a.nq, a.head_dim) > a.partials_bytes) return cudaErrorInvalidValue;

@@ -52,6 +52,23 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream is still
+// running.  pdl_wait() returns once that kernel has completed and its writes
+// are visible (at once if the launch had no such dependency).  Every kernel of
+// this library calls it in every CTA before its first read of data another
+// kernel of the chain wrote and before its first global write, so a kernel's
+// completion implies its predecessor's.  pdl_trigger() lets the next kernel
+// start; kernels call it only after their own pdl_wait(), so at most two
+// kernels overlap and the data read before pdl_wait() (weights, batch
+// metadata) is data no kernel of the chain writes.  A kernel that never calls
+// it triggers the next one when it completes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -17,7 +17,9 @@
 // data-parallel (whole tiles, grouped raster for L2 reuse); problems with few
 // tiles (decode) are split stream-K: every CTA gets an equal share of the
 // (tile, k-block) units, partial tiles go to a workspace and a fixup kernel
-// sums them in a fixed order and applies the same epilogue.
+// sums them in CTA order (a fixed order, so the result is deterministic) and
+// applies the same epilogue, spread over many CTAs so the partial reads run
+// in parallel.
 //
 // Sources: [WALKTHROUGH] "模型库与算子层 — 代码走读", Linear layers (F.linear with
 // Parameter(out, in)); [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", §4
@@ -26,10 +28,13 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace llama {
 
@@ -59,6 +64,7 @@ struct GemmParams {
   float* partials;
   int* err;
   QkvEpilogueArgs qkv;
+  float2 rope_tab[64];  // qkv epilogue: per rotated pair, revolutions per position as (hi, lo)
 };
 
 struct Work {
@@ -99,6 +105,14 @@ __host__ __device__ __forceinline__ long long sk_start(long long units, int grid
   return units * c / grid;
 }
 
+// the CTA whose stream-K range holds unit u
+__device__ __forceinline__ int sk_owner(const GemmParams& p, long long u) {
+  int c = static_cast<int>((u * p.grid) / p.units);
+  while (c + 1 < p.grid && sk_start(p.units, p.grid, c + 1) <= u) ++c;
+  while (c > 0 && sk_start(p.units, p.grid, c) > u) --c;
+  return c;
+}
+
 // ---------------------------------------------------------------------------
 // RoPE frequency table: per pair i, the rotation rate in revolutions per
 // position, r_i = inv_freq'_i / (2 pi), split into a float pair (hi, lo) so
@@ -107,10 +121,12 @@ __host__ __device__ __forceinline__ long long sk_start(long long units, int grid
 // orig/high_freq_factor keep their frequency, longer than orig/low_freq_factor
 // are divided by factor, in between they blend linearly in orig/wavelength.
 // ---------------------------------------------------------------------------
-__device__ void build_rope_table(const RopeParams& rp, int head_dim, float2* tab, int tid, int nthreads) {
+// Computed once per launch on the host, in double precision (the device's
+// FP64 rate is low and the fixup kernel would pay for it on its critical path).
+void rope_table_host(const RopeParams& rp, int head_dim, float2* tab) {
   const int half = head_dim / 2;
-  for (int i = tid; i < half; i += nthreads) {
-    double inv = pow(static_cast<double>(rp.theta), -2.0 * i / head_dim);
+  for (int i = 0; i < half; ++i) {
+    double inv = std::pow(static_cast<double>(rp.theta), -2.0 * i / head_dim);
     if (rp.llama3) {
       const double two_pi = 6.283185307179586476925287;
       const double lam = two_pi / inv;
@@ -129,6 +145,10 @@ __device__ void build_rope_table(const RopeParams& rp, int head_dim, float2* tab
     const float rl = static_cast<float>(r - static_cast<double>(rh));
     tab[i] = make_float2(rh, rl);
   }
+}
+
+__device__ __forceinline__ void copy_rope_table(const GemmParams& p, float2* tab, int tid, int nthreads) {
+  for (int i = tid; i < p.qkv.head_dim / 2; i += nthreads) tab[i] = p.rope_tab[i];
 }
 
 // sin/cos of 2*pi*pos*r with r = (hi + lo): the product pos*hi is split into
@@ -375,29 +395,37 @@ struct TmemLoader {
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const { tmem_ld32(taddr + col, v); }
 };
 
-// Sum of the partial tiles that the CTAs covering part of a split tile left
-// in the workspace, in CTA order.
+// Partial tiles in the workspace: two slots per CTA (its first work item, and
+// the split tile that ends its range), each [BN / 4][BM] float4, so 32
+// consecutive rows of one 4-column group are 512 contiguous bytes.
+__device__ __forceinline__ float4* partial_slot(float* partials, int cta, int slot) {
+  return reinterpret_cast<float4*>(partials) + (static_cast<size_t>(cta) * 2 + slot) * (BM * BN / 4);
+}
+
+// Sum of the partial tiles that CTAs c_first..c_last left for one tile, in
+// CTA order.  A CTA whose range starts inside the tile holds it in slot 0
+// (its first work item), the others in slot 1.
 struct PartialLoader {
-  const float* partials;
-  long long units, t0, t1;
-  int grid, c_first, row;
+  float* partials;
+  long long units, t0;
+  int grid, c_first, c_last, row;
+  bool valid;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = 0.f;
-    for (int c = c_first; c < grid; ++c) {
-      const long long s = sk_start(units, grid, c), e = sk_start(units, grid, c + 1);
-      if (s >= t1) break;
-      if (e <= t0 || s == e) continue;
-      const int slot = s >= t0 ? 0 : 1;
-      const float4* src = reinterpret_cast<const float4*>(partials + (static_cast<size_t>(c) * 2 + slot) * (BM * BN) +
-                                                          static_cast<size_t>(row) * BN + col);
+    if (!valid) return;
+    for (int c = c_first; c <= c_last; ++c) {
+      const int slot = sk_start(units, grid, c) >= t0 ? 0 : 1;
+      const float4* src = partial_slot(partials, c, slot) + (col / 4) * BM + row;
+      float4 t[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t[q] = __ldcg(src + q * BM);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 t = src[q];
-        v[4 * q] += t.x;
-        v[4 * q + 1] += t.y;
-        v[4 * q + 2] += t.z;
-        v[4 * q + 3] += t.w;
+        v[4 * q] += t[q].x;
+        v[4 * q + 1] += t[q].y;
+        v[4 * q + 2] += t[q].z;
+        v[4 * q + 3] += t[q].w;
       }
     }
   }
@@ -405,7 +433,8 @@ struct PartialLoader {
 
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -448,7 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   if constexpr (EPI == kEpiQkv) {
-    if (warp >= 2) build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
+    if (warp >= 2) copy_rope_table(p, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
   }
   tc_fence_before();
   __syncthreads();
@@ -466,6 +495,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
+    // The weight tiles of the first STAGES k-blocks are requested before
+    // waiting for the previous kernel (no kernel of the chain writes weights);
+    // their activation tiles follow once it has completed.
     const uint64_t pol_a = policy_evict_last();
     const uint64_t pol_b = p.b_evict_first ? policy_evict_first() : policy_evict_normal();
     int stage = 0;
@@ -473,6 +505,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t uses[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+    bool waited = false;
+    int n_pre = 0;
+    int pre_kb[STAGES], pre_row[STAGES];
+    auto finish_wait = [&]() {
+      pdl_wait();
+      if (lane == 0)
+        for (int i = 0; i < n_pre; ++i)
+          tma_load_2d(sbase + i * STAGE_BYTES, &tmA, full_bar(i), pre_kb[i] * BK, pre_row[i], pol_a);
+      __syncwarp();
+      waited = true;
+    };
     Work w;
     bool ok = true;
     while (ok && next_work(p, cursor, end, w)) {
@@ -490,18 +533,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
+          if (waited) tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
           tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
           tma_load_2d(sb + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow1, pol_b);
         }
         __syncwarp();
+        if (!waited) {  // stage == n_pre here
+          pre_kb[n_pre] = kb;
+          pre_row[n_pre] = arow;
+          ++n_pre;
+        }
         uses[stage]++;
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
+        if (!waited && n_pre == STAGES) finish_wait();
       }
     }
+    if (!waited) finish_wait();
+    // Every load is queued: the next kernel may be scheduled now.  (A trigger
+    // at the start would park its CTAs beside this persistent kernel for its
+    // whole run.)
+    if (lane == 0) pdl_trigger();
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmProducer);
       *abort_flag = 1;
@@ -511,6 +565,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // its bounded waits start only once the previous kernel has completed
+    pdl_wait();
     constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
     int stage = 0;
     uint32_t phase = 0;
@@ -566,6 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue warps ----------------
     const int quad = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row_in_tile = quad * 32 + lane;
+    pdl_wait();
     int acc = 0;
     uint32_t acc_phase = 0;
     int nseg = 0;
@@ -580,29 +637,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int tm, tn;
       tile_coords(p, w.tile, tm, tn);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      const bool valid = tm * BM + row_in_tile < p.M;
       if (w.kb0 == 0 && w.kb1 == p.kb) {
         TmemLoader ld{taddr};
         epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
       } else {
-        const int slot = nseg == 0 ? 0 : 1;
-        float* dst = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * (BM * BN) +
-                     static_cast<size_t>(row_in_tile) * BN;
-        const bool valid = tm * BM + row_in_tile < p.M;
+        // a split tile: this CTA's partial goes to the workspace
+        float4* dst = partial_slot(p.partials, blockIdx.x, nseg == 0 ? 0 : 1) + row_in_tile;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           tmem_ld32(taddr + c, v);
           if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              dst[(c / 4 + q) * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
       }
       ++nseg;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -619,33 +678,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Sums the stream-K partial tiles of every tile that was split across CTAs
-// (fixed CTA order, so the result is deterministic) and applies the epilogue.
-// One thread per (row, column unit): a tile is spread over BM / kRows CTAs so
-// the partial reads of a decode-sized problem run on many SMs at once.
-constexpr int kFixThreads = 256;
+// and applies the epilogue.  One thread per (row, column unit): warp w of a
+// CTA finishes unit w for 32 consecutive rows (its lanes), so every partial
+// load of a warp is 512 contiguous bytes, and a tile is spread over BM / 32
+// CTAs so the reads of a decode-sized problem run on many SMs at once.
+constexpr int kFixRows = 32;
 
 template <int EPI>
-__global__ void __launch_bounds__(kFixThreads) k_gemm_fixup(GemmParams p) {
+__global__ void __launch_bounds__(EpiUnits<EPI>::kUnits * 32) k_gemm_fixup(const __grid_constant__ GemmParams p) {
   constexpr int kUnits = EpiUnits<EPI>::kUnits;
-  constexpr int kRows = kFixThreads / kUnits;
   __shared__ float2 rope_tab[64];
+  pdl_wait();
+  pdl_trigger();
   const int tile = blockIdx.x;
-  const long long t0 = static_cast<long long>(tile) * p.kb, t1 = t0 + p.kb;
-  // first CTA whose range contains unit t0
-  int c = static_cast<int>((t0 * p.grid) / p.units);
-  while (c + 1 < p.grid && sk_start(p.units, p.grid, c + 1) <= t0) ++c;
-  while (c > 0 && sk_start(p.units, p.grid, c) > t0) --c;
-  if (sk_start(p.units, p.grid, c) <= t0 && sk_start(p.units, p.grid, c + 1) >= t1) return;  // whole tile in one CTA
+  const long long t0 = static_cast<long long>(tile) * p.kb;
+  const int c_first = sk_owner(p, t0), c_last = sk_owner(p, t0 + p.kb - 1);
+  if (c_first == c_last) return;  // the whole tile was in one CTA
   int tm, tn;
   tile_coords(p, tile, tm, tn);
-  if (tm * BM + static_cast<int>(blockIdx.y) * kRows >= p.M) return;  // no valid row in this CTA
+  if (tm * BM + static_cast<int>(blockIdx.y) * kFixRows >= p.M) return;  // no valid row in this CTA
   if constexpr (EPI == kEpiQkv) {
-    build_rope_table(p.qkv.rope, p.qkv.head_dim, rope_tab, threadIdx.x, kFixThreads);
+    copy_rope_table(p, rope_tab, threadIdx.x, kUnits * 32);
     __syncthreads();
   }
-  const int row_in_tile = blockIdx.y * kRows + threadIdx.x / kUnits;
-  const int unit = threadIdx.x % kUnits;
-  PartialLoader ld{p.partials, p.units, t0, t1, p.grid, c, row_in_tile};
+  const int unit = threadIdx.x >> 5;
+  const int row_in_tile = blockIdx.y * kFixRows + (threadIdx.x & 31);
+  PartialLoader ld{p.partials, p.units, t0, p.grid, c_first, c_last, row_in_tile, tm * BM + row_in_tile < p.M};
   epilogue_unit<EPI>(p, tm, tn, row_in_tile, unit, ld, rope_tab);
 }
 
@@ -686,22 +744,17 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int bo
 }
 
 template <int EPI>
-int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t s) {
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, bool pdl, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  k_gemm_tc<EPI><<<p.grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.sk) {
-    constexpr int kRows = kFixThreads / EpiUnits<EPI>::kUnits;
-    k_gemm_fixup<EPI><<<dim3(p.tiles, BM / kRows), kFixThreads, 0, s>>>(p);
-    e = cudaGetLastError();
-  }
-  return e;
+  cudaError_t e = launch_kernel(k_gemm_tc<EPI>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
+  if (e != cudaSuccess || !p.sk) return e;
+  return launch_kernel(k_gemm_fixup<EPI>, dim3(p.tiles, BM / kFixRows), dim3(EpiUnits<EPI>::kUnits * 32), 0, s,
+                       true, p);
 }
 
 }  // namespace
@@ -718,6 +771,10 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.ldo = a.ldo;
   p.err = a.err;
   p.qkv = a.qkv;
+  if (a.epi == kEpiQkv) {
+    if (a.qkv.head_dim > 128 || a.qkv.head_dim % 64) return cudaErrorInvalidValue;
+    rope_table_host(a.qkv.rope, a.qkv.head_dim, p.rope_tab);
+  }
   p.partials = a.partials;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.kb = (a.K + BK - 1) / BK;
@@ -762,13 +819,13 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   if (!make_tmap_bf16(&tb, a.B, a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
   switch (a.epi) {
     case kEpiBf16:
-      return launch_typed<kEpiBf16>(ta, tb, p, s);
+      return launch_typed<kEpiBf16>(ta, tb, p, a.pdl != 0, s);
     case kEpiQkv:
-      return launch_typed<kEpiQkv>(ta, tb, p, s);
+      return launch_typed<kEpiQkv>(ta, tb, p, a.pdl != 0, s);
     case kEpiSwiGlu:
-      return launch_typed<kEpiSwiGlu>(ta, tb, p, s);
+      return launch_typed<kEpiSwiGlu>(ta, tb, p, a.pdl != 0, s);
     case kEpiF32:
-      return launch_typed<kEpiF32>(ta, tb, p, s);
+      return launch_typed<kEpiF32>(ta, tb, p, a.pdl != 0, s);
     default:
       return cudaErrorInvalidValue;
   }

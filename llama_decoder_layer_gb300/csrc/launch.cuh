@@ -1,0 +1,31 @@
+// Host-side kernel launch with an optional programmatic dependency on the
+// kernel before it on the stream (see pdl_wait / pdl_trigger in common.cuh).
+// The first kernel of a public call is launched without it, so it starts only
+// after everything the caller queued earlier has completed; the kernels after
+// it in the same call overlap their prologues (barrier setup, tensor-memory
+// allocation, weight prefetch) with the tail of their predecessor.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace llama {
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace llama

@@ -1,7 +1,10 @@
 // Row-wise and indexing kernels: fused residual-add + RMSNorm, cache slot
 // mapping, the standalone paged-cache write, the embedding gather and the
 // greedy argmax.  All are HBM-bound: 16-byte vector loads/stores, fp32
-// arithmetic, warp-shuffle reductions.
+// arithmetic, warp-shuffle reductions.  They wait for the kernel before them
+// (pdl_wait) but do not trigger the next one early: a norm over thousands of
+// rows that let the following GEMM in early made the 70B prefill layer ~8%
+// slower (measured), so the next kernel starts when they complete.
 //
 // Sources: [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", §3
 // input_layernorm (RMSNorm fused with the residual add; residual None on the
@@ -13,6 +16,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace llama {
 
@@ -44,8 +48,12 @@ template <int MAXC>
 __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __restrict__ x, const uint4* res_in,
                                                               uint4* res_out, uint4* h_out,
                                                               const uint4* __restrict__ gamma, int H, float eps,
-                                                              const int32_t* __restrict__ qsl) {
+                                                              const int32_t* __restrict__ qsl, int* zero_ints,
+                                                              int n_zero) {
   __shared__ float red[33];
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_ints[i] = 0;
   const int out_row = blockIdx.x;
   const int in_row = qsl != nullptr ? qsl[out_row + 1] - 1 : out_row;
   const int nch = H >> 3;
@@ -115,6 +123,7 @@ __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __res
 __global__ void k_slot_mapping(const int32_t* __restrict__ positions, const int32_t* __restrict__ qsl,
                                const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table, int T,
                                int B, int max_blocks, int bs, int num_blocks, int32_t* __restrict__ slots, int* err) {
+  pdl_wait();
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
@@ -164,6 +173,7 @@ __global__ void k_kv_write(const uint4* __restrict__ k, const uint4* __restrict_
 
 __global__ void k_embed(const uint4* __restrict__ table, const int32_t* __restrict__ ids, int H, int vocab,
                         uint4* __restrict__ out, int* err) {
+  pdl_wait();
   const int t = blockIdx.x;
   const int id = ids[t];
   const int nch = H >> 3;
@@ -177,6 +187,7 @@ __global__ void k_embed(const uint4* __restrict__ table, const int32_t* __restri
 __global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logits, int vocab, int32_t* out) {
   __shared__ float sv[32];
   __shared__ int si[32];
+  pdl_wait();
   const float* row = logits + static_cast<size_t>(blockIdx.x) * vocab;
   float best = -FLT_MAX;
   int bi = 0x7fffffff;
@@ -230,7 +241,8 @@ int grid_for(long long work, int threads) {
 }  // namespace
 
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma, int rows,
-                       int H, float eps, const int32_t* row_index_qsl, cudaStream_t s) {
+                       int H, float eps, const int32_t* row_index_qsl, int* zero_ints, int n_zero, bool pdl,
+                       cudaStream_t s) {
   if (rows <= 0) return 0;
   const int nch = H / 8;
   const int per = (nch + kNormThreads - 1) / kNormThreads;
@@ -239,26 +251,24 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
   auto RO = static_cast<uint4*>(res_out);
   auto HO = static_cast<uint4*>(h_out);
   auto G = static_cast<const uint4*>(gamma);
-  if (per <= 1)
-    k_add_rmsnorm<1><<<rows, kNormThreads, 0, s>>>(X, R, RO, HO, G, H, eps, row_index_qsl);
-  else if (per <= 2)
-    k_add_rmsnorm<2><<<rows, kNormThreads, 0, s>>>(X, R, RO, HO, G, H, eps, row_index_qsl);
-  else if (per <= 4)
-    k_add_rmsnorm<4><<<rows, kNormThreads, 0, s>>>(X, R, RO, HO, G, H, eps, row_index_qsl);
-  else if (per <= 8)
-    k_add_rmsnorm<8><<<rows, kNormThreads, 0, s>>>(X, R, RO, HO, G, H, eps, row_index_qsl);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (zero_ints == nullptr) n_zero = 0;
+  auto go = [&](auto kernel) {
+    return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl,
+                         zero_ints, n_zero);
+  };
+  if (per <= 1) return go(k_add_rmsnorm<1>);
+  if (per <= 2) return go(k_add_rmsnorm<2>);
+  if (per <= 4) return go(k_add_rmsnorm<4>);
+  if (per <= 8) return go(k_add_rmsnorm<8>);
+  return cudaErrorInvalidValue;
 }
 
 int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* block_table, int T, int B, int max_blocks, int block_size, int num_blocks,
-                        int32_t* slots, int* err, cudaStream_t s) {
+                        int32_t* slots, int* err, bool pdl, cudaStream_t s) {
   if (T <= 0) return 0;
-  k_slot_mapping<<<grid_for(T, 256), 256, 0, s>>>(positions, qsl, seq_lens, block_table, T, B, max_blocks,
-                                                   block_size, num_blocks, slots, err);
-  return cudaGetLastError();
+  return launch_kernel(k_slot_mapping, dim3(grid_for(T, 256)), dim3(256), 0, s, pdl, positions, qsl, seq_lens,
+                       block_table, T, B, max_blocks, block_size, num_blocks, slots, err);
 }
 
 int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, int n_kv, int head_dim,
@@ -271,17 +281,16 @@ int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, i
   return cudaGetLastError();
 }
 
-int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab, void* out, int* err,
+int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab, void* out, int* err, bool pdl,
                  cudaStream_t s) {
   if (T <= 0) return 0;
-  k_embed<<<T, 256, 0, s>>>(static_cast<const uint4*>(table), ids, H, vocab, static_cast<uint4*>(out), err);
-  return cudaGetLastError();
+  return launch_kernel(k_embed, dim3(T), dim3(256), 0, s, pdl, static_cast<const uint4*>(table), ids, H, vocab,
+                       static_cast<uint4*>(out), err);
 }
 
-int argmax_launch(const float* logits, int rows, int vocab, int32_t* out, cudaStream_t s) {
+int argmax_launch(const float* logits, int rows, int vocab, int32_t* out, bool pdl, cudaStream_t s) {
   if (rows <= 0) return 0;
-  k_argmax<<<rows, 1024, 0, s>>>(logits, vocab, out);
-  return cudaGetLastError();
+  return launch_kernel(k_argmax, dim3(rows), dim3(1024), 0, s, pdl, logits, vocab, out);
 }
 
 }  // namespace llama
