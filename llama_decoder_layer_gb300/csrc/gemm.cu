@@ -677,6 +677,233 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Split-K over a thread-block cluster, for problems with at most half as many
+// tiles as SMs (decode-sized M).  The S CTAs of a cluster compute one tile,
+// CTA rank r over k-blocks [r*kb/S, (r+1)*kb/S), and each leaves its fp32
+// accumulator in its own shared memory ([BN/4][BM] float4 in the operand
+// ring, which is idle by then).  After a cluster barrier CTA r finishes the
+// column units u with u % S == r of every row, summing the S slices in rank
+// order through distributed shared memory; a second barrier keeps every
+// slice alive until all reads are done.  No partial tile leaves the chip and
+// no second kernel runs.
+// ---------------------------------------------------------------------------
+struct ClusterLoader {
+  uint32_t slice;  // shared::cta address of this CTA's fp32 slice
+  int S, row;
+  __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+    const uint32_t off = slice + static_cast<uint32_t>(((col / 4) * BM + row) * 16);
+    for (int c = 0; c < S; ++c) {
+      const uint32_t a = mapa_shared(off, static_cast<uint32_t>(c));
+      float4 t[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) t[q] = ld_cluster_f4(a + q * BM * 16);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[4 * q] += t[q].x;
+        v[4 * q + 1] += t[q].y;
+        v[4 * q + 2] += t[q].z;
+        v[4 * q + 3] += t[q].w;
+      }
+    }
+  }
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_cluster(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+
+  uint8_t* meta = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull, drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* rope_tab = reinterpret_cast<float2*>(meta + 512);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int kb0 = static_cast<int>(static_cast<long long>(rank) * p.kb / S);
+  const int kb1 = static_cast<int>(static_cast<long long>(rank + 1) * p.kb / S);
+  int tm, tn;
+  tile_coords(p, tile, tm, tn);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), BN);
+    tmem_relinquish();
+  }
+  if constexpr (EPI == kEpiQkv) {
+    if (warp >= 2) copy_rope_table(p, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (weights of the first stages before the
+    // previous kernel completes, as in k_gemm_tc) ----------------
+    const uint64_t pol_a = policy_evict_last();
+    const uint64_t pol_b = policy_evict_first();
+    const int arow = tm * BM;
+    const int brow0 = tn * p.b_tile_rows;
+    const int brow1 = brow0 + p.b_row_step;
+    uint32_t uses[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool waited = false, ok = true;
+    int n_pre = 0;
+    int pre_kb[STAGES];
+    auto finish_wait = [&]() {
+      pdl_wait();
+      if (lane == 0)
+        for (int i = 0; i < n_pre; ++i)
+          tma_load_2d(sbase + i * STAGE_BYTES, &tmA, full_bar(i), pre_kb[i] * BK, arow, pol_a);
+      __syncwarp();
+      waited = true;
+    };
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+        if (waited) tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
+        tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
+        tma_load_2d(sb + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow1, pol_b);
+      }
+      __syncwarp();
+      if (!waited) pre_kb[n_pre++] = kb;
+      uses[stage]++;
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (!waited && n_pre == STAGES) finish_wait();
+    }
+    if (!waited) finish_wait();
+    if (lane == 0) pdl_trigger();
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmProducer);
+      *abort_flag = 1;
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    pdl_wait();
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, issued = false;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc_mma_f16(tmem_base, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k), idesc,
+                     (kb > kb0 || k > 0) ? 1u : 0u);
+        tc_commit(empty_bar(stage));
+        issued = true;
+      }
+      __syncwarp();
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmMma);
+      *abort_flag = 1;
+    } else if (lane == 0) {
+      tc_commit(tfull_bar);
+    }
+    if (lane == 0 && issued) tc_commit(drain_bar);
+    __syncwarp();
+    if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain_bar, 0, nullptr);
+  } else {
+    // ---------------- epilogue warps: accumulator -> this CTA's slice ----------------
+    pdl_wait();
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    if (mbar_wait(tfull_bar, 0, abort_flag)) {
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      float4* dst = reinterpret_cast<float4*>(smem) + row_in_tile;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[(c / 4 + q) * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    } else {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmEpilogue);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();  // every slice of the cluster is in shared memory
+  if (warp >= 2 && !*abort_flag) {
+    constexpr int kUnits = EpiUnits<EPI>::kUnits;
+    const int e = warp - 2;
+    int item = 0;
+    for (int u = rank; u < kUnits; u += S) {
+      for (int g = 0; g < BM / 32; ++g, ++item) {
+        if ((item & 3) != e || tm * BM + g * 32 >= p.M) continue;
+        const int row_in_tile = g * 32 + lane;
+        ClusterLoader ld{sbase, S, row_in_tile};
+        epilogue_unit<EPI>(p, tm, tn, row_in_tile, u, ld, rope_tab);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // no slice is released while another CTA may still read it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, BN);
+}
+
 // Sums the stream-K partial tiles of every tile that was split across CTAs
 // and applies the epilogue.  One thread per (row, column unit): warp w of a
 // CTA finishes unit w for 32 consecutive rows (its lanes), so every partial
@@ -744,13 +971,73 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int bo
 }
 
 template <int EPI>
-int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, bool pdl, cudaStream_t s) {
+cudaError_t set_smem_attrs() {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
+  static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_gemm_cluster<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
+  return err;
+}
+
+// Clusters of S CTAs of k_gemm_cluster<EPI> that fit on the device at once
+// (they need S SMs of one GPC each); cached per device.
+template <int EPI>
+int max_active_clusters(int S) {
+  constexpr int kDevs = 64;
+  static int cache[kDevs][9] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs || S < 2 || S > 8) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][S] == 0) {
+    int n = -1;
+    if (set_smem_attrs<EPI>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(S * 64);
+      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = static_cast<unsigned>(S);
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int v = 0;
+      if (cudaOccupancyMaxActiveClusters(&v, k_gemm_cluster<EPI>, &cfg) == cudaSuccess && v > 0) n = v;
+      else cudaGetLastError();
+    }
+    cache[dev][S] = n;
+  }
+  return cache[dev][S] > 0 ? cache[dev][S] : 0;
+}
+
+int max_active_clusters_of(int epi, int S) {
+  switch (epi) {
+    case kEpiBf16:
+      return max_active_clusters<kEpiBf16>(S);
+    case kEpiQkv:
+      return max_active_clusters<kEpiQkv>(S);
+    case kEpiSwiGlu:
+      return max_active_clusters<kEpiSwiGlu>(S);
+    case kEpiF32:
+      return max_active_clusters<kEpiF32>(S);
+    default:
+      return 0;
+  }
+}
+
+template <int EPI>
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pdl,
+                 cudaStream_t s) {
+  const cudaError_t attr_err = set_smem_attrs<EPI>();
   if (attr_err != cudaSuccess) return attr_err;
+  if (cluster > 1)
+    return launch_kernel_cluster(k_gemm_cluster<EPI>, dim3(p.tiles * cluster), dim3(NUM_THREADS), SMEM_BYTES, s, pdl,
+                                 cluster, ta, tb, p);
   cudaError_t e = launch_kernel(k_gemm_tc<EPI>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
   if (e != cudaSuccess || !p.sk) return e;
   return launch_kernel(k_gemm_fixup<EPI>, dim3(p.tiles, BM / kFixRows), dim3(EpiUnits<EPI>::kUnits * 32), 0, s,
@@ -800,7 +1087,17 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.b_evict_first = 1;
   p.group_m = p.tiles_m < 24 ? p.tiles_m : 24;
   const int sms = num_sms();
-  bool sk = p.tiles < 2 * sms;
+  // At most sms / 2 tiles: split K over clusters of S CTAs (S as large as the
+  // SMs allow, at least two k-blocks per CTA, all clusters resident at once).
+  int cluster = 0;
+  if ((a.force_mode == -1 || a.force_mode == 2) && p.tiles * 2 <= sms) {
+    for (int S = sms / p.tiles < 8 ? sms / p.tiles : 8; S >= 2; --S) {
+      if (p.kb < 2 * S || max_active_clusters_of(a.epi, S) < p.tiles) continue;
+      cluster = S;
+      break;
+    }
+  }
+  bool sk = cluster == 0 && p.tiles < 2 * sms;
   if (a.force_mode == 0) sk = false;
   if (a.force_mode == 1) sk = true;
   p.units = static_cast<long long>(p.tiles) * p.kb;
@@ -819,13 +1116,13 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   if (!make_tmap_bf16(&tb, a.B, a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
   switch (a.epi) {
     case kEpiBf16:
-      return launch_typed<kEpiBf16>(ta, tb, p, a.pdl != 0, s);
+      return launch_typed<kEpiBf16>(ta, tb, p, cluster, a.pdl != 0, s);
     case kEpiQkv:
-      return launch_typed<kEpiQkv>(ta, tb, p, a.pdl != 0, s);
+      return launch_typed<kEpiQkv>(ta, tb, p, cluster, a.pdl != 0, s);
     case kEpiSwiGlu:
-      return launch_typed<kEpiSwiGlu>(ta, tb, p, a.pdl != 0, s);
+      return launch_typed<kEpiSwiGlu>(ta, tb, p, cluster, a.pdl != 0, s);
     case kEpiF32:
-      return launch_typed<kEpiF32>(ta, tb, p, a.pdl != 0, s);
+      return launch_typed<kEpiF32>(ta, tb, p, cluster, a.pdl != 0, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -31,9 +31,14 @@ def _ws(n):
 # ----------------------------------------------------------------- GEMM
 
 
+# tiles = ceil(M/128) * ceil(N/256) against the SM count (152 on GB300): at most
+# half of it -> split-K over a cluster, up to twice it -> stream-K + fixup,
+# more -> data-parallel.  Ragged M, N and K tails throughout.
 @pytest.mark.parametrize("M,N,K", [
-    (1, 256, 64), (37, 768, 512), (128, 1024, 1376), (300, 1000, 512),   # stream-K split tiles (few tiles)
-    (4096, 4096, 256), (2500, 2304, 192),                                # data-parallel (many tiles), ragged M
+    (37, 768, 512), (128, 1024, 1376), (300, 1000, 512),      # cluster split-K (S = 4, 8, 4)
+    (1, 256, 64), (64, 40960, 512), (200, 20480, 256),        # stream-K (one k-block; 160 tiles; 2 M-tiles)
+    (2500, 2304, 192),                                        # stream-K, 180 tiles of 20 M-tiles
+    (4096, 4096, 256),                                        # data-parallel
 ])
 def test_linear_bf16(M, N, K):
     x = I.normal_bf16((M, K), 1.0, 0.0, 11 + M, DEV)
@@ -55,7 +60,7 @@ def test_linear_fp32_out_and_repeat():
     y1 = y.clone()
     lb.linear(x, w, y, ws)
     torch.cuda.synchronize()
-    assert torch.equal(y, y1), "stream-K reduction is not deterministic"
+    assert torch.equal(y, y1), "split-K reduction is not deterministic"
     ref = O.linear(f32(x), f32(w))
     e = assert_close(f32(y), ref, "linear fp32")
     assert e < 1e-3  # fp32 output: only accumulation-order differences
