@@ -42,8 +42,7 @@
  *     prologue while the one before it finishes (programmatic dependent
  *     launch) and reads that kernel's results only after it has completed.
  *   - A workspace belongs to one call at a time: calls that may overlap on the
- *     GPU need separate workspaces.  Its contents need not be initialised;
- *     the split-KV arrival counters in it are cleared by the call.
+ *     GPU need separate workspaces.  Its contents need not be initialised.
  *   - A call returns LLAMA_OK, or a status code without launching anything
  *     when its arguments are rejected.  No C++ exception crosses the ABI.
  *   - Kernels never trap.  An out-of-range index met on the device (a cache
@@ -136,9 +135,7 @@ typedef struct {
  * block_table[b][pos/16]*16 + pos%16 is derived on the device; a negative
  * slot skips the token's cache write).  Host ints: max_query_len and
  * max_seq_len bound the batch's query lengths and seq_lens (they size the
- * launch grids; a sequence beyond them is reported as a device guard).
- * max_seq_len above 196608 (384 split-KV chunks of 512 keys) is rejected
- * with LLAMA_ERR_UNSUPPORTED. */
+ * launch grids; a sequence beyond them is reported as a device guard). */
 typedef struct {
   int num_tokens;
   int num_seqs;
@@ -227,8 +224,7 @@ int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residu
 /* Causal GQA attention of q [num_tokens, n_heads, head_dim] (already rotated)
  * over the paged caches, for the batch described by `batch`; writes
  * out [num_tokens, n_heads*head_dim].  ([WALKTHROUGH] Attention.)
- * The workspace llama_workspace_size() gives for the batch is large enough;
- * the call clears its split-KV arrival counters with one cudaMemsetAsync. */
+ * The workspace llama_workspace_size() gives for the batch is large enough. */
 int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
                           const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
                           llama_stream_t stream);
@@ -243,13 +239,11 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
  * bytes (32 MiB) inside the library.  Every GPU that loads the library holds it
  * until the process exits.  A batch whose scratch needs more than that
  * (num_seqs * ceil(ceil(max_seq_len/16)/32) * n_heads * (head_dim+2) * 4
- * + 4 * (ceil(num_tokens/8) + num_seqs) + 4 * num_seqs * n_kv_heads bytes,
- * plus up to 1 KiB of alignment) is rejected with LLAMA_ERR_SCRATCH_LIMIT
- * before anything is launched.  The first call on a device looks up the array's device address
+ * + 4 * (ceil(num_tokens/8) + num_seqs) + 256 bytes) is rejected with
+ * LLAMA_ERR_SCRATCH_LIMIT before anything is launched.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one array, so calls that overlap on the GPU race on it:
- * the caller must serialise them.  Nothing in it has to start at zero: the
- * call clears the arrival counters it uses.
+ * the caller must serialise them.  Nothing in it has to start at zero.
  * Arguments and results are those of llama_paged_attention. */
 int llama_paged_attention_noalloc(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q,
                                   const void* k_cache, const void* v_cache, void* out, llama_stream_t stream);

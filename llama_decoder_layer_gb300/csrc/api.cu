@@ -81,14 +81,12 @@ int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
   if (static_cast<long long>(b->num_seqs) * b->max_blocks_per_seq > 0x7fffffffLL) return LLAMA_ERR_ARG;
   if (b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;                   // grid z dimension
   if ((b->num_tokens + 7) / 8 + b->num_seqs > 65535) return LLAMA_ERR_UNSUPPORTED;  // prefill work items
-  if (b->max_seq_len > kMaxSeqLen) return LLAMA_ERR_UNSUPPORTED;  // split-KV merge scratch
   return LLAMA_OK;
 }
 
 struct Layout {
-  size_t slots, h, q, o, a, gpart, apart, cnt, hf, logits, total;
+  size_t slots, h, q, o, a, gpart, apart, hf, logits, total;
   size_t gpart_bytes, apart_bytes;
-  int cnt_attn;  // split-KV arrival counters, one per (sequence, KV head)
 };
 
 Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int vocab) {
@@ -113,9 +111,6 @@ Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int
   L.apart_bytes =
       attn_partials_bytes(B > 0 ? B : 1, T > 0 ? T : 1, max_seq_len > 0 ? max_seq_len : 1, c.n_heads, c.head_dim);
   off += align256(L.apart_bytes);
-  L.cnt = off;
-  L.cnt_attn = static_cast<int>(attn_counter_count(B, c.n_kv_heads));
-  off += align256(static_cast<size_t>(L.cnt_attn) * sizeof(int));
   if (vocab > 0) {
     L.hf = off;
     off += align256(static_cast<size_t>(B) * c.hidden * 2);
@@ -155,7 +150,7 @@ int check_weights(const LlamaLayerWeights* w) {
 }
 
 AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q, const void* kc, const void* vc,
-                   void* out, float* part, size_t part_bytes, int* counters, int* err, bool pdl) {
+                   void* out, float* part, size_t part_bytes, int* err, bool pdl) {
   AttnArgs a{};
   a.q = q;
   a.k_cache = kc;
@@ -177,7 +172,6 @@ AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q
   a.max_seq_len = b.max_seq_len;
   a.partials = part;
   a.partials_bytes = part_bytes;
-  a.counters = counters;
   a.err = err;
   a.pdl = pdl ? 1 : 0;
   return a;
@@ -201,7 +195,6 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   auto a = ws + L.a;
   float* gpart = reinterpret_cast<float*>(ws + L.gpart);
   float* apart = reinterpret_cast<float*>(ws + L.apart);
-  int* acnt = reinterpret_cast<int*>(ws + L.cnt);
   int e;
 
   const int32_t* slot_map = b.slot_mapping;
@@ -212,9 +205,8 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
     slot_map = slots;
     chain = true;
   }
-  // input_layernorm; it also clears the attention's arrival counters
-  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, acnt, L.cnt_attn, chain,
-                         s);
+  // input_layernorm
+  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, chain, s);
   if (e) return cuda_status(e);
   auto gemm = [&](int epi, const void* A, const void* B, int N, int K, void* out, int ldo) {
     GemmArgs g{};
@@ -249,13 +241,13 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   e = gemm_launch(g, s);
   if (e) return cuda_status(e);
   // attention
-  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, acnt, err, true), s);
+  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, err, true), s);
   if (e) return cuda_status(e);
   // o_proj -> y (in the h buffer)
   e = gemm_launch(gemm(kEpiBf16, o, w.w_o, H, qsz, h, H), s);
   if (e) return cuda_status(e);
   // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
-  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, nullptr, 0, true, s);
+  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, true, s);
   if (e) return cuda_status(e);
   // gate_up_proj + SiluAndMul
   e = gemm_launch(gemm(kEpiSwiGlu, h, w.w_gate_up, 2 * I, H, a, I), s);
@@ -348,7 +340,7 @@ int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const Llama
   // final norm over the last token of every sequence
   void* hf = ws + L.hf;
   e = add_rmsnorm_launch(hidden_states, residual, nullptr, hf, final_norm_w, B, H, cfg->rms_eps,
-                         batch->query_start_loc, nullptr, 0, true, s);
+                         batch->query_start_loc, true, s);
   if (e) return LLAMA_ERR_CUDA;
   float* logits = out_logits ? out_logits : reinterpret_cast<float*>(ws + L.logits);
   GemmArgs g{};
@@ -454,8 +446,8 @@ int llama_fused_add_rmsnorm(const void* x, const void* residual_in, void* residu
   if (!a16(x) || !a16(h) || !a16(gamma) || (residual_in && !a16(residual_in)) ||
       (residual_out && !a16(residual_out)))
     return LLAMA_ERR_UNSUPPORTED;
-  return cuda_status(add_rmsnorm_launch(x, residual_in, residual_out, h, gamma, rows, H, eps, nullptr, nullptr, 0,
-                                        false, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(add_rmsnorm_launch(x, residual_in, residual_out, h, gamma, rows, H, eps, nullptr, false,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, const void* q, const void* k_cache,
@@ -467,19 +459,12 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
   if (batch->num_tokens == 0) return LLAMA_OK;
   if (!q || !k_cache || !v_cache || !out) return LLAMA_ERR_ARG;
   if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(out)) return LLAMA_ERR_UNSUPPORTED;
-  const int B = batch->num_seqs, T = batch->num_tokens, S = batch->max_seq_len;
-  const size_t part = attn_partials_bytes(B, T, S, cfg->n_heads, cfg->head_dim);
-  const size_t ncnt = attn_counter_count(B, cfg->n_kv_heads);
-  if (workspace == nullptr ||
-      workspace_bytes < attn_workspace_bytes(B, T, S, cfg->n_heads, cfg->n_kv_heads, cfg->head_dim))
-    return LLAMA_ERR_WORKSPACE;
-  uint8_t* ws = ws_base(workspace);
-  int* counters = reinterpret_cast<int*>(ws + attn_workspace_counter_offset(B, T, S, cfg->n_heads, cfg->head_dim));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(counters, 0, ncnt * sizeof(int), s) != cudaSuccess) return LLAMA_ERR_CUDA;
-  AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws), part, counters,
+  const size_t part =
+      attn_partials_bytes(batch->num_seqs, batch->num_tokens, batch->max_seq_len, cfg->n_heads, cfg->head_dim);
+  if (workspace == nullptr || workspace_bytes < part + 256) return LLAMA_ERR_WORKSPACE;
+  AttnArgs a = attn_args(*cfg, *batch, q, k_cache, v_cache, out, reinterpret_cast<float*>(ws_base(workspace)), part,
                          device_error_word(), false);
-  return cuda_status(attention_launch(a, s));
+  return cuda_status(attention_launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_get_device_error(llama_stream_t stream, int* detail) {

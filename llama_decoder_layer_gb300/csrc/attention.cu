@@ -13,8 +13,10 @@
 //   of the context); its 4 warps stream disjoint blocks of the chunk through
 //   their own 3-stage TMA rings with the group's q heads as the 16 MMA rows,
 //   merge in shared memory, and either write the output (one chunk) or a
-//   partial (unnormalised o, running max, sum).  The chunk CTA that completes
-//   the (sequence, KV head) arrival count merges the partials, in chunk order.
+//   partial (unnormalised o, running max, sum) that k_attn_combine merges in
+//   chunk order.  (Merging in the decode kernel itself, by the chunk CTA that
+//   completes a per-(sequence, KV head) arrival count, was measured slower:
+//   the fence and atomic every chunk CTA then pays hold its SM slot.)
 // * prefill (query length >= 2): one CTA per (sequence, KV head, 16 query
 //   tokens); warp w owns q head w of the group; a producer warp streams
 //   64-key K/V tiles through a 2-stage ring; fully masked tiles are skipped.
@@ -56,7 +58,6 @@ struct AttnParams {
   float* part_o;
   float2* part_ml;
   uint32_t* pre_items;  // prefill work list: (sequence << 16) | q-tile, 0xFFFFFFFF past the end
-  int* counters;        // [B][nkv] split-KV arrival counts
   int* err;
 };
 
@@ -135,7 +136,6 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   const uint32_t ring = raw + pad;                                   // [warp][stage][K | V]
   uint8_t* qtile = smem + kDecWarps * kDecStages * 2 * TB;           // [16][D + 8] bf16
   uint64_t* bars = reinterpret_cast<uint64_t*>(qtile + 16 * QS);     // [warp][stage]
-  __shared__ int merge_here;
 
   pdl_wait();
   pdl_trigger();
@@ -339,85 +339,36 @@ __global__ void __launch_bounds__(kDecWarps * 32)
       if (col == 0) p.part_ml[pi] = make_float2(M, L);
     }
   }
-  if (nch == 1) return;
+}
 
-  // Count this chunk in; the CTA that completes the count merges all chunks
-  // of the group's heads in chunk order (the same result whichever CTA it is).
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int* cnt = p.counters + b * p.nkv + kvh;
-    const int last = atomicAdd(cnt, 1) == nch - 1;
-    if (last) atomicExch(cnt, 0);  // every chunk is in: ready for the next launch
-    merge_here = last;
-  }
-  __syncthreads();
-  if (!merge_here) return;
-  __threadfence();
-  // chunk weights f = 2^(m_c - M) and the normaliser L per head, in shared
-  // memory (the ring is free again); the sums run in chunk order
-  // (4 * G * (2 * nch + 1) bytes: within the ring and q tile for every
-  // G <= 16 and nch <= kMaxSeqLen / 512)
-  float* fw = reinterpret_cast<float*>(smem);  // [G][nch] running maxima, then weights
-  float* lsum = fw + G * nch;                  // [G][nch] partial sums
-  float* ltot = lsum + G * nch;                // [G]
-  const size_t sb = static_cast<size_t>(b) * p.max_chunks * p.nq + kvh * G;  // (chunk 0, head kvh*G)
-  for (int i = threadIdx.x; i < G * nch; i += blockDim.x) {
-    const int r = i / nch, c = i % nch;
-    const float2 ml = __ldcg(p.part_ml + sb + static_cast<size_t>(c) * p.nq + r);
-    fw[i] = ml.x;
-    lsum[i] = ml.y;
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int r = threadIdx.x;
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, fw[r * nch + c]);
-    float L = 0.f;
+// Merges the split-KV partials of every multi-chunk decode sequence: one CTA
+// per (q head, sequence), one thread per output column, chunks in order.
+template <int D>
+__global__ void k_attn_combine(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.y, h = blockIdx.x, col = threadIdx.x;
+  const int t0 = p.qsl[b];
+  if (p.qsl[b + 1] - t0 != 1) return;
+  const int pos = p.positions[t0];
+  const int n_keys = pos + 1;
+  if (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) return;
+  const int nch = num_chunks((n_keys + kBS - 1) / kBS);
+  if (nch <= 1 || nch > p.max_chunks) return;
+  const size_t base = static_cast<size_t>(b) * p.max_chunks * p.nq + h;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(c) * p.nq].x);
+  float L = 0.f, O = 0.f;
+  if (M != -INFINITY) {
     for (int c = 0; c < nch; ++c) {
-      const float f = M == -INFINITY ? 0.f : exp2f(fw[r * nch + c] - M);
-      fw[r * nch + c] = f;
-      L += lsum[r * nch + c] * f;
-    }
-    ltot[r] = L;
-  }
-  __syncthreads();
-  constexpr int kPer = 16 * D / (kDecWarps * 32);  // elements per thread, 16 rows x D
-  constexpr int kU = 4;                             // chunks whose loads are in flight together
-  float O[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) O[k] = 0.f;
-  const float* po = p.part_o + sb * D;
-  for (int c0 = 0; c0 < nch; c0 += kU) {
-    float v[kU][kPer];
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int idx = threadIdx.x + k * kDecWarps * 32;
-        const int r = idx / D;
-        v[u][k] = (c0 + u < nch && r < G) ? __ldcg(po + (static_cast<size_t>(c0 + u) * p.nq + r) * D + idx % D)
-                                          : 0.f;
-      }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (c0 + u >= nch) break;
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int r = (threadIdx.x + k * kDecWarps * 32) / D;
-        if (r < G) O[k] += v[u][k] * fw[r * nch + c0 + u];
-      }
+      const size_t pi = base + static_cast<size_t>(c) * p.nq;
+      const float2 ml = p.part_ml[pi];
+      const float f = exp2f(ml.x - M);
+      L += ml.y * f;
+      O += p.part_o[pi * D + col] * f;
     }
   }
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int idx = threadIdx.x + k * kDecWarps * 32;
-    const int r = idx / D, col = idx % D;
-    if (r < G) {
-      const float L = ltot[r];
-      p.out[static_cast<size_t>(t0) * p.nq * D + (kvh * G + r) * D + col] = __float2bfloat16_rn(L > 0.f ? O[k] / L : 0.f);
-    }
-  }
+  p.out[static_cast<size_t>(t0) * p.nq * D + h * D + col] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -1185,8 +1136,6 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   p.max_chunks = num_chunks(max_blk);
   if (p.max_chunks < 1) p.max_chunks = 1;
-  if (p.max_chunks > 1 && p.counters == nullptr) return cudaErrorInvalidValue;
-  if (a.max_seq_len > kMaxSeqLen) return cudaErrorInvalidValue;
   // the first kernel takes the caller's dependency mode, the others follow it
   bool pdl = a.pdl != 0;
   auto next_pdl = [&]() {
@@ -1205,7 +1154,12 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   }
   dim3 gd(p.max_chunks, a.nkv, a.B);
   e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), s, next_pdl(), tk, tv, p);
-  if (e != cudaSuccess || a.max_query_len < 2) return e;
+  if (e != cudaSuccess) return e;
+  if (p.max_chunks > 1) {
+    e = launch_kernel(k_attn_combine<D>, dim3(a.nq, a.B), dim3(D), 0, s, next_pdl(), p);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.max_query_len < 2) return cudaSuccess;
   if (tc) {
     static std::once_flag tc_once;
     static cudaError_t tc_attr = cudaSuccess;
@@ -1226,22 +1180,11 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
 
 }  // namespace
 
-size_t attn_counter_count(int B, int nkv) { return static_cast<size_t>(B > 0 ? B : 1) * nkv; }
-
 size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim) {
   const int nch = num_chunks((max_seq_len + kBS - 1) / kBS);
   const size_t n = static_cast<size_t>(B) * (nch < 1 ? 1 : nch) * nq;
   return n * head_dim * sizeof(float) + n * sizeof(float2) +
          static_cast<size_t>(max_prefill_items(T, B)) * sizeof(uint32_t) + 256;
-}
-
-size_t attn_workspace_counter_offset(int B, int T, int max_seq_len, int nq, int head_dim) {
-  return (attn_partials_bytes(B, T, max_seq_len, nq, head_dim) + 255) & ~static_cast<size_t>(255);
-}
-
-size_t attn_workspace_bytes(int B, int T, int max_seq_len, int nq, int nkv, int head_dim) {
-  const size_t cnt = (attn_counter_count(B, nkv) * sizeof(int) + 255) & ~static_cast<size_t>(255);
-  return attn_workspace_counter_offset(B, T, max_seq_len, nq, head_dim) + cnt + 256;
 }
 
 int attention_launch(const AttnArgs& a, cudaStream_t s) {
@@ -1264,7 +1207,6 @@ int attention_launch(const AttnArgs& a, cudaStream_t s) {
   p.group = a.nq / a.nkv;
   p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.head_dim));
   p.err = a.err;
-  p.counters = a.counters;
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   const size_t n = static_cast<size_t>(a.B) * (num_chunks(max_blk) < 1 ? 1 : num_chunks(max_blk)) * a.nq;
   if (attn_partials_bytes(a.B, a.T, a.max_seq_len, a.nq, a.head_dim) > a.partials_bytes) return cudaErrorInvalidValue;

@@ -53,11 +53,8 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s);  // returns 0 or a CUDA erro
 //   r = x (+ res_in); h = r * rsqrt(mean(r^2) + eps) * gamma
 // row_index_qsl != nullptr: output row b reads input row qsl[b+1]-1 (last
 // token of sequence b), otherwise row b reads row b.
-// zero_ints != nullptr: the kernel also sets n_zero ints there to zero (the
-// arrival counters of the attention that follows it in a layer).
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma,
-                       int rows, int H, float eps, const int32_t* row_index_qsl, int* zero_ints, int n_zero,
-                       bool pdl, cudaStream_t s);
+                       int rows, int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s);
 
 int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* block_table, int T, int B, int max_blocks, int block_size, int num_blocks,
@@ -70,10 +67,6 @@ int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab,
                  cudaStream_t s);
 
 int argmax_launch(const float* logits, int rows, int vocab, int32_t* out, bool pdl, cudaStream_t s);
-
-// Longest context the attention takes: the split-KV merge stages two floats
-// per (q head of a group, 512-key chunk) in the decode kernel's shared memory.
-constexpr int kMaxSeqLen = 384 * 512;
 
 struct AttnArgs {
   const void* q;        // [T, nq, d] bf16 (rotated)
@@ -89,21 +82,12 @@ struct AttnArgs {
   int max_query_len, max_seq_len;
   float* partials;  // decode split-KV partials
   size_t partials_bytes;
-  int* counters;    // attn_counter_count(B, nkv) ints, zero on entry; left at zero
   int* err;
   int pdl;          // as GemmArgs::pdl
 };
 
 // split-KV partials + the prefill work list of a batch of B sequences and T tokens
 size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim);
-// Arrival counters of the split-KV merge: one per (sequence, KV head).  The
-// chunk CTA that completes a count merges the chunks.
-size_t attn_counter_count(int B, int nkv);
-// Workspace of a standalone attention call: partials + work list, then the
-// counters, each 256-byte aligned, plus 256 bytes for aligning the base.
-size_t attn_workspace_bytes(int B, int T, int max_seq_len, int nq, int nkv, int head_dim);
-// Offset of the counters in that workspace (from its 256-aligned base).
-size_t attn_workspace_counter_offset(int B, int T, int max_seq_len, int nq, int head_dim);
 int attention_launch(const AttnArgs& a, cudaStream_t s);
 
 int num_sms();

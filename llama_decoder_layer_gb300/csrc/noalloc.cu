@@ -21,8 +21,8 @@
 
 // 32 MiB: the split-KV partials of B sequences whose contexts span C chunks
 // of 512 keys take B * C * n_heads * (head_dim + 2) * 4 bytes, plus a work
-// list of 4 * (ceil(T/8) + B) bytes, B * n_kv_heads arrival counters and
-// alignment: e.g. up to ~1000 sequence-chunks at 64 heads x 128.
+// list of 4 * (ceil(T/8) + B) bytes and 256 of alignment: e.g. up to ~1000
+// sequence-chunks at 64 heads x 128.
 static constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;
 
 static __device__ __align__(256) unsigned char llama_noalloc_attn_scratch[kNoAllocScratchBytes];
@@ -59,13 +59,14 @@ extern "C" int llama_paged_attention_noalloc(const LlamaLayerConfig* cfg, const 
   if (cfg == nullptr || batch == nullptr) return LLAMA_ERR_ARG;
   if (batch->num_tokens > 0 && batch->num_seqs > 0 && batch->max_seq_len > 0 && cfg->n_heads > 0 &&
       cfg->head_dim > 0) {
-    const size_t need = llama::attn_workspace_bytes(batch->num_seqs, batch->num_tokens, batch->max_seq_len,
-                                                    cfg->n_heads, cfg->n_kv_heads, cfg->head_dim);
+    const size_t need = llama::attn_partials_bytes(batch->num_seqs, batch->num_tokens, batch->max_seq_len,
+                                                   cfg->n_heads, cfg->head_dim) +
+                        256;
     if (need > kNoAllocScratchBytes) return LLAMA_ERR_SCRATCH_LIMIT;
   }
   void* scratch = scratch_address();
   if (scratch == nullptr) return LLAMA_ERR_CUDA;
-  // The call clears the split-KV arrival counters itself; the merge reads only
+  // Nothing in the scratch has to start at zero: the combine step reads only
   // partials that the decode kernel wrote earlier in this same call, and the
   // prefill kernel reads only the work list the planning kernel wrote first.
   return llama_paged_attention(cfg, batch, q, k_cache, v_cache, out, scratch, kNoAllocScratchBytes, stream);

@@ -48,12 +48,9 @@ template <int MAXC>
 __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __restrict__ x, const uint4* res_in,
                                                               uint4* res_out, uint4* h_out,
                                                               const uint4* __restrict__ gamma, int H, float eps,
-                                                              const int32_t* __restrict__ qsl, int* zero_ints,
-                                                              int n_zero) {
+                                                              const int32_t* __restrict__ qsl) {
   __shared__ float red[33];
   pdl_wait();
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_ints[i] = 0;
   const int out_row = blockIdx.x;
   const int in_row = qsl != nullptr ? qsl[out_row + 1] - 1 : out_row;
   const int nch = H >> 3;
@@ -241,8 +238,7 @@ int grid_for(long long work, int threads) {
 }  // namespace
 
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma, int rows,
-                       int H, float eps, const int32_t* row_index_qsl, int* zero_ints, int n_zero, bool pdl,
-                       cudaStream_t s) {
+                       int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s) {
   if (rows <= 0) return 0;
   const int nch = H / 8;
   const int per = (nch + kNormThreads - 1) / kNormThreads;
@@ -251,10 +247,8 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
   auto RO = static_cast<uint4*>(res_out);
   auto HO = static_cast<uint4*>(h_out);
   auto G = static_cast<const uint4*>(gamma);
-  if (zero_ints == nullptr) n_zero = 0;
   auto go = [&](auto kernel) {
-    return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl,
-                         zero_ints, n_zero);
+    return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl);
   };
   if (per <= 1) return go(k_add_rmsnorm<1>);
   if (per <= 2) return go(k_add_rmsnorm<2>);

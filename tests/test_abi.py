@@ -87,15 +87,3 @@ def test_host_argument_checks_without_a_gpu(lib):
     # norm: H must be a multiple of 8 within 16384
     assert L.llama_fused_add_rmsnorm(None, None, None, None, None, 4, 100, 1e-5, None) == lb.LLAMA_ERR_ARG
 
-
-def test_context_limit_rejected_on_the_host(lib):
-    # max_seq_len above 384 chunks of 512 keys is refused before any launch
-    # (the split-KV merge stages its per-chunk weights in shared memory); the
-    # pointers are never dereferenced on this path
-    L = lib
-    cfg = lb.LayerConfig(8192, 64, 8, 128, 28672, 1e-5, 5e5).c()
-    fake = ctypes.c_void_p(256)
-    for max_seq_len, want in ((384 * 512, lb.LLAMA_ERR_WORKSPACE), (384 * 512 + 1, lb.LLAMA_ERR_UNSUPPORTED)):
-        b = lb.LlamaBatch(1, 1, (max_seq_len + 15) // 16, 100000, 1, max_seq_len, fake, fake, fake, fake, None)
-        st = L.llama_paged_attention(ctypes.byref(cfg), ctypes.byref(b), fake, fake, fake, fake, None, 0, None)
-        assert st == want, (max_seq_len, lb.status_string(st))
