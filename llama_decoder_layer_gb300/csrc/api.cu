@@ -174,6 +174,7 @@ AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q
   a.partials_bytes = part_bytes;
   a.err = err;
   a.pdl = pdl ? 1 : 0;
+  a.overlap = 1;
   return a;
 }
 
@@ -241,10 +242,13 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   e = gemm_launch(g, s);
   if (e) return cuda_status(e);
   // attention
-  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, err, true), s);
+  bool joined = false;
+  e = attention_launch(attn_args(c, b, q, kc, vc, o, apart, L.apart_bytes, err, true), s, &joined);
   if (e) return cuda_status(e);
   // o_proj -> y (in the h buffer)
-  e = gemm_launch(gemm(kEpiBf16, o, w.w_o, H, qsz, h, H), s);
+  GemmArgs go = gemm(kEpiBf16, o, w.w_o, H, qsz, h, H);
+  go.pdl = joined ? 0 : 1;
+  e = gemm_launch(go, s);
   if (e) return cuda_status(e);
   // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
   e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, true, s);

@@ -1122,7 +1122,28 @@ size_t prefill_smem() {
 }
 
 template <int D>
-int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams& p, cudaStream_t s) {
+int launch_prefill_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, bool tc,
+                     int tile_tokens, int items, bool pdl, cudaStream_t s);
+
+// One non-blocking stream per device, created on first use and kept for the
+// life of the process.
+cudaStream_t side_stream() {
+  constexpr int kDevs = 64;
+  static cudaStream_t st[kDevs] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (st[dev] == nullptr && cudaStreamCreateWithFlags(&st[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    st[dev] = nullptr;
+  }
+  return st[dev];
+}
+
+template <int D>
+int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams& p, cudaStream_t s,
+             bool* joined) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
@@ -1136,30 +1157,61 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   const int max_blk = (a.max_seq_len + kBS - 1) / kBS;
   p.max_chunks = num_chunks(max_blk);
   if (p.max_chunks < 1) p.max_chunks = 1;
-  // the first kernel takes the caller's dependency mode, the others follow it
-  bool pdl = a.pdl != 0;
-  auto next_pdl = [&]() {
-    const bool r = pdl;
-    pdl = true;
-    return r;
-  };
   const bool tc = a.max_query_len >= 2 && D == 128 && 128 % p.group == 0;
   const int tile_tokens = tc ? 128 / p.group : 16;  // tensor-core prefill: 128 rows = tokens x group heads
   const int items = (a.T + tile_tokens - 1) / tile_tokens + a.B;
-  cudaError_t e;
+  // With prefill sequences in the batch, the decode kernels (HBM-bound) run on
+  // the library's side stream beside the prefill kernel (tensor-bound): the
+  // caller's stream forks to it after the previous kernel and joins it before
+  // the next.  Otherwise everything runs in order on the caller's stream.
+  cudaStream_t sd = s;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  if (a.max_query_len >= 2 && a.overlap) {
+    cudaStream_t side = side_stream();
+    if (side != nullptr && cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventRecord(ev_fork, s) == cudaSuccess && cudaStreamWaitEvent(side, ev_fork, 0) == cudaSuccess) {
+      sd = side;
+    } else {
+      cudaGetLastError();
+      if (ev_fork) cudaEventDestroy(ev_fork);
+      if (ev_join) cudaEventDestroy(ev_join);
+      ev_fork = ev_join = nullptr;
+    }
+  }
+  const bool forked = sd != s;
+  if (joined) *joined = forked;
+  // the first kernel on each stream takes the caller's dependency mode (none
+  // after a fork), the ones after it overlap their predecessor
+  bool pdl_s = a.pdl != 0, pdl_d = forked ? false : a.pdl != 0;
+  cudaError_t e = cudaSuccess;
   if (a.max_query_len >= 2) {
-    e = launch_kernel(k_attn_plan, dim3(1), dim3(1024), 0, s, next_pdl(), a.qsl, a.B, tile_tokens, p.pre_items,
-                      items);
-    if (e != cudaSuccess) return e;
+    e = launch_kernel(k_attn_plan, dim3(1), dim3(1024), 0, s, pdl_s, a.qsl, a.B, tile_tokens, p.pre_items, items);
+    pdl_s = true;
+    if (!forked) pdl_d = true;
   }
-  dim3 gd(p.max_chunks, a.nkv, a.B);
-  e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), s, next_pdl(), tk, tv, p);
-  if (e != cudaSuccess) return e;
-  if (p.max_chunks > 1) {
-    e = launch_kernel(k_attn_combine<D>, dim3(a.nq, a.B), dim3(D), 0, s, next_pdl(), p);
-    if (e != cudaSuccess) return e;
+  if (e == cudaSuccess) {
+    dim3 gd(p.max_chunks, a.nkv, a.B);
+    e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), sd, pdl_d, tk, tv, p);
+    if (e == cudaSuccess && p.max_chunks > 1)
+      e = launch_kernel(k_attn_combine<D>, dim3(a.nq, a.B), dim3(D), 0, sd, true, p);
+    if (!forked) pdl_s = true;
   }
-  if (a.max_query_len < 2) return cudaSuccess;
+  if (e == cudaSuccess && a.max_query_len >= 2)
+    e = static_cast<cudaError_t>(launch_prefill_d<D>(a, tk, tv, p, tc, tile_tokens, items, pdl_s, s));
+  if (forked) {  // join even after a failed launch, so the caller's stream never runs ahead of the side stream
+    const cudaError_t j1 = cudaEventRecord(ev_join, sd);
+    const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, ev_join, 0) : j1;
+    cudaEventDestroy(ev_fork);
+    cudaEventDestroy(ev_join);
+    if (e == cudaSuccess) e = j2;
+  }
+  return e;
+}
+
+template <int D>
+int launch_prefill_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, bool tc,
+                     int tile_tokens, int items, bool pdl, cudaStream_t s) {
   if (tc) {
     static std::once_flag tc_once;
     static cudaError_t tc_attr = cudaSuccess;
@@ -1169,13 +1221,13 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
     if (tc_attr != cudaSuccess) return tc_attr;
     CUtensorMap tq;
     if (!make_q_tmap(&tq, a.q, a.T, a.nq, p.group, tile_tokens)) return cudaErrorInvalidValue;
-    return launch_kernel(k_attn_prefill_tc, dim3(a.nkv, items), dim3(kTcThreads), kTcSmem, s, next_pdl(), tq, tk,
+    return launch_kernel(k_attn_prefill_tc, dim3(a.nkv, items), dim3(kTcThreads), kTcSmem, s, pdl, tq, tk,
                          tv, p);
   }
   const int n_hc = (p.group + kPreMaxHeads - 1) / kPreMaxHeads;
   const int warps = (p.group < kPreMaxHeads ? p.group : kPreMaxHeads) + 1;
   return launch_kernel(k_attn_prefill<D>, dim3(a.nkv * n_hc, items), dim3(warps * 32), prefill_smem<D>(), s,
-                       next_pdl(), tk, tv, p);
+                       pdl, tk, tv, p);
 }
 
 }  // namespace
@@ -1187,7 +1239,8 @@ size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim) 
          static_cast<size_t>(max_prefill_items(T, B)) * sizeof(uint32_t) + 256;
 }
 
-int attention_launch(const AttnArgs& a, cudaStream_t s) {
+int attention_launch(const AttnArgs& a, cudaStream_t s, bool* joined) {
+  if (joined) *joined = false;
   if (a.T <= 0 || a.B <= 0) return 0;
   const long long rows = static_cast<long long>(a.num_blocks) * a.nkv * kBS;
   CUtensorMap tk, tv;
@@ -1214,8 +1267,8 @@ int attention_launch(const AttnArgs& a, cudaStream_t s) {
   p.part_o = a.partials;
   p.part_ml = reinterpret_cast<float2*>(a.partials + n * a.head_dim);
   p.pre_items = reinterpret_cast<uint32_t*>(p.part_ml + n);
-  if (a.head_dim == 128) return launch_d<128>(a, tk, tv, p, s);
-  if (a.head_dim == 64) return launch_d<64>(a, tk, tv, p, s);
+  if (a.head_dim == 128) return launch_d<128>(a, tk, tv, p, s, joined);
+  if (a.head_dim == 64) return launch_d<64>(a, tk, tv, p, s, joined);
   return cudaErrorInvalidValue;
 }
 

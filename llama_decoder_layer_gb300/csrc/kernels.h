@@ -84,11 +84,14 @@ struct AttnArgs {
   size_t partials_bytes;
   int* err;
   int pdl;          // as GemmArgs::pdl
+  int overlap;      // 1: with prefill sequences present, run the decode kernels on a side stream
 };
 
 // split-KV partials + the prefill work list of a batch of B sequences and T tokens
 size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim);
-int attention_launch(const AttnArgs& a, cudaStream_t s);
+// *joined (if given) is set when the caller's stream waited on the side
+// stream: the next kernel then has a full dependency, not a programmatic one.
+int attention_launch(const AttnArgs& a, cudaStream_t s, bool* joined = nullptr);
 
 int num_sms();
 
