@@ -230,7 +230,10 @@ def layer_algorithmic(spec, bl):
             "bytes": w_elems * 2 + kv_bytes + act_bytes, "flops": flops}
 
 
-def time_steps(step, steps, warmup, world, sampler=None):
+def time_steps(step, steps, warmup, world, sampler=None, counter=None):
+    """Mean device time of one step in ms (max over ranks) and the clock record.
+    counter: the library's launch counter; the kernels launched in the timed
+    region are left in time_steps.launches."""
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -240,10 +243,12 @@ def time_steps(step, steps, warmup, world, sampler=None):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.start()
+    n0 = counter() if counter else None
     e0.record(s)
     for _ in range(steps):
         step()
     e1.record(s)
+    time_steps.launches = counter() - n0 if counter else None
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     barrier(world)
@@ -384,7 +389,8 @@ def run_ours(args, world, rank, local):
 
     # main line: the stack step
     sampler = ClockSampler(local)
-    ms, clocks = time_steps(W.step, args.steps, args.warmup, world, sampler)
+    ms, clocks = time_steps(W.step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
+    stack_launches = time_steps.launches
     st, detail = lb.get_device_error()
     if st != lb.LLAMA_OK:
         raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
@@ -441,9 +447,6 @@ def run_ours(args, world, rank, local):
     # algorithmic totals of the stack step
     alg_layers = [layer_algorithmic(W.spec, W.bl) for _ in range(1)][0]
     stack_flops = alg_layers["flops"] * W.layers_n + 2.0 * W.bl.num_seqs * W.spec.hidden * W.spec.vocab
-    # per layer: slot map, 2 norms, 4 GEMMs, decode attention + combine + prefill attention;
-    # per step: embedding, final norm, lm_head GEMM + stream-K fixup, argmax
-    launches = W.layers_n * 10 + 5
     line = {
         "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
         "value": round(value, 1), "unit": "tokens/s per layer", "n_gpus": world, "steps": args.steps,
@@ -458,7 +461,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": stack_launches,
         "cpu_baseline": cpu,
     }
     line.update(extra)
@@ -489,7 +492,8 @@ def run_gate_up(args, world, rank, local, lb, I, dev, peaks, peak_src):
     out = torch.empty((T, spec.intermediate), dtype=torch.bfloat16, device=dev)
     ws = lb.alloc_workspace(lb.linear_workspace_size(), dev)
     sampler = ClockSampler(local)
-    ms, clocks = time_steps(lambda: lb.gate_up_silu(x, w, out, ws), args.steps, args.warmup, world, sampler)
+    ms, clocks = time_steps(lambda: lb.gate_up_silu(x, w, out, ws), args.steps, args.warmup, world, sampler,
+                            counter=lb.launch_count)
     flops = 2.0 * T * 2 * spec.intermediate * spec.hidden
     tf = flops / (ms / 1e3) / 1e12
     line = {
@@ -502,7 +506,7 @@ def run_gate_up(args, world, rank, local, lb, I, dev, peaks, peak_src):
         "roofline": {"kernel": "k_gemm_tc<SwiGLU>", "bound": "tensor", "achieved": round(tf, 1),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                      "peak_source": f"bf16_tflops ({peak_src}, burst)", "flops_per_launch": flops, "traffic": None},
-        "clocks": clocks, "gpu_launches": args.steps, "cpu_baseline": None, "e2e": None,
+        "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -521,7 +525,7 @@ def run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
     ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), dev)
     sampler = ClockSampler(local)
     ms, clocks = time_steps(lambda: lb.paged_attention(cfg, batch, q, kc, vc, out, ws), args.steps, args.warmup,
-                            world, sampler)
+                            world, sampler, counter=lb.launch_count)
     d, nq, nkv = spec.head_dim, spec.n_heads, spec.n_kv_heads
     pairs = sum(c * q_ + q_ * (q_ + 1) // 2 for c, q_ in zip(bl.ctx_lens, bl.q_lens))
     kv_bytes = sum(c + q_ for c, q_ in zip(bl.ctx_lens, bl.q_lens)) * nkv * d * 2 * 2
@@ -541,7 +545,8 @@ def run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
         "value": round(bl.num_tokens * world / (ms / 1e3), 1), "unit": "tokens/s through attention",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload}, "roofline": roof, "clocks": clocks, "gpu_launches": None,
+        "config": {"workload": args.workload}, "roofline": roof, "clocks": clocks,
+        "gpu_launches": time_steps.launches,
         "cpu_baseline": None, "e2e": None,
     }
     if rank == 0:
@@ -552,7 +557,7 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
     """One decoder layer of the named workload per step (residual in, residual out)."""
     L = setup_layer(lb, I, args.workload, seed, dev)
     sampler = ClockSampler(local)
-    ms, clocks = time_steps(L.step, args.steps, args.warmup, world, sampler)
+    ms, clocks = time_steps(L.step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
     st, detail = lb.get_device_error()
     if st != lb.LLAMA_OK:
         raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
@@ -567,7 +572,7 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
                    "l2": "inputs larger than L2" if alg["bytes"] > L2_BYTES else "inputs smaller than L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": layer_roofline(args.workload, alg, ms, peaks, peak_src),
-        "clocks": clocks, "gpu_launches": None, "cpu_baseline": None, "e2e": None,
+        "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

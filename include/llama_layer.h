@@ -260,6 +260,11 @@ const char* llama_status_string(int status);
 /* Number of streaming multiprocessors of the current device (cached). */
 int llama_num_sms(void);
 
+/* Kernels this process has launched through the library so far, on every
+ * device (a host-side counter, incremented when a launch is accepted).  The
+ * difference across a region counts that region's kernels. */
+uint64_t llama_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

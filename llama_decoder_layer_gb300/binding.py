@@ -73,6 +73,7 @@ SIGNATURES = {
     "llama_get_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_int)]),
     "llama_status_string": (ctypes.c_char_p, [_I]),
     "llama_num_sms": (_I, []),
+    "llama_launch_count": (ctypes.c_uint64, []),
 }
 
 _lib = None
@@ -282,3 +283,8 @@ def get_device_error(stream=None):
 
 def num_sms() -> int:
     return int(lib().llama_num_sms())
+
+
+def launch_count() -> int:
+    """Kernels launched through the library so far in this process."""
+    return int(lib().llama_launch_count())

@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "llama_layer.h"
 
 namespace llama {
@@ -263,6 +264,8 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
 
 }  // namespace
 
+std::atomic<unsigned long long> g_launch_count{0};
+
 int num_sms() {
   static int sms[kMaxDevices] = {};
   const int d = current_device();
@@ -509,5 +512,7 @@ const char* llama_status_string(int status) {
 }
 
 int llama_num_sms(void) { return num_sms(); }
+
+uint64_t llama_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 }  // extern "C"

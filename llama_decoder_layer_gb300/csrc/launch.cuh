@@ -8,9 +8,19 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 namespace llama {
+
+// Kernels this process has launched through the library (every device);
+// read by llama_launch_count().
+extern std::atomic<unsigned long long> g_launch_count;
+
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
@@ -25,7 +35,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return counted(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
 // The same, for a kernel launched in thread-block clusters of cluster_x CTAs.
@@ -46,7 +56,7 @@ cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return counted(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
 }
 
 }  // namespace llama

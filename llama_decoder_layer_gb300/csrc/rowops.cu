@@ -269,10 +269,9 @@ int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, i
                     int block_size, int num_blocks, void* k_cache, void* v_cache, int* err, cudaStream_t s) {
   if (T <= 0) return 0;
   const long long work = static_cast<long long>(T) * n_kv * (head_dim / 8);
-  k_kv_write<<<grid_for(work, 256), 256, 0, s>>>(static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, T,
-                                                  n_kv, head_dim, block_size, num_blocks,
-                                                  static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), err);
-  return cudaGetLastError();
+  return launch_kernel(k_kv_write, dim3(grid_for(work, 256)), dim3(256), 0, s, false, static_cast<const uint4*>(k),
+                       static_cast<const uint4*>(v), slots, T, n_kv, head_dim, block_size, num_blocks,
+                       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), err);
 }
 
 int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab, void* out, int* err, bool pdl,

@@ -87,3 +87,10 @@ def test_host_argument_checks_without_a_gpu(lib):
     # norm: H must be a multiple of 8 within 16384
     assert L.llama_fused_add_rmsnorm(None, None, None, None, None, 4, 100, 1e-5, None) == lb.LLAMA_ERR_ARG
 
+
+
+def test_launch_counter_counts_only_accepted_launches(lib):
+    # a call rejected on the host launches nothing; the counter is monotonic
+    before = lb.launch_count()
+    assert lib.llama_linear(None, None, 4, 250, 256, None, 0, None, 0, None) == lb.LLAMA_ERR_ARG
+    assert lb.launch_count() == before
