@@ -700,18 +700,21 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
 // 64 columns) and 128-key K/V tiles (2-stage ring); one thread of warp 1 issues
 // S = Q K^T into a double-buffered TMEM accumulator and O += P V into a TMEM
-// accumulator (V is the MN-major B operand); warps 2-5 (one row each) run the
-// online softmax from TMEM, write P as bf16 into a 128-byte-swizzled tile and
-// rescale O in TMEM only when a row's running max grows by more than 2^8.
+// accumulator (V is the MN-major B operand); warps 2-5 (one row each) read
+// each S tile from TMEM once, write P as bf16 pairs back over the first half
+// of that S buffer (tcgen05.st), and rescale O in TMEM only when a row's
+// running max grows by more than 2^8.  P V takes its A operand from tensor
+// memory, so the softmax of tile j+1 runs while P V of tile j is in the tensor
+// pipe: S buffer j%2 is next written by S of tile j+2, which the MMA warp
+// issues after P V of tile j.
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 192;
 constexpr int kTcKeys = 64;                        // keys per K/V tile
 constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-column halves)
 constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
 constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
-constexpr int kTcPBytes = 128 * kTcKeys * 2;       // P tile (16 KB)
 constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
-constexpr int kTcSmem = 2 * kTcQHalf + 2 * 2 * kTcTileBytes + kTcPBytes + 256 + kTcSlack;
+constexpr int kTcSmem = 2 * kTcQHalf + 2 * 2 * kTcTileBytes + 256 + kTcSlack;
 constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
 
 __global__ void __launch_bounds__(kTcThreads, 2)
@@ -731,9 +734,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t q_s = sb;                                   // Q: two 64-column halves
   auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes; };
   auto v_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes + kTcTileBytes; };
-  const uint32_t p_s = sb + 2u * kTcQHalf + 4u * kTcTileBytes;      // P (bf16, K-major over keys)
-  uint8_t* p_gen = smem + 2 * kTcQHalf + 4 * kTcTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + 4 * kTcTileBytes + kTcPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + 4 * kTcTileBytes);
   const uint32_t bar0 = smem_u32(bars);
   // K and V have their own 2-stage rings: a K stage is free as soon as its
   // S = Q K^T is done, so the next K tile is fetched while P V still runs
@@ -892,10 +893,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (lane == 0) {
         const int st = j & 1;
 #pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(p_s + ks * 32);
+        for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
           const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(st) + ks * 2048, kTcHalf, 1024);
-          tc_mma_f16(tmem + 2 * kTcKeys, a, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem + 2 * kTcKeys, tmem + st * kTcKeys + ks * 8, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc_commit(v_empty0 + 8 * st);
         tc_commit(o_done);
@@ -926,26 +926,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         break;
       }
       tc_fence_after();
-      // pass 1: masked, scaled row maximum of S (TMEM read in 64-column chunks,
-      // eight independent max chains)
+      // S of this tile, read once: masked, scaled row maximum (eight
+      // independent max chains)
       const int kbase = j * kTcKeys;
       const bool full_tile = kbase + kTcKeys - 1 <= pos_lo;  // CTA-uniform
+      const int lim = pos - kbase;                           // column e is visible when e <= lim
+      float t[kTcKeys];
+      tmem_ld64(lane_addr + st * kTcKeys, t);
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < kTcKeys / 64; ++c) {
-        float t[64];
-        tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
-        const int lim = pos - kbase - c * 64;  // column e is visible when e <= lim
-        if (full_tile) {
+      if (full_tile) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
-        } else {
+        for (int e = 0; e < kTcKeys; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
-        }
+        for (int e = 0; e < kTcKeys; ++e)
+          if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -955,15 +952,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const bool need = j > 0 && m_new > m_run + kRescaleLog2;
       const bool warp_rescale = __any_sync(0xffffffffu, need);
       if (j == 0) m_run = m_new;
-      if (j > 0) {
-        // P V of the previous tile must be done: the P tile is reused and O may be rescaled
+      if (warp_rescale) {
+        // P V of the previous tile must be done before O is rescaled (P V of
+        // the tile before it is: S of this tile was issued after it)
         if (!mbar_wait(o_done, (j - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      if (warp_rescale) {
         const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -977,45 +973,40 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         m_run = m_new;
       }
       const float base = m_run == -INFINITY ? 0.f : m_run;
-      // pass 2: P = exp2(S - max) as bf16 into the swizzled K-major tile
+      // P = exp2(S - max) as bf16 pairs over the first 32 columns of this S buffer
       float ls8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < kTcKeys / 64; ++c) {
-        float t[64];
-        tmem_ld64(lane_addr + st * kTcKeys + c * 64, t);
-        const int lim = pos - kbase - c * 64;
-        auto emit = [&](auto masked) {
+      float pw[kTcKeys / 2];
+      auto emit = [&](auto masked) {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const int e = q4 * 8 + e2 * 2;
-              float x0 = fast_exp2(fmaf(t[e], p.scale_log2, -base));
-              float x1 = fast_exp2(fmaf(t[e + 1], p.scale_log2, -base));
-              if (decltype(masked)::value) {
-                x0 = e <= lim ? x0 : 0.f;
-                x1 = e + 1 <= lim ? x1 : 0.f;
-              }
-              ls8[e2 * 2] += x0;
-              ls8[e2 * 2 + 1] += x1;
-              w[e2] = pack_bf16x2(x0, x1);
-            }
-            const int ch = c * 8 + q4;  // 16-byte chunk of the P row (64 keys = one 128-byte row)
-            *reinterpret_cast<uint4*>(p_gen + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c2 = 0; c2 < kTcKeys / 2; ++c2) {
+          const int e = 2 * c2;
+          float x0 = fast_exp2(fmaf(t[e], p.scale_log2, -base));
+          float x1 = fast_exp2(fmaf(t[e + 1], p.scale_log2, -base));
+          if (decltype(masked)::value) {
+            x0 = e <= lim ? x0 : 0.f;
+            x1 = e + 1 <= lim ? x1 : 0.f;
           }
-        };
-        if (full_tile)
-          emit(std::false_type{});
-        else
-          emit(std::true_type{});
-      }
+          ls8[e & 7] += x0;
+          ls8[(e + 1) & 7] += x1;
+          pw[c2] = __uint_as_float(pack_bf16x2(x0, x1));
+        }
+      };
+      if (full_tile)
+        emit(std::false_type{});
+      else
+        emit(std::true_type{});
+      tmem_st32(lane_addr + st * kTcKeys, pw);
       l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       // keys past the context inside the last loaded block: zero their V rows
-      // (P is zero there, but stale cache contents must not reach the MMA)
+      // (P is zero there, but stale cache contents must not reach the MMA),
+      // once the tile's V load has landed
       if (j == ntiles - 1) {
+        if (!mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         const int valid = n_keys - kbase;
         uint8_t* vg = smem + (v_s(st) - sb);
         for (int i = threadIdx.x - 64; i < (kTcKeys - valid) * 2 * 8; i += 128) {
