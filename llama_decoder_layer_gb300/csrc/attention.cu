@@ -936,9 +936,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      if (full_tile) {
+      if (full_tile) {  // the softmax warps are issue-bound: two scores per max instruction
 #pragma unroll
-        for (int e = 0; e < kTcKeys; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+        for (int c2 = 0; c2 < kTcKeys / 2; ++c2) mx8[c2 & 7] = fmax3(mx8[c2 & 7], t[2 * c2], t[2 * c2 + 1]);
       } else {
 #pragma unroll
         for (int e = 0; e < kTcKeys; ++e)
@@ -973,23 +973,27 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         m_run = m_new;
       }
       const float base = m_run == -INFINITY ? 0.f : m_run;
-      // P = exp2(S - max) as bf16 pairs over the first 32 columns of this S buffer
-      float ls8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ls8[i] = 0.f;
+      // P = exp2(S - max) as bf16 pairs over the first 32 columns of this S
+      // buffer; scale-and-shift and the row sum run as paired fp32 operations
       float pw[kTcKeys / 2];
+      uint64_t ls2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ls2[i] = f2_pack(0.f, 0.f);
+      const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+      const uint64_t nbase2 = f2_pack(-base, -base);
       auto emit = [&](auto masked) {
 #pragma unroll
         for (int c2 = 0; c2 < kTcKeys / 2; ++c2) {
           const int e = 2 * c2;
-          float x0 = fast_exp2(fmaf(t[e], p.scale_log2, -base));
-          float x1 = fast_exp2(fmaf(t[e + 1], p.scale_log2, -base));
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(t[e], t[e + 1]), scale2, nbase2), a0, a1);
+          float x0 = fast_exp2(a0);
+          float x1 = fast_exp2(a1);
           if (decltype(masked)::value) {
             x0 = e <= lim ? x0 : 0.f;
             x1 = e + 1 <= lim ? x1 : 0.f;
           }
-          ls8[e & 7] += x0;
-          ls8[(e + 1) & 7] += x1;
+          ls2[c2 & 3] = f2_add(ls2[c2 & 3], f2_pack(x0, x1));
           pw[c2] = __uint_as_float(pack_bf16x2(x0, x1));
         }
       };
@@ -998,7 +1002,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       else
         emit(std::true_type{});
       tmem_st32(lane_addr + st * kTcKeys, pw);
-      l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      {
+        float s[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f2_unpack(ls2[i], s[2 * i], s[2 * i + 1]);
+        l += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+      }
       // keys past the context inside the last loaded block: zero their V rows
       // (P is zero there, but stale cache contents must not reach the MMA),
       // once the tile's V load has landed
