@@ -238,7 +238,7 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
  * The split-KV scratch is a fixed array of llama_paged_attention_noalloc_limit()
  * bytes (32 MiB) inside the library.  Every GPU that loads the library holds it
  * until the process exits.  A batch whose scratch needs more than that
- * (num_seqs * ceil(ceil(max_seq_len/16)/32) * n_heads * (head_dim+2) * 4
+ * (num_seqs * ceil(ceil(max_seq_len/16)/96) * n_heads * (head_dim+2) * 4
  * + 4 * (ceil(num_tokens/8) + num_seqs) + 256 bytes) is rejected with
  * LLAMA_ERR_SCRATCH_LIMIT before anything is launched.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.

@@ -41,7 +41,8 @@ namespace {
 constexpr int kBS = 16;             // tokens per cache block
 constexpr int kDecWarps = 4;
 constexpr int kDecStages = 3;
-constexpr int kChunkBlocks = 32;    // at most 512 keys per split-KV chunk
+constexpr int kChunkBlocks = 96;    // at most 1536 keys per split-KV chunk (sweep: 512 -> 1536 keys took
+                                    // the 70B decode batch from 0.372 to 0.329 ms)
 constexpr int kPreStages = 2;
 constexpr int kPreKeys = 64;        // keys per prefill K/V tile (4 blocks)
 constexpr float kLog2e = 1.4426950408889634f;

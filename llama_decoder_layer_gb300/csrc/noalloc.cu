@@ -20,7 +20,7 @@
 #include "llama_layer.h"
 
 // 32 MiB: the split-KV partials of B sequences whose contexts span C chunks
-// of 512 keys take B * C * n_heads * (head_dim + 2) * 4 bytes, plus a work
+// of 1536 keys take B * C * n_heads * (head_dim + 2) * 4 bytes, plus a work
 // list of 4 * (ceil(T/8) + B) bytes and 256 of alignment: e.g. up to ~1000
 // sequence-chunks at 64 heads x 128.
 static constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;

@@ -149,9 +149,10 @@ def _attn_case(nq, nkv, d, groups, seed):
 
 @pytest.mark.parametrize("nq,nkv,d", [(8, 2, 64), (16, 2, 128), (64, 8, 128)])
 def test_attention_decode(nq, nkv, d):
-    # contexts 0 (one visible key), 15, 16 (block edges), 511/512 (chunk edges), up to 1500 (3 chunks)
+    # contexts 0 (one visible key), 15, 16 (block edges), 1535/1536 (chunk edges: 1536 keys per
+    # split-KV chunk), up to 5000 (4 chunks)
     groups = (("decode", 1, 1, 0, 0), ("decode", 1, 1, 15, 15), ("decode", 1, 1, 16, 16),
-              ("decode", 1, 1, 511, 511), ("decode", 1, 1, 512, 512), ("decode", 5, 1, 1, 1500))
+              ("decode", 1, 1, 1535, 1535), ("decode", 1, 1, 1536, 1536), ("decode", 5, 1, 1, 5000))
     g, r = _attn_case(nq, nkv, d, groups, 21)
     assert_close(g, r, "decode attention")
 
@@ -166,7 +167,7 @@ def test_attention_prefill(nq, nkv, d):
 
 
 def test_attention_mixed_batch():
-    groups = (("decode", 4, 1, 20, 900), ("prefill", 2, 50, 0, 0), ("decode", 2, 1, 0, 40),
+    groups = (("decode", 4, 1, 20, 4000), ("prefill", 2, 50, 0, 0), ("decode", 2, 1, 0, 40),
               ("prefill", 1, 17, 30, 30))
     g, r = _attn_case(16, 2, 128, groups, 41)
     assert_close(g, r, "mixed attention")

@@ -40,9 +40,9 @@ def _case(nq, nkv, d, groups, seed):
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
-    # decode contexts up to 1500 keys (three 512-key chunks: the scratch is
+    # decode contexts up to 5000 keys (four 1536-key chunks: the scratch is
     # used) plus prefill sequences with and without a cached prefix
-    groups = (("decode", 6, 1, 20, 1500), ("prefill", 2, 40, 0, 0), ("decode", 2, 1, 0, 30),
+    groups = (("decode", 6, 1, 20, 5000), ("prefill", 2, 40, 0, 0), ("decode", 2, 1, 0, 30),
               ("prefill", 1, 17, 30, 30))
     cfg, batch, q, kc, vc, bl = _case(64, 8, 128, groups, 51)
     ref = torch.empty((bl.num_tokens, 64 * 128), dtype=torch.bfloat16, device=DEV)
@@ -61,13 +61,14 @@ def test_noalloc_matches_workspace_entry_point_twice():
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
     limit = int(lb.lib().llama_paged_attention_noalloc_limit())
     assert limit == 32 << 20
-    # 128 sequences x 8193-token contexts x 64 heads need far more than 32 MiB
+    # 128 sequences x 16385-token contexts (11 split-KV chunks each) x 64 heads
+    # need 47 MB of partials, more than the 32 MiB array
     spec = I.SPECS["decode_70b"]
     cfg = lb.LayerConfig.from_spec(spec)
     z = torch.zeros(1, dtype=torch.int32, device=DEV)
     batch = lb.Batch(torch.zeros(128, dtype=torch.int32, device=DEV), torch.arange(129, dtype=torch.int32, device=DEV),
-                     torch.full((128,), 8193, dtype=torch.int32, device=DEV),
-                     torch.zeros((128, 513), dtype=torch.int32, device=DEV), 1, 1, 8193)
+                     torch.full((128,), 16385, dtype=torch.int32, device=DEV),
+                     torch.zeros((128, 1025), dtype=torch.int32, device=DEV), 1, 1, 16385)
     with pytest.raises(lb.LlamaError) as e:
         lb.paged_attention_noalloc(cfg, batch, z, z, z, z)
     assert e.value.status == lb.LLAMA_ERR_SCRATCH_LIMIT
