@@ -6,20 +6,24 @@
 // The q heads sharing one KV head (g = n_heads / n_kv_heads of them) are
 // processed together, so every K/V block is loaded from memory once per group.
 // K/V blocks (16 tokens x head_dim of one KV head, contiguous in the cache) are
-// fetched by TMA with 128-byte swizzle and consumed with ldmatrix + mma.sync
-// (bf16 in, fp32 accumulate); softmax is online, in the exp2 domain.
+// fetched by TMA with 128-byte swizzle; softmax is online, in the exp2 domain.
 //
-// * decode (query length 1): split-KV.  One CTA per (sequence, KV head, chunk
-//   of the context); its 4 warps stream disjoint blocks of the chunk through
-//   their own 3-stage TMA rings with the group's q heads as the 16 MMA rows,
-//   merge in shared memory, and either write the output (one chunk) or a
-//   partial (unnormalised o, running max, sum) that k_attn_combine merges in
-//   chunk order.  (Merging in the decode kernel itself, by the chunk CTA that
-//   completes a per-(sequence, KV head) arrival count, was measured slower:
-//   the fence and atomic every chunk CTA then pays hold its SM slot.)
-// * prefill (query length >= 2): one CTA per (sequence, KV head, 16 query
-//   tokens); warp w owns q head w of the group; a producer warp streams
-//   64-key K/V tiles through a 2-stage ring; fully masked tiles are skipped.
+// * decode (query length 1): split-KV, ldmatrix + mma.sync (bf16 in, fp32
+//   accumulate: the group's q heads fill only 8 of 16 MMA rows, too few for
+//   the 128-row tensor-memory MMA).  One CTA per (sequence, KV head, chunk of
+//   up to 1536 keys); its 4 warps stream disjoint blocks of the chunk through
+//   their own 3-stage TMA rings, merge in shared memory, and either write the
+//   output (one chunk) or a partial (unnormalised o, running max, sum) that
+//   k_attn_combine merges in chunk order.  (Merging in the decode kernel
+//   itself, by the chunk CTA that completes a per-(sequence, KV head) arrival
+//   count, was measured slower: the fence and atomic every chunk CTA then pays
+//   hold its SM slot.)
+// * prefill (query length >= 2), head_dim 128: k_attn_prefill_tc on the
+//   tensor-memory MMA (S and O accumulate in TMEM, P goes back to TMEM as the
+//   A operand of P V); other shapes: k_attn_prefill, one CTA per (sequence,
+//   KV head, 16 query tokens), warp w owns q head w of the group, mma.sync.
+// * In a batch with prefill sequences the decode kernels run on a side stream
+//   beside the prefill kernel (HBM-bound next to tensor-bound work).
 //
 // Sources: [WALKTHROUGH] "模型库与算子层 — 代码走读", Attention
 // (attn_backend.forward(q, k, v, kv_cache.block_table) after _update_kv_cache);

@@ -1,25 +1,33 @@
 // Tensor-core GEMM y = x * W^T for the four projections (and lm_head), on the
 // 5th-generation tensor cores: TMA loads 128-byte-swizzled K-major tiles into
 // a shared-memory ring, one thread issues tcgen05.mma (M=128, N=256, K=16)
-// into a double-buffered fp32 accumulator in tensor memory, and four epilogue
-// warps drain it with tcgen05.ld and apply the fused epilogue:
+// into an fp32 accumulator in tensor memory, and four epilogue warps drain it
+// with tcgen05.ld and apply the fused epilogue:
 //   * plain bf16 store                         (o_proj, down_proj)
 //   * RoPE on q/k + q store + paged K/V scatter (qkv_proj; the cache update
 //     precedes attention, as LlamaAttention.forward does)
 //   * SiluAndMul: silu(x[:d]) * x[d:]          (gate_up_proj; a tile loads 128
 //     gate rows and the matching 128 up rows, so both halves meet in one
 //     thread)
+//   * fp32 store                               (lm_head logits)
 // Every tensor a module of the layer returns is bf16 (the model's dtype), so
 // the fused epilogues round the projection output to bf16 before RoPE and
 // before SiluAndMul, exactly where the unfused modules would store it.
-//   * fp32 store                               (lm_head logits)
-// The kernel is persistent (one CTA per SM).  Large problems are scheduled
-// data-parallel (whole tiles, grouped raster for L2 reuse); problems with few
-// tiles (decode) are split stream-K: every CTA gets an equal share of the
-// (tile, k-block) units, partial tiles go to a workspace and a fixup kernel
-// sums them in CTA order (a fixed order, so the result is deterministic) and
-// applies the same epilogue, spread over many CTAs so the partial reads run
-// in parallel.
+//
+// Three schedules, by the number of output tiles against the SM count:
+//   * many tiles (prefill): k_gemm_tc, persistent (one CTA per SM), whole
+//     tiles in a grouped raster for L2 reuse, the accumulator double-buffered
+//     so the epilogue of one tile overlaps the MMAs of the next;
+//   * at most half as many tiles as SMs (decode qkv, o_proj, down_proj):
+//     k_gemm_cluster, split-K over a thread-block cluster whose CTAs sum their
+//     fp32 slices through distributed shared memory;
+//   * in between (decode gate_up): k_gemm_tc stream-K, every CTA an equal
+//     share of (tile, k-block) units, partial tiles in a workspace, and
+//     k_gemm_fixup summing them in CTA order (deterministic) spread over many
+//     CTAs.
+// The kernels wait for the previous kernel of the call (pdl_wait) only where
+// they first need its results; the weight tiles of their first stages are
+// requested before that.
 //
 // Sources: [WALKTHROUGH] "模型库与算子层 — 代码走读", Linear layers (F.linear with
 // Parameter(out, in)); [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", §4
