@@ -257,6 +257,27 @@ def time_steps(step, steps, warmup, world, sampler=None, counter=None):
     return max_over_ranks(ms, world), clocks
 
 
+def time_graph(step, steps, warmup, world):
+    """Mean device time of one step replayed from a CUDA graph.  The step is
+    run twice on a side stream first (every lazy set-up of the library happens
+    outside the capture), captured once on that stream, then replayed on the
+    current stream and timed like time_steps."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            step(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(stream=s)
+    torch.cuda.synchronize()
+    ms, _ = time_steps(g.replay, steps, warmup, world)
+    del g
+    return ms
+
+
 def time_e2e(lb, W, steps, warmup, world, dev):
     """Same stack step through the public API with the step's inputs copied
     from pinned host memory and the sampled tokens copied back, every step."""
@@ -428,6 +449,11 @@ def run_ours(args, world, rank, local):
             tps = L.tokens_per_step * world / (lms / 1e3)
             extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
                            "roofline": layer_roofline(name, alg, lms, peaks, peak_src)}
+            if name.startswith("decode"):
+                gms = time_graph(L.step, steps, args.warmup, world)
+                extra[name]["cuda_graph"] = {"layer_ms": round(gms, 4),
+                                             "tokens_per_s": round(L.tokens_per_step * world / (gms / 1e3), 1),
+                                             "roofline": layer_roofline(name, alg, gms, peaks, peak_src)}
             st, detail = lb.get_device_error()
             if st != lb.LLAMA_OK:
                 raise RuntimeError(f"device error in {name}: {lb.status_string(st)}")
@@ -574,6 +600,12 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
         "roofline": layer_roofline(args.workload, alg, ms, peaks, peak_src),
         "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
     }
+    if args.workload.startswith("decode"):
+        # the same step replayed from a CUDA graph (launch overheads removed)
+        gms = time_graph(L.step, args.steps, args.warmup, world)
+        line["cuda_graph"] = {"ms_per_step": round(gms, 4),
+                              "value": round(L.tokens_per_step * world / (gms / 1e3), 1),
+                              "roofline": layer_roofline(args.workload, alg, gms, peaks, peak_src)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

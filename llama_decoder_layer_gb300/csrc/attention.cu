@@ -1146,6 +1146,28 @@ cudaStream_t side_stream() {
   return st[dev];
 }
 
+// The fork and join events of the current host thread on the current device,
+// created on first use and reused by every later call of that thread (a
+// stream wait takes the event's state when it is enqueued, so re-recording
+// afterwards does not disturb it).  Creating them outside any stream capture
+// (the first call of a thread is eager) keeps the call capture-safe.
+bool fork_join_events(cudaEvent_t* fork, cudaEvent_t* join) {
+  constexpr int kDevs = 64;
+  thread_local cudaEvent_t ev[kDevs][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return false;
+  for (int i = 0; i < 2; ++i) {
+    if (ev[dev][i] == nullptr && cudaEventCreateWithFlags(&ev[dev][i], cudaEventDisableTiming) != cudaSuccess) {
+      ev[dev][i] = nullptr;
+      cudaGetLastError();
+      return false;
+    }
+  }
+  *fork = ev[dev][0];
+  *join = ev[dev][1];
+  return true;
+}
+
 template <int D>
 int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams& p, cudaStream_t s,
              bool* joined) {
@@ -1173,15 +1195,11 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   if (a.max_query_len >= 2 && a.overlap) {
     cudaStream_t side = side_stream();
-    if (side != nullptr && cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) == cudaSuccess &&
-        cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) == cudaSuccess &&
-        cudaEventRecord(ev_fork, s) == cudaSuccess && cudaStreamWaitEvent(side, ev_fork, 0) == cudaSuccess) {
+    if (side != nullptr && fork_join_events(&ev_fork, &ev_join) && cudaEventRecord(ev_fork, s) == cudaSuccess &&
+        cudaStreamWaitEvent(side, ev_fork, 0) == cudaSuccess) {
       sd = side;
     } else {
       cudaGetLastError();
-      if (ev_fork) cudaEventDestroy(ev_fork);
-      if (ev_join) cudaEventDestroy(ev_join);
-      ev_fork = ev_join = nullptr;
     }
   }
   const bool forked = sd != s;
@@ -1207,8 +1225,6 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   if (forked) {  // join even after a failed launch, so the caller's stream never runs ahead of the side stream
     const cudaError_t j1 = cudaEventRecord(ev_join, sd);
     const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(s, ev_join, 0) : j1;
-    cudaEventDestroy(ev_fork);
-    cudaEventDestroy(ev_join);
     if (e == cudaSuccess) e = j2;
   }
   return e;
