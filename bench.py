@@ -610,6 +610,76 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
         print(json.dumps(line), flush=True)
 
 
+def run_deep_decode(args, world, rank, local):
+    """The full-depth 70B decode step: embedding, 80 layers, final norm,
+    lm_head and greedy sampling in one llama_stack_forward call, timed eager
+    and replayed from a CUDA graph.  Every layer has its own weight and cache
+    buffers (137 GB + 48 GB); their values are layer 0's, copied, since
+    drawing 68 G random numbers would dominate the run."""
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    from llama_decoder_layer_gb300 import inputs as I
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    seed = 1000 + rank
+    spec = I.SPECS["decode_70b_80l"]
+    bl = I.make_batch(spec, seed, dev)
+    w0 = I.make_layer_weights(spec, seed, 0, dev)
+    layers = [w0] + [{k: v.clone() for k, v in w0.items()} for _ in range(spec.num_layers - 1)]
+    kc0, vc0 = I.make_kv_cache(spec, bl.num_blocks, seed, 0, dev)
+    caches = [(kc0, vc0)] + [(kc0.clone(), vc0.clone()) for _ in range(spec.num_layers - 1)]
+    emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, seed, dev)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T, B = bl.num_tokens, bl.num_seqs
+    hidden = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device=dev)
+    residual = torch.empty_like(hidden)
+    tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, T, B, batch.max_seq_len, spec.vocab), dev)
+    kcs, vcs = [c[0] for c in caches], [c[1] for c in caches]
+
+    def step(stream=None):
+        lb.stack_forward(cfg, layers, fn, lm, batch, hidden, residual, kcs, vcs, tokens, ws, embed=emb,
+                         input_ids=ids, stream=stream)
+
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
+    launches = time_steps.launches
+    gms = time_graph(step, args.steps, args.warmup, world)
+    st, detail = lb.get_device_error()
+    if st != lb.LLAMA_OK:
+        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+    alg = layer_algorithmic(spec, bl)
+    head_bytes = spec.vocab * spec.hidden * 2 + B * spec.vocab * 4
+    step_bytes = spec.num_layers * alg["bytes"] + head_bytes
+
+    def roof(t_ms):
+        gbs = step_bytes / (t_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes": step_bytes, "traffic": None}
+
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(B * spec.num_layers * world / (ms / 1e3), 1), "unit": "tokens/s per layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; every layer's buffers hold layer 0's random values)",
+        "config": {"workload": f"decode_70b_80l: embedding + 80 x 70B-shaped layers + final norm + lm_head(128256) "
+                               f"+ greedy argmax; {B} decode seqs, ctx U[512,4096]",
+                   "tokens_per_step": T, "layers": spec.num_layers,
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.0f} GB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof(ms), "clocks": clocks, "gpu_launches": launches, "cpu_baseline": None, "e2e": None,
+        "cuda_graph": {"ms_per_step": round(gms, 4), "value": round(B * spec.num_layers * world / (gms / 1e3), 1),
+                       "roofline": roof(gms)},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """Times the CPU oracle (fp32) on a bounded sample of the stack workload:
     each step runs one decode sequence through all layers + head."""
@@ -658,10 +728,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stack_70b",
                     choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny", "gemm_gate_up",
-                             "attn_prefill", "attn_decode"],
+                             "attn_prefill", "attn_decode", "decode_70b_80l"],
                     help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
                          "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
-                         "attn_decode: the paged attention of the 70B prefill / decode batch alone")
+                         "attn_decode: the paged attention of the 70B prefill / decode batch alone; "
+                         "decode_70b_80l: the full-depth 70B decode step (~190 GB on the device, about a "
+                         "minute of set-up)")
     ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -671,6 +743,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "decode_70b_80l":
+        run_deep_decode(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -82,6 +82,11 @@ SPECS = {
     "stack_70b": Spec("stack_70b", 8192, 64, 8, 128, 28672, 1e-5, 500000.0, LLAMA3_SCALING,
                       groups=(("decode", 32, 1, 1024, 16384), ("prefill", 2, 2048, 0, 0)),
                       residual_none=True, num_layers=8, vocab=128256),
+    # the full-depth 70B decode step (all 80 layers, embedding to sampled
+    # token) at a batch that fits one GPU next to 137 GB of layer weights
+    "decode_70b_80l": Spec("decode_70b_80l", 8192, 64, 8, 128, 28672, 1e-5, 500000.0, LLAMA3_SCALING,
+                           groups=(("decode", 64, 1, 512, 4096),), residual_none=True, num_layers=80,
+                           vocab=128256),
 }
 
 # seed offsets per tensor kind

@@ -68,3 +68,56 @@ def test_layer_graph_replay_matches_eager(name, groups):
         assert lb.get_device_error()[0] == lb.LLAMA_OK
         for a, b, what in zip((hidden, res_out, kc, vc), eager, ("hidden", "residual", "k cache", "v cache")):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{what} differs after graph replay"
+
+
+def test_stack_graph_replay_matches_eager():
+    # a 2-layer stack with embedding, final norm, lm_head and argmax over a
+    # mixed batch, captured as one call
+    spec = dataclasses.replace(I.SPECS["tiny"], num_layers=2, vocab=1024, residual_none=True,
+                               groups=(("decode", 3, 1, 10, 1800), ("prefill", 2, 20, 0, 0)))
+    bl = I.make_batch(spec, 11, DEV)
+    layers = [I.make_layer_weights(spec, 11, l, DEV) for l in range(spec.num_layers)]
+    caches0 = [I.make_kv_cache(spec, bl.num_blocks, 11, l, DEV) for l in range(spec.num_layers)]
+    emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, 11, DEV)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T, B = bl.num_tokens, bl.num_seqs
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, T, B, batch.max_seq_len, spec.vocab), DEV)
+    hidden = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device=DEV)
+    residual = torch.empty_like(hidden)
+    tokens = torch.empty(B, dtype=torch.int32, device=DEV)
+    logits = torch.empty((B, spec.vocab), dtype=torch.float32, device=DEV)
+    caches = [(k.clone(), v.clone()) for k, v in caches0]
+
+    def reset():
+        for (k, v), (k0, v0) in zip(caches, caches0):
+            k.copy_(k0)
+            v.copy_(v0)
+        tokens.fill_(-1)
+        logits.zero_()
+
+    def call(stream):
+        lb.stack_forward(cfg, layers, fn, lm, batch, hidden, residual, [c[0] for c in caches],
+                         [c[1] for c in caches], tokens, ws, embed=emb, input_ids=ids, out_logits=logits,
+                         stream=stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        reset()
+        call(s)
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
+    eager = (tokens.clone(), logits.clone(), [c[0].clone() for c in caches])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(s)
+    torch.cuda.synchronize()
+    reset()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
+    assert torch.equal(tokens, eager[0])
+    assert torch.equal(logits, eager[1])
+    for k, k_eager in zip([c[0] for c in caches], eager[2]):
+        assert torch.equal(k.view(torch.int16), k_eager.view(torch.int16))
