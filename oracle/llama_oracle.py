@@ -47,6 +47,10 @@ Parity status of each function:
   at position 0 are pinned; the rotate-half pairing itself is a reading (R4)
   that no invariant on the pages separates from the interleaved pairing:
   parity unpinned for the pairing choice.
+* sample: pinned (argmax limits, inverse-CDF frequencies over a grid of
+  draws, closed-form temperature and hand-worked top-k / top-p sets with ties,
+  scipy's log_softmax for the logprob); R21..R25 are readings of a page that
+  names the steps without their formulas.
 * decoder_layer / stack_forward: compositions of the pinned parts, cross-checked
   against the unfused form and brute force; no value on the pages fixes an
   end-to-end number, so end-to-end parity beyond composition is unpinned.
@@ -511,6 +515,77 @@ def greedy_argmax(logits):
     part = np.sort(logits, axis=-1)
     gap = part[..., -1] - part[..., -2]
     return tok.astype(np.int64), gap
+
+
+# ---------------------------------------------------------------------------
+# Sampler beyond greedy
+# ---------------------------------------------------------------------------
+GREEDY_TEMPERATURE = 1e-5  # R21
+
+
+def sample(logits, temperature, top_k, top_p, uniform, dtype=np.float64):
+    """[LLAMA-70B] Sampler, sample(): greedy rows take the argmax; the others
+    are scaled by their temperature, cut by top-k and top-p, and drawn at
+    random; logprobs are gathered from the raw log-softmax.  Readings:
+
+    * R21: a row is greedy when its temperature is below 1e-5 (the page merges
+      greedy results below a temperature threshold without giving it).
+    * R22: top-k keeps every token whose logit is at least the k-th largest
+      (ties at the boundary are kept); k <= 0 or k >= vocab keeps all.
+    * R23: top-p, applied after top-k to the temperature-scaled probabilities,
+      keeps every token whose probability is at least tau, the largest value
+      for which the kept mass is >= p times the mass of the top-k set (ties
+      kept); p >= 1 keeps all.
+    * R24: the random draw is an input, one uniform u in [0, 1) per row: the
+      token is the first kept token in index order at which the cumulative
+      kept probability exceeds u times the total kept probability (inverse
+      CDF).
+    * R25: the returned logprob is the raw log-softmax of the unscaled logits
+      at the sampled token (the page's raw_logprobs mode).
+
+    Returns (tokens [B] int64, logprobs [B], margins [B]): a margin is the
+    distance of the draw u * total from the nearest CDF boundary, relative to
+    the total (inf for greedy rows), which tells a comparison how close the
+    integer decision was."""
+    logits = np.asarray(logits, dtype=dtype)
+    B, V = logits.shape
+    tokens = np.empty(B, dtype=np.int64)
+    logprobs = np.empty(B, dtype=dtype)
+    margins = np.empty(B, dtype=dtype)
+    for b in range(B):
+        lrow = logits[b]
+        lmax = lrow.max()
+        log_z = lmax + np.log(np.sum(np.exp(lrow - lmax)))
+        t = float(temperature[b])
+        if t < GREEDY_TEMPERATURE:
+            tok = int(np.argmax(lrow))
+            margin = np.inf
+        else:
+            w = np.exp((lrow - lmax) / t)  # unnormalised tempered probabilities
+            keep = np.ones(V, dtype=bool)
+            k = int(top_k[b])
+            if 0 < k < V:
+                kth = np.sort(lrow)[V - k]
+                keep &= lrow >= kth
+            p = float(top_p[b])
+            if p < 1.0:
+                mass_k = np.sum(w[keep])
+                vals = np.sort(w[keep])[::-1]
+                csum = np.cumsum(vals)
+                idx = int(np.searchsorted(csum, p * mass_k, side="left"))
+                tau = vals[min(idx, vals.size - 1)]
+                keep &= w >= tau
+            wk = np.where(keep, w, 0.0)
+            c = np.cumsum(wk)
+            total = c[-1]
+            target = float(uniform[b]) * total
+            tok = int(np.searchsorted(c, target, side="right"))
+            lo = c[tok - 1] if tok > 0 else 0.0
+            margin = min(c[tok] - target, target - lo) / total
+        tokens[b] = tok
+        logprobs[b] = lrow[tok] - log_z
+        margins[b] = margin
+    return tokens, logprobs, margins
 
 
 def stack_forward(shape: LayerShape, layers: Sequence[LayerWeights], final_norm, lm_head, batch: Batch,
