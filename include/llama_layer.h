@@ -249,6 +249,28 @@ int llama_paged_attention_noalloc(const LlamaLayerConfig* cfg, const LlamaBatch*
                                   const void* k_cache, const void* v_cache, void* out, llama_stream_t stream);
 size_t llama_paged_attention_noalloc_limit(void);
 
+/* Sampling beyond greedy ([LLAMA-70B] Sampler, sample(): temperature scaling,
+ * the top-k / top-p sampler, greedy rows below a temperature threshold, the
+ * sampled tokens' logprobs).  For every row b of logits [rows, vocab] (fp32):
+ *   temperature[b] < 1e-5: the token is the argmax (lowest index on ties);
+ *   otherwise, with w_i = exp((l_i - max l) / temperature[b]):
+ *     top-k keeps every token whose logit is >= the top_k[b]-th largest
+ *       (ties kept; top_k[b] <= 0 or >= vocab keeps all),
+ *     top-p keeps, inside that set, every token with w_i >= tau, tau the
+ *       largest value whose kept mass is >= top_p[b] times the top-k set's
+ *       mass (ties kept; top_p[b] >= 1 keeps all, <= 0 only the maximum),
+ *     the token is the first kept token in index order at which the running
+ *       kept mass exceeds uniform[b] times the total kept mass.
+ * uniform [rows] holds the caller's random draws in [0, 1) (values outside are
+ * clamped); temperature, top_p [rows] fp32 and top_k [rows] int32 are device
+ * arrays.  out_tokens [rows] int32; out_logprobs [rows] fp32 (or NULL) gets
+ * the raw log-softmax of the unscaled logits at the sampled token.  Masses
+ * are exact 64-bit fixed-point sums (weights below 2^-40 count as zero), so a
+ * call is deterministic. */
+int llama_sample(const float* logits, int rows, int vocab, const float* temperature, const int32_t* top_k,
+                 const float* top_p, const float* uniform, int32_t* out_tokens, float* out_logprobs,
+                 llama_stream_t stream);
+
 /* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
  * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.
  * *detail (may be NULL) receives the code of the first place that reported. */

@@ -74,6 +74,7 @@ SIGNATURES = {
     "llama_status_string": (ctypes.c_char_p, [_I]),
     "llama_num_sms": (_I, []),
     "llama_launch_count": (ctypes.c_uint64, []),
+    "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 
 _lib = None
@@ -283,6 +284,17 @@ def get_device_error(stream=None):
 
 def num_sms() -> int:
     return int(lib().llama_num_sms())
+
+
+def sample(logits: torch.Tensor, temperature: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor,
+           uniform: torch.Tensor, out_tokens: torch.Tensor, out_logprobs: Optional[torch.Tensor] = None,
+           stream=None) -> None:
+    """Temperature / top-k / top-p sampling of fp32 logits [rows, vocab] with
+    the caller's uniforms (one per row); see llama_sample in the header."""
+    rows, vocab = logits.shape
+    st = lib().llama_sample(_ptr(logits), rows, vocab, _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(uniform),
+                            _ptr(out_tokens), _ptr(out_logprobs), _stream(stream))
+    _check(st, "llama_sample")
 
 
 def launch_count() -> int:

@@ -474,6 +474,18 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
   return cuda_status(attention_launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int llama_sample(const float* logits, int rows, int vocab, const float* temperature, const int32_t* top_k,
+                 const float* top_p, const float* uniform, int32_t* out_tokens, float* out_logprobs,
+                 llama_stream_t stream) {
+  if (rows < 0 || vocab < 1) return LLAMA_ERR_ARG;
+  if (rows == 0) return LLAMA_OK;
+  if (!logits || !temperature || !top_k || !top_p || !uniform || !out_tokens) return LLAMA_ERR_ARG;
+  if (static_cast<long long>(rows) * vocab > 0x7fffffffffffLL) return LLAMA_ERR_ARG;
+  if (rows > 0x7fffffff) return LLAMA_ERR_UNSUPPORTED;
+  return cuda_status(sample_launch(logits, rows, vocab, temperature, top_k, top_p, uniform, out_tokens, out_logprobs,
+                                   false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int llama_get_device_error(llama_stream_t stream, int* detail) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LLAMA_ERR_CUDA;
   int* w = device_error_word();

@@ -68,6 +68,12 @@ int embed_launch(const void* table, const int32_t* ids, int T, int H, int vocab,
 
 int argmax_launch(const float* logits, int rows, int vocab, int32_t* out, bool pdl, cudaStream_t s);
 
+// temperature / top-k / top-p sampling of fp32 logits rows (one uniform per
+// row supplied by the caller); out_logprobs may be null
+int sample_launch(const float* logits, int rows, int vocab, const float* temperature, const int32_t* top_k,
+                  const float* top_p, const float* uniform, int32_t* out_tokens, float* out_logprobs, bool pdl,
+                  cudaStream_t s);
+
 struct AttnArgs {
   const void* q;        // [T, nq, d] bf16 (rotated)
   const void* k_cache;  // [num_blocks, nkv, bs, d]

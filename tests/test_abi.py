@@ -94,3 +94,12 @@ def test_launch_counter_counts_only_accepted_launches(lib):
     before = lb.launch_count()
     assert lib.llama_linear(None, None, 4, 250, 256, None, 0, None, 0, None) == lb.LLAMA_ERR_ARG
     assert lb.launch_count() == before
+
+
+def test_sampler_host_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    assert lib.llama_sample(None, 0, 10, None, None, None, None, None, None, None) == lb.LLAMA_OK  # no rows
+    assert lib.llama_sample(fake, -1, 10, fake, fake, fake, fake, fake, None, None) == lb.LLAMA_ERR_ARG
+    assert lib.llama_sample(fake, 4, 0, fake, fake, fake, fake, fake, None, None) == lb.LLAMA_ERR_ARG
+    assert lib.llama_sample(fake, 4, 10, fake, None, fake, fake, fake, None, None) == lb.LLAMA_ERR_ARG
+    assert lib.llama_sample(fake, 4, 10, fake, fake, fake, None, fake, None, None) == lb.LLAMA_ERR_ARG
