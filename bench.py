@@ -680,6 +680,47 @@ def run_deep_decode(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_sampler(args, world, rank, local):
+    """llama_sample on the stack's head: 34 rows of fp32 logits over vocab
+    128256, temperature 0.8, top-k 50, top-p 0.9, one uniform per row."""
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    rows, vocab = 34, 128256
+    g = torch.Generator(device=dev)
+    g.manual_seed(77 + rank)
+    logits = torch.randn((rows, vocab), generator=g, device=dev) * 2.5
+    temp = torch.full((rows,), 0.8, device=dev)
+    top_k = torch.full((rows,), 50, dtype=torch.int32, device=dev)
+    top_p = torch.full((rows,), 0.9, device=dev)
+    u = torch.rand((rows,), generator=g, device=dev)
+    tok = torch.empty(rows, dtype=torch.int32, device=dev)
+    lp = torch.empty(rows, dtype=torch.float32, device=dev)
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(lambda: lb.sample(logits, temp, top_k, top_p, u, tok, lp), args.steps, args.warmup,
+                            world, sampler, counter=lb.launch_count)
+    nbytes = rows * vocab * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(rows * world / (ms / 1e3), 1), "unit": "sampled tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"sample: {rows} x {vocab} fp32 logits, temperature 0.8, top-k 50, top-p 0.9"},
+        "roofline": {"kernel": "k_sample", "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
+                     "algorithmic_bytes": nbytes, "traffic": None,
+                     "note": "one CTA per row and up to 13 passes over its 513 KB (L2-resident after the first): "
+                             "latency-bound, not bandwidth-bound"},
+        "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """Times the CPU oracle (fp32) on a bounded sample of the stack workload:
     each step runs one decode sequence through all layers + head."""
@@ -728,12 +769,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stack_70b",
                     choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny", "gemm_gate_up",
-                             "attn_prefill", "attn_decode", "decode_70b_80l"],
+                             "attn_prefill", "attn_decode", "decode_70b_80l", "sample"],
                     help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
                          "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
                          "attn_decode: the paged attention of the 70B prefill / decode batch alone; "
-                         "decode_70b_80l: the full-depth 70B decode step (~190 GB on the device, about a "
-                         "minute of set-up)")
+                         "decode_70b_80l: the full-depth 70B decode step (~193 GB on the device); sample: "
+                         "llama_sample on the stack's 34 x 128256 head")
     ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -745,6 +786,8 @@ def main():
         run_reference(args, world, rank)
     elif args.workload == "decode_70b_80l":
         run_deep_decode(args, world, rank, local)
+    elif args.workload == "sample":
+        run_sampler(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -12,7 +12,7 @@
 //
 // One CTA per row.  Thresholds are found on the logits' order-preserving
 // 32-bit keys (dividing by T > 0 keeps the order): top-k by a radix select on
-// counts, top-p by a radix descent on mass, four 8-bit digits each.  Masses are
+// counts, top-p by a radix descent on mass, digits of 12, 12 and 8 bits.  Masses are
 // 64-bit fixed point (w_i * 2^40, w_i in (0, 1]), so every histogram, sum and
 // scan is exact integer arithmetic: the result does not depend on the order of
 // the atomic adds, and the same call always returns the same tokens.
@@ -104,9 +104,10 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan_u64(unsigned 
   return (w > 0 ? red[w - 1] : 0ull) + inc - v;
 }
 
+constexpr int kBinsMax = 4096;  // 12-bit digits
+
 struct SampleShared {
-  unsigned int count[256];
-  unsigned long long mass[256];
+  unsigned long long hist[kBinsMax];
   unsigned long long red_u[kSampWarps];
   float red_f[kSampWarps];
   float best_v[kSampWarps];
@@ -116,68 +117,79 @@ struct SampleShared {
   int token;
 };
 
-// Largest key t with count(key >= t) >= k (the k-th largest key), by four
-// 8-bit digits from the top.
-__device__ uint32_t kth_largest_key(const float* row, int V, int k, SampleShared& sh) {
-  uint32_t prefix = 0, mask = 0;
-  unsigned int need = static_cast<unsigned int>(k);
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kSampThreads) sh.count[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < V; i += kSampThreads) {
-      const uint32_t key = order_key(row[i]);
-      if ((key & mask) == prefix) atomicAdd(&sh.count[(key >> shift) & 255u], 1u);
+// Every pass over a row goes through for_row: each thread loads kUnroll
+// elements (stride kSampThreads) before it uses any of them, so a thread keeps
+// that many L2 requests in flight (one CTA per row is all the parallelism a
+// 34-row head gives).
+constexpr int kUnroll = 8;
+
+template <class F>
+__device__ __forceinline__ void for_row(const float* __restrict__ row, int V, F&& f) {
+  for (int base = threadIdx.x; base < V; base += kSampThreads * kUnroll) {
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kSampThreads;
+      x[u] = i < V ? __ldg(row + i) : 0.f;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned int above = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (above + sh.count[d] >= need) break;
-        above += sh.count[d];
-      }
-      sh.digit = static_cast<uint32_t>(d);
-      sh.acc = need - above;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kSampThreads;
+      if (i < V) f(i, x[u]);
     }
-    __syncthreads();
-    need = static_cast<unsigned int>(sh.acc);
-    prefix |= sh.digit << shift;
-    mask |= 255u << shift;
   }
-  return prefix;
 }
 
-// Largest key t with mass(key >= t) >= target, by four 8-bit digits from the
-// top; mass in 40-bit fixed point.
-__device__ uint32_t mass_threshold_key(const float* row, int V, float lmax, float inv_t, unsigned long long target,
-                                       SampleShared& sh) {
+// Largest key t with S(key >= t) >= need, where S counts the tokens (MASS
+// false) or sums their fixed-point weights (MASS true), by digits of 12, 12
+// and 8 bits from the top.  The first digit holds the sign, the exponent and
+// three mantissa bits, so the logits of a row spread over many bins (an 8-bit
+// first digit put nearly all of them in two or three, and the shared-memory
+// atomics on those bins serialised).  The bin where the running sum from the
+// top reaches `need` is found by a block-wide scan.  Keys below floor_key are
+// left out: the answer is known to be >= floor_key, and S(key >= t) for
+// t >= floor_key does not depend on them.
+template <bool MASS>
+__device__ uint32_t threshold_key(const float* row, int V, float lmax, float inv_t, unsigned long long need,
+                                  uint32_t floor_key, SampleShared& sh) {
   uint32_t prefix = 0, mask = 0;
-  unsigned long long above_total = 0;  // mass of the keys above the current prefix range
+  unsigned long long above = 0;  // S of the keys above the current prefix range
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kSampThreads) sh.mass[i] = 0;
+  for (int level = 0; level < 3; ++level) {
+    const int bits = level < 2 ? 12 : 8;
+    const int shift = level == 0 ? 20 : (level == 1 ? 8 : 0);
+    const int nb = 1 << bits;
+    for (int i = threadIdx.x; i < nb; i += kSampThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < V; i += kSampThreads) {
-      const float l = row[i];
+    for_row(row, V, [&](int, float l) {
       const uint32_t key = order_key(l);
-      if ((key & mask) == prefix) atomicAdd(&sh.mass[(key >> shift) & 255u], fixed_weight(l, lmax, inv_t));
-    }
+      if (key >= floor_key && (key & mask) == prefix)
+        atomicAdd(&sh.hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], MASS ? fixed_weight(l, lmax, inv_t) : 1ull);
+    });
     __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long above = above_total;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (above + sh.mass[d] >= target) break;
-        above += sh.mass[d];
+    // thread t owns the bins j = nb-1-t*per .. nb-1-(t+1)*per+1 (descending)
+    const int per = nb >= kSampThreads ? nb / kSampThreads : 1;
+    const int j0 = threadIdx.x * per;
+    unsigned long long local = 0;
+    if (j0 < nb)
+      for (int q = 0; q < per; ++q) local += sh.hist[nb - 1 - (j0 + q)];
+    const unsigned long long excl = above + block_exclusive_scan_u64(local, sh.red_u);
+    if (j0 < nb && excl < need && need <= excl + local) {
+      unsigned long long run = excl;
+      for (int q = 0; q < per; ++q) {
+        const int bin = nb - 1 - (j0 + q);
+        if (run + sh.hist[bin] >= need) {
+          sh.digit = static_cast<uint32_t>(bin);
+          sh.acc = run;
+          break;
+        }
+        run += sh.hist[bin];
       }
-      sh.digit = static_cast<uint32_t>(d);
-      sh.acc = above;
     }
     __syncthreads();
-    above_total = sh.acc;
+    above = sh.acc;
     prefix |= sh.digit << shift;
-    mask |= 255u << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
   }
   return prefix;
 }
@@ -185,14 +197,13 @@ __device__ uint32_t mass_threshold_key(const float* row, int V, float lmax, floa
 __device__ __forceinline__ unsigned long long kept_mass(const float* row, int V, float lmax, float inv_t,
                                                         uint32_t t_key, SampleShared& sh) {
   unsigned long long m = 0;
-  for (int i = threadIdx.x; i < V; i += kSampThreads) {
-    const float l = row[i];
+  for_row(row, V, [&](int, float l) {
     if (order_key(l) >= t_key) m += fixed_weight(l, lmax, inv_t);
-  }
+  });
   return block_sum_u64(m, sh.red_u);
 }
 
-__global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict__ logits, int V,
+__global__ void __launch_bounds__(kSampThreads, 1) k_sample(const float* __restrict__ logits, int V,
                                                           const float* __restrict__ temperature,
                                                           const int32_t* __restrict__ top_k,
                                                           const float* __restrict__ top_p,
@@ -208,13 +219,12 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
   // maximum and its lowest index
   float best = -FLT_MAX;
   int bi = 0x7fffffff;
-  for (int i = threadIdx.x; i < V; i += kSampThreads) {
-    const float x = row[i];
+  for_row(row, V, [&](int i, float x) {  // i increases within a thread: strict > keeps the lowest
     if (x > best) {
       best = x;
       bi = i;
     }
-  }
+  });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, best, o);
@@ -245,7 +255,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
 
   // log of the raw normaliser
   float se = 0.f;
-  for (int i = threadIdx.x; i < V; i += kSampThreads) se += expf(row[i] - lmax);
+  for_row(row, V, [&](int, float x) { se += expf(x - lmax); });
   const float log_z = lmax + logf(block_sum_f(se, sh.red_f));
 
   const float t = temperature[b];
@@ -254,7 +264,8 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     const float inv_t = 1.f / t;
     const int k = top_k[b];
     uint32_t t_key = 0;  // keep everything
-    if (k > 0 && k < V) t_key = kth_largest_key(row, V, k, sh);
+    if (k > 0 && k < V)
+      t_key = threshold_key<false>(row, V, lmax, inv_t, static_cast<unsigned long long>(k), 0u, sh);
     const float p = top_p[b];
     if (p < 1.f) {
       const unsigned long long mass_k = kept_mass(row, V, lmax, inv_t, t_key, sh);
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
       // weight (p -> 0 keeps the maximum and its ties)
       unsigned long long target = static_cast<unsigned long long>(pc * static_cast<double>(mass_k));
       if (target < 1) target = 1;
-      const uint32_t t_p = mass_threshold_key(row, V, lmax, inv_t, target, sh);
+      const uint32_t t_p = threshold_key<true>(row, V, lmax, inv_t, target, t_key, sh);
       if (t_p > t_key) t_key = t_p;
     }
     const unsigned long long total = kept_mass(row, V, lmax, inv_t, t_key, sh);
