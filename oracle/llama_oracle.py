@@ -51,6 +51,11 @@ Parity status of each function:
   draws, closed-form temperature and hand-worked top-k / top-p sets with ties,
   scipy's log_softmax for the logprob); R21..R25 are readings of a page that
   names the steps without their formulas.
+* moe_route, moe_expert, moe_combine, moe_block: pinned (the page's worked
+  combine example, a single expert with k = 1 equal to the dense MLP, expert
+  relabelling invariance, weights summing to one, brute-force top-k);
+  R26..R29 are readings of pages that name the steps without their
+  precision.
 * decoder_layer / stack_forward: compositions of the pinned parts, cross-checked
   against the unfused form and brute force; no value on the pages fixes an
   end-to-end number, so end-to-end parity beyond composition is unpinned.
@@ -544,9 +549,11 @@ def sample(logits, temperature, top_k, top_p, uniform, dtype=np.float64):
       at the sampled token (the page's raw_logprobs mode).
 
     Returns (tokens [B] int64, logprobs [B], margins [B]): a margin is the
-    distance of the draw u * total from the nearest CDF boundary, relative to
-    the total (inf for greedy rows), which tells a comparison how close the
-    integer decision was."""
+    smaller of the distance of the draw u * total from the nearest CDF
+    boundary (relative to the total) and the distance of the top-p target
+    from the nearest cumulative sum of the sorted kept probabilities
+    (relative to the top-k mass); inf for greedy rows.  It tells a comparison
+    how close the integer decision was."""
     logits = np.asarray(logits, dtype=dtype)
     B, V = logits.shape
     tokens = np.empty(B, dtype=np.int64)
@@ -568,6 +575,7 @@ def sample(logits, temperature, top_k, top_p, uniform, dtype=np.float64):
                 kth = np.sort(lrow)[V - k]
                 keep &= lrow >= kth
             p = float(top_p[b])
+            p_margin = np.inf
             if p < 1.0:
                 mass_k = np.sum(w[keep])
                 vals = np.sort(w[keep])[::-1]
@@ -575,17 +583,91 @@ def sample(logits, temperature, top_k, top_p, uniform, dtype=np.float64):
                 idx = int(np.searchsorted(csum, p * mass_k, side="left"))
                 tau = vals[min(idx, vals.size - 1)]
                 keep &= w >= tau
+                near = np.abs(csum - p * mass_k)
+                p_margin = near.min() / mass_k if p > 0 else np.inf
             wk = np.where(keep, w, 0.0)
             c = np.cumsum(wk)
             total = c[-1]
             target = float(uniform[b]) * total
             tok = int(np.searchsorted(c, target, side="right"))
             lo = c[tok - 1] if tok > 0 else 0.0
-            margin = min(c[tok] - target, target - lo) / total
+            margin = min((c[tok] - target) / total, (target - lo) / total, p_margin)
         tokens[b] = tok
         logprobs[b] = lrow[tok] - log_z
         margins[b] = margin
     return tokens, logprobs, margins
+
+
+# ---------------------------------------------------------------------------
+# Sparse MoE block (Qwen3MoeSparseMoeBlock / FusedMoE)
+# ---------------------------------------------------------------------------
+
+
+def moe_route(router_logits, top_k: int):
+    """[LLAMA-70B] Qwen3MoeSparseMoeBlock: the gate gives one logit per expert
+    and every token picks its top-k experts; [WALKTHROUGH] FusedMoE:
+    torch.topk(router_logits, top_k).  Readings:
+
+    * R26: the router logits are the gate's fp32-accumulated outputs, kept in
+      fp32 for routing (like the Sampler's logits.float()); ties between equal
+      logits go to the lower expert index.
+    * R27: norm_topk_prob (true in the page's config) renormalises the top-k
+      probabilities to sum to one, i.e. the weights are the softmax of the k
+      selected logits.
+
+    Returns (ids [T, k] int64 in descending logit order, weights [T, k], gap
+    [T]): gap is the distance between the k-th and (k+1)-th largest logits,
+    which tells a comparison how close the expert choice was."""
+    x = np.asarray(router_logits, dtype=np.float64)
+    T, E = x.shape
+    order = np.argsort(-x, axis=1, kind="stable")  # stable: equal logits keep index order
+    ids = order[:, :top_k]
+    sel = np.take_along_axis(x, ids, axis=1)
+    w = np.exp(sel - sel[:, :1])
+    w = w / w.sum(axis=1, keepdims=True)
+    if top_k < E:
+        nxt = np.take_along_axis(x, order[:, top_k:top_k + 1], axis=1)[:, 0]
+        gap = sel[:, -1] - nxt
+    else:
+        gap = np.full(T, np.inf)
+    return ids.astype(np.int64), w, gap
+
+
+def moe_expert(x, w13_e, w2_e, dtype=np.float64, bf16_tensors=True):
+    """One expert: a two-layer FFN with SiluAndMul, w13_e [2I, H] holding the
+    gate rows then the up rows ([WALKTHROUGH] FusedMoE w13 / w2; [LLAMA-70B]
+    每个专家是双层FFN 2048 -> 768 -> 2048).  R28: as for the dense MLP (R3) the
+    merged projection, SiluAndMul and the expert output are stored in bf16."""
+    gu = store(linear(x, w13_e, dtype), bf16_tensors, dtype)
+    act = store(silu_and_mul(gu, dtype), bf16_tensors, dtype)
+    return store(linear(act, w2_e, dtype), bf16_tensors, dtype)
+
+
+def moe_combine(expert_outputs, weights, dtype=np.float64):
+    """[LLAMA-70B] the token's MoE output is the sum of its experts' outputs,
+    each multiplied by its routing weight.  R29: the sum runs in ``dtype``
+    over the k experts in routing order."""
+    out = np.zeros_like(np.asarray(expert_outputs[0], dtype=dtype))
+    for y, w in zip(expert_outputs, weights):
+        out = out + np.asarray(w, dtype=dtype) * np.asarray(y, dtype=dtype)
+    return out
+
+
+def moe_block(h, w_router, w13, w2, top_k: int, dtype=np.float64, bf16_tensors=True):
+    """Qwen3MoeSparseMoeBlock forward over tokens h [T, H]: router logits
+    (R26), top-k routing with renormalised weights (R27), the selected experts
+    (R28) and the weighted sum (R29), no shared expert; the block's output is
+    stored in bf16 (R3).  w_router [E, H], w13 [E, 2I, H], w2 [E, H, I].
+    Returns (out [T, H], ids, weights, gap)."""
+    h = np.asarray(h, dtype=dtype)
+    logits = linear(h, w_router, dtype)
+    ids, wts, gap = moe_route(logits, top_k)
+    T = h.shape[0]
+    out = np.zeros((T, np.asarray(w2).shape[1]), dtype=dtype)
+    for t in range(T):
+        ys = [moe_expert(h[t:t + 1], w13[e], w2[e], dtype, bf16_tensors)[0] for e in ids[t]]
+        out[t] = moe_combine(ys, wts[t], dtype)
+    return store(out, bf16_tensors, dtype), ids, wts, gap
 
 
 def stack_forward(shape: LayerShape, layers: Sequence[LayerWeights], final_norm, lm_head, batch: Batch,
