@@ -721,6 +721,62 @@ def run_sampler(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_moe(args, world, rank, local):
+    """The sparse MoE block (llama_moe_forward) on Qwen3-30B-A3B shapes: hidden
+    2048, 128 experts, top-8, moe_intermediate 768, random-init weights.
+    moe_decode: 64 tokens (HBM-bound: the experts the routing touches are read
+    once); moe_prefill: 4096 tokens (tensor-bound)."""
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    from llama_decoder_layer_gb300 import inputs as I
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    H, E, K, Im = 2048, 128, 8, 768
+    T = 64 if args.workload == "moe_decode" else 4096
+    seed = 500 + rank
+    h = I.normal_bf16((T, H), 1.0, 0.0, seed, dev)
+    wr = I.normal_bf16((E, H), 0.02, 0.0, seed + 1, dev)
+    w13 = I.normal_bf16((E, 2 * Im, H), 0.02, 0.0, seed + 2, dev)
+    w2 = I.normal_bf16((E, H, Im), 0.02, 0.0, seed + 3, dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = lb.alloc_workspace(lb.moe_workspace_size(H, E, K, Im, T), dev)
+    lb.moe_forward(h, wr, w13, w2, K, out, ws, ids)
+    torch.cuda.synchronize()
+    touched = int(torch.unique(ids).numel())
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(lambda: lb.moe_forward(h, wr, w13, w2, K, out, ws), args.steps, args.warmup, world,
+                            sampler, counter=lb.launch_count)
+    st, detail = lb.get_device_error()
+    if st != lb.LLAMA_OK:
+        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+    flops = 2.0 * T * (E * H + K * (2 * Im * H + H * Im))
+    nbytes = (E * H + touched * (2 * Im * H + H * Im)) * 2 + 2 * T * H * 2
+    if T <= 256:
+        gbs = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes": nbytes, "experts_touched": touched, "traffic": None}
+    else:
+        tf = flops / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tf / peaks["bf16_tflops"], 4), "peak_source": f"bf16_tflops ({peak_src}, burst)",
+                "algorithmic_flops": flops, "traffic": None}
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(T * world / (ms / 1e3), 1), "unit": "tokens/s through the MoE block", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": f"{args.workload}: Qwen3-30B-A3B MoE block, {T} tokens, hidden {H}, {E} experts, "
+                               f"top-{K}, moe_intermediate {Im}"},
+        "roofline": roof, "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """Times the CPU oracle (fp32) on a bounded sample of the stack workload:
     each step runs one decode sequence through all layers + head."""
@@ -769,12 +825,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stack_70b",
                     choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny", "gemm_gate_up",
-                             "attn_prefill", "attn_decode", "decode_70b_80l", "sample"],
+                             "attn_prefill", "attn_decode", "decode_70b_80l", "sample", "moe_decode",
+                             "moe_prefill"],
                     help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
                          "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
                          "attn_decode: the paged attention of the 70B prefill / decode batch alone; "
                          "decode_70b_80l: the full-depth 70B decode step (~193 GB on the device); sample: "
-                         "llama_sample on the stack's 34 x 128256 head")
+                         "llama_sample on the stack's 34 x 128256 head; moe_decode / moe_prefill: the "
+                         "Qwen3-30B-A3B MoE block over 64 / 4096 tokens")
     ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -788,6 +846,8 @@ def main():
         run_deep_decode(args, world, rank, local)
     elif args.workload == "sample":
         run_sampler(args, world, rank, local)
+    elif args.workload in ("moe_decode", "moe_prefill"):
+        run_moe(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -271,6 +271,36 @@ int llama_sample(const float* logits, int rows, int vocab, const float* temperat
                  const float* top_p, const float* uniform, int32_t* out_tokens, float* out_logprobs,
                  llama_stream_t stream);
 
+/* Sparse MoE block (the Qwen3 MoE MLP: [LLAMA-70B] Qwen3MoeSparseMoeBlock;
+ * [WALKTHROUGH] Fused MoE).  For every token row t of h [num_tokens, hidden]:
+ *   logits = h[t] w_router^T (fp32 accumulation, kept in fp32),
+ *   the top_k experts by logit (equal logits: the lower expert index) with
+ *   weights = softmax of their k logits (norm_topk_prob),
+ *   y_e = SiluAndMul(h[t] w13[e]^T) w2[e]^T for each of them, every module
+ *   output stored in bf16 like the dense MLP,
+ *   out[t] = sum over the k experts, in routing order, of weight * y_e (fp32
+ *   sum, bf16 out).  No shared expert.
+ * w_router [num_experts, hidden], w13 [num_experts, 2*moe_intermediate,
+ * hidden] (gate rows then up rows per expert), w2 [num_experts, hidden,
+ * moe_intermediate], all bf16; out [num_tokens, hidden] bf16.  The chosen
+ * experts and weights go to out_expert_ids [num_tokens, top_k] int32 and
+ * out_expert_weights [num_tokens, top_k] fp32 when those are not NULL.
+ * num_experts <= 512, top_k <= 32, hidden and moe_intermediate multiples of 8.
+ * The workspace (llama_moe_workspace_size) holds the router logits, the
+ * routing, the tokens permuted into per-expert segments of whole 128-row tiles
+ * and the experts' intermediate activations. */
+typedef struct {
+  int hidden;
+  int num_experts;
+  int top_k;
+  int moe_intermediate;
+} LlamaMoeConfig;
+
+size_t llama_moe_workspace_size(const LlamaMoeConfig* cfg, int max_tokens);
+int llama_moe_forward(const LlamaMoeConfig* cfg, const void* h, int num_tokens, const void* w_router, const void* w13,
+                      const void* w2, void* out, int32_t* out_expert_ids, float* out_expert_weights, void* workspace,
+                      size_t workspace_bytes, llama_stream_t stream);
+
 /* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
  * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.
  * *detail (may be NULL) receives the code of the first place that reported. */

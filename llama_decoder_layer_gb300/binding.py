@@ -47,6 +47,11 @@ class LlamaLayerWeights(ctypes.Structure):
                 ("ln2_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
 
 
+class LlamaMoeConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("moe_intermediate", ctypes.c_int)]
+
+
 class LlamaBatch(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_query_len", ctypes.c_int), ("max_seq_len", ctypes.c_int),
@@ -75,6 +80,8 @@ SIGNATURES = {
     "llama_num_sms": (_I, []),
     "llama_launch_count": (ctypes.c_uint64, []),
     "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
+    "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
 }
 
 _lib = None
@@ -295,6 +302,24 @@ def sample(logits: torch.Tensor, temperature: torch.Tensor, top_k: torch.Tensor,
     st = lib().llama_sample(_ptr(logits), rows, vocab, _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(uniform),
                             _ptr(out_tokens), _ptr(out_logprobs), _stream(stream))
     _check(st, "llama_sample")
+
+
+def moe_workspace_size(hidden: int, num_experts: int, top_k: int, moe_intermediate: int, max_tokens: int) -> int:
+    c = LlamaMoeConfig(hidden, num_experts, top_k, moe_intermediate)
+    return int(lib().llama_moe_workspace_size(ctypes.byref(c), max_tokens))
+
+
+def moe_forward(h: torch.Tensor, w_router: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, top_k: int,
+                out: torch.Tensor, workspace: torch.Tensor, out_ids: Optional[torch.Tensor] = None,
+                out_weights: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The sparse MoE block over h [T, H]: w_router [E, H], w13 [E, 2I, H],
+    w2 [E, H, I]; see llama_moe_forward in the header."""
+    E, H = w_router.shape
+    c = LlamaMoeConfig(H, E, top_k, int(w2.shape[2]))
+    st = lib().llama_moe_forward(ctypes.byref(c), _ptr(h), int(h.shape[0]), _ptr(w_router), _ptr(w13), _ptr(w2),
+                                 _ptr(out), _ptr(out_ids), _ptr(out_weights), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(st, "llama_moe_forward")
 
 
 def launch_count() -> int:

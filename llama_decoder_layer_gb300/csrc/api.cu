@@ -486,6 +486,52 @@ int llama_sample(const float* logits, int rows, int vocab, const float* temperat
                                    false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int check_moe_cfg(const LlamaMoeConfig* c) {
+  if (c == nullptr) return LLAMA_ERR_ARG;
+  if (c->hidden < 8 || c->num_experts < 1 || c->top_k < 1 || c->moe_intermediate < 8) return LLAMA_ERR_ARG;
+  if (c->top_k > c->num_experts) return LLAMA_ERR_ARG;
+  if (c->hidden % 8 || c->moe_intermediate % 8) return LLAMA_ERR_UNSUPPORTED;
+  if (c->num_experts > 512 || c->top_k > 32) return LLAMA_ERR_UNSUPPORTED;
+  return LLAMA_OK;
+}
+
+size_t llama_moe_workspace_size(const LlamaMoeConfig* cfg, int max_tokens) {
+  if (check_moe_cfg(cfg) != LLAMA_OK || max_tokens < 0) return 0;
+  return moe_layout(max_tokens, cfg->hidden, cfg->num_experts, cfg->top_k, cfg->moe_intermediate, num_sms()).total;
+}
+
+int llama_moe_forward(const LlamaMoeConfig* cfg, const void* h, int num_tokens, const void* w_router, const void* w13,
+                      const void* w2, void* out, int32_t* out_expert_ids, float* out_expert_weights, void* workspace,
+                      size_t workspace_bytes, llama_stream_t stream) {
+  int st = check_moe_cfg(cfg);
+  if (st) return st;
+  if (num_tokens < 0) return LLAMA_ERR_ARG;
+  if (num_tokens == 0) return LLAMA_OK;
+  if (!h || !w_router || !w13 || !w2 || !out) return LLAMA_ERR_ARG;
+  if (!a16(h) || !a16(w_router) || !a16(w13) || !a16(w2) || !a16(out)) return LLAMA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_tokens) * cfg->top_k > 0x7fffffffLL) return LLAMA_ERR_UNSUPPORTED;
+  const MoeLayout L =
+      moe_layout(num_tokens, cfg->hidden, cfg->num_experts, cfg->top_k, cfg->moe_intermediate, num_sms());
+  if (L.rows > 0x7fffffffULL) return LLAMA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
+  MoeArgs a{};
+  a.h = h;
+  a.w_router = w_router;
+  a.w13 = w13;
+  a.w2 = w2;
+  a.out = out;
+  a.out_ids = out_expert_ids;
+  a.out_wts = out_expert_weights;
+  a.T = num_tokens;
+  a.H = cfg->hidden;
+  a.E = cfg->num_experts;
+  a.K = cfg->top_k;
+  a.I = cfg->moe_intermediate;
+  a.ws = ws_base(workspace);
+  a.err = device_error_word();
+  return cuda_status(moe_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int llama_get_device_error(llama_stream_t stream, int* detail) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LLAMA_ERR_CUDA;
   int* w = device_error_word();

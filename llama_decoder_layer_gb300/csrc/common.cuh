@@ -33,6 +33,7 @@ enum : int {
   kWhereGemmEpilogue = 18,
   kWhereAttnDecode = 32,
   kWhereAttnPrefill = 33,
+  kWhereMoe = 48,
 };
 
 __device__ __forceinline__ void report_error(int* err, int flag, int where) {

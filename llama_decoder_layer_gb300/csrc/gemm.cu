@@ -73,10 +73,19 @@ struct GemmParams {
   int* err;
   QkvEpilogueArgs qkv;
   float2 rope_tab[64];  // qkv epilogue: per rotated pair, revolutions per position as (hi, lo)
+  // grouped mode (the experts of an MoE block): tiles come from a list built on
+  // the device, {A row, B base row of the tile's expert, N tile, valid rows}
+  const int4* group_tiles;
+  const int* group_count;
 };
 
 struct Work {
   int tile, kb0, kb1;
+};
+
+// A row, B rows, output tile coordinates and the row bound of a work item
+struct TileCoords {
+  int tm, tn, arow, brow0, m_limit;
 };
 
 __device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor, long long end, Work& w) {
@@ -90,7 +99,8 @@ __device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor
     cursor = e;
     return true;
   }
-  if (cursor >= p.tiles) return false;
+  const long long n_tiles = p.group_tiles != nullptr ? *p.group_count : p.tiles;
+  if (cursor >= n_tiles) return false;
   w.tile = static_cast<int>(cursor);
   w.kb0 = 0;
   w.kb1 = p.kb;
@@ -107,6 +117,24 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
   const int r = tile - g * group;
   tm = first_m + r % gm;
   tn = r / gm;
+}
+
+__device__ __forceinline__ TileCoords resolve_tile(const GemmParams& p, int tile) {
+  TileCoords c;
+  if (p.group_tiles != nullptr) {
+    const int4 t = p.group_tiles[tile];
+    c.tm = t.x / BM;
+    c.tn = t.z;
+    c.arow = t.x;
+    c.brow0 = t.y + t.z * p.b_tile_rows;
+    c.m_limit = t.x + t.w;
+  } else {
+    tile_coords(p, tile, c.tm, c.tn);
+    c.arow = c.tm * BM;
+    c.brow0 = c.tn * p.b_tile_rows;
+    c.m_limit = p.M;
+  }
+  return c;
 }
 
 __host__ __device__ __forceinline__ long long sk_start(long long units, int grid, int c) {
@@ -336,9 +364,9 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, int tm, int t
 // the heads of the tile.
 template <int EPI, class Loader>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int tn, int row_in_tile, Loader& ld,
-                                              const float2* rope_tab) {
+                                              const float2* rope_tab, int m_limit) {
   const int row = tm * BM + row_in_tile;
-  const bool valid = row < p.M;
+  const bool valid = row < m_limit;
   if constexpr (EPI == kEpiBf16 || EPI == kEpiF32) {
     const int n_base = tn * BN;
 #pragma unroll 1
@@ -526,11 +554,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     Work w;
     bool ok = true;
+    if (p.group_tiles != nullptr) finish_wait();  // the tile list itself comes from the previous kernel
     while (ok && next_work(p, cursor, end, w)) {
-      int tm, tn;
-      tile_coords(p, w.tile, tm, tn);
-      const int arow = tm * BM;
-      const int brow0 = tn * p.b_tile_rows;
+      const TileCoords tc = resolve_tile(p, w.tile);
+      const int arow = tc.arow;
+      const int brow0 = tc.brow0;
       const int brow1 = brow0 + p.b_row_step;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
@@ -642,13 +670,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      int tm, tn;
-      tile_coords(p, w.tile, tm, tn);
+      const TileCoords tc = resolve_tile(p, w.tile);
+      const int tm = tc.tm, tn = tc.tn;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-      const bool valid = tm * BM + row_in_tile < p.M;
+      const bool valid = tm * BM + row_in_tile < tc.m_limit;
       if (w.kb0 == 0 && w.kb1 == p.kb) {
         TmemLoader ld{taddr};
-        epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab);
+        epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab, tc.m_limit);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -1097,8 +1125,12 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   const int sms = num_sms();
   // At most sms / 2 tiles: split K over clusters of S CTAs (S as large as the
   // SMs allow, at least two k-blocks per CTA, all clusters resident at once).
+  p.group_tiles = static_cast<const int4*>(a.group_tiles);
+  p.group_count = a.group_count;
+  const bool grouped = a.group_tiles != nullptr;
+  if (grouped && a.group_count == nullptr) return cudaErrorInvalidValue;
   int cluster = 0;
-  if ((a.force_mode == -1 || a.force_mode == 2) && p.tiles * 2 <= sms) {
+  if (!grouped && (a.force_mode == -1 || a.force_mode == 2) && p.tiles * 2 <= sms) {
     for (int S = sms / p.tiles < 8 ? sms / p.tiles : 8; S >= 2; --S) {
       if (p.kb < 2 * S || max_active_clusters_of(a.epi, S) < p.tiles) continue;
       cluster = S;
@@ -1108,6 +1140,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   bool sk = cluster == 0 && p.tiles < 2 * sms;
   if (a.force_mode == 0) sk = false;
   if (a.force_mode == 1) sk = true;
+  if (grouped) sk = false;
   p.units = static_cast<long long>(p.tiles) * p.kb;
   if (sk) {
     long long g = p.units < sms ? p.units : sms;
@@ -1115,13 +1148,13 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
     p.grid = static_cast<int>(g);
     if (gemm_partials_bytes(p.grid) > a.partials_bytes || a.partials == nullptr) return cudaErrorInvalidValue;
   } else {
-    p.grid = p.tiles < sms ? p.tiles : sms;
+    p.grid = grouped ? sms : (p.tiles < sms ? p.tiles : sms);  // grouped: the tile count is on the device
   }
   p.sk = sk ? 1 : 0;
 
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a.A, a.M, a.K, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, a.B, a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, a.B, a.b_rows > 0 ? a.b_rows : a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
   switch (a.epi) {
     case kEpiBf16:
       return launch_typed<kEpiBf16>(ta, tb, p, cluster, a.pdl != 0, s);

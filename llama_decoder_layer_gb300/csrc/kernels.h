@@ -44,6 +44,13 @@ struct GemmArgs {
   int* err;
   int force_mode;  // -1 auto, 0 data-parallel, 1 stream-K (tests)
   int pdl;         // 1: may start before the previous kernel on the stream (one of this library's) completes
+  // Grouped mode (MoE experts): when group_tiles is set, the tiles are
+  // {A row, B base row, N tile, valid rows} entries of a device list with
+  // *group_count entries (written by a kernel earlier in the call); B holds
+  // b_rows rows (all experts stacked) and A holds M rows.  Data-parallel only.
+  const void* group_tiles;
+  const int* group_count;
+  int b_rows;
 };
 
 size_t gemm_partials_bytes(int num_sms);
@@ -98,6 +105,29 @@ size_t attn_partials_bytes(int B, int T, int max_seq_len, int nq, int head_dim);
 // *joined (if given) is set when the caller's stream waited on the side
 // stream: the next kernel then has a full dependency, not a programmatic one.
 int attention_launch(const AttnArgs& a, cudaStream_t s, bool* joined = nullptr);
+
+// Sparse MoE block: workspace layout (byte offsets from a 256-aligned base)
+// and the launch sequence.
+struct MoeLayout {
+  size_t rows;  // rows of the permuted activation matrices (segments padded to 128)
+  size_t logits, ids, wts, slot_row, offset, fill, counts, tiles1, tiles2, x_perm, act, y_perm, gpart, total;
+  size_t gpart_bytes;
+};
+MoeLayout moe_layout(int T, int H, int E, int K, int I, int sms);
+
+struct MoeArgs {
+  const void* h;         // [T, H] bf16
+  const void* w_router;  // [E, H]
+  const void* w13;       // [E, 2I, H]: gate rows then up rows per expert
+  const void* w2;        // [E, H, I]
+  void* out;             // [T, H] bf16
+  int32_t* out_ids;      // [T, K] or null
+  float* out_wts;        // [T, K] or null
+  int T, H, E, K, I;
+  uint8_t* ws;           // 256-aligned, moe_layout(...).total - 256 bytes
+  int* err;
+};
+int moe_launch(const MoeArgs& a, cudaStream_t s);
 
 int num_sms();
 

@@ -1,0 +1,87 @@
+"""llama_moe_forward against the oracle's MoE block on the same bf16 values.
+
+The expert choice is an integer that floating point decides (fp32 router
+accumulation on the GPU, fp64 in the oracle): the chosen experts and weights
+must match wherever the oracle's gap between the k-th and (k+1)-th logit
+exceeds 1e-4, and the block output must be within 2e-2 * max|ref| on those
+rows.  Two calls are bit-identical (the order in which tokens land inside an
+expert's segment does not matter)."""
+
+import numpy as np
+import pytest
+import torch
+
+from llama_decoder_layer_gb300 import binding as lb
+from llama_decoder_layer_gb300 import build as lbuild
+from llama_decoder_layer_gb300 import inputs as I
+from oracle import llama_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lbuild.build()
+    lb.lib()
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("T,H,E,K,Im", [
+    (37, 256, 16, 4, 128),      # small, ragged token count
+    (64, 2048, 128, 8, 768),    # Qwen3-30B-A3B shapes, decode-sized batch
+    (300, 2048, 128, 8, 768),   # prefill-sized, several tiles per expert
+    (5, 128, 8, 8, 64),         # k = E: every expert for every token
+    (1, 256, 32, 2, 96),        # one token; moe_intermediate not a multiple of 128
+])
+def test_moe_block_matches_the_oracle(T, H, E, K, Im):
+    seed = T * 7 + E
+    h = I.normal_bf16((T, H), 1.0, 0.0, seed, DEV)
+    wr = I.normal_bf16((E, H), 0.02, 0.0, seed + 1, DEV)
+    w13 = I.normal_bf16((E, 2 * Im, H), 0.02, 0.0, seed + 2, DEV)
+    w2 = I.normal_bf16((E, H, Im), 0.02, 0.0, seed + 3, DEV)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, K), dtype=torch.float32, device=DEV)
+    ws = lb.alloc_workspace(lb.moe_workspace_size(H, E, K, Im, T), DEV)
+    lb.moe_forward(h, wr, w13, w2, K, out, ws, ids, wts)
+    out2 = torch.empty_like(out)
+    lb.moe_forward(h, wr, w13, w2, K, out2, ws)
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), "two calls differ"
+
+    ref, ref_ids, ref_w, gap = O.moe_block(_f64(h), _f64(wr), _f64(w13), _f64(w2), K)
+    gids = ids.cpu().numpy()
+    gw = wts.cpu().numpy()
+    sure = gap > 1e-4
+    assert sure.sum() >= max(1, int(0.9 * T))
+    assert np.array_equal(gids[sure], ref_ids[sure])
+    assert np.max(np.abs(gw[sure] - ref_w[sure])) < 1e-4
+    got = out.float().cpu().numpy()
+    err = np.max(np.abs(got[sure] - ref[sure]))
+    assert err <= 2e-2 * np.max(np.abs(ref[sure])), (err, np.max(np.abs(ref[sure])))
+
+
+def test_moe_routing_concentrated_on_few_experts():
+    # a router that sends every token to the same experts: one segment holds all rows
+    T, H, E, K, Im = 200, 256, 16, 2, 128
+    h = I.normal_bf16((T, H), 1.0, 0.0, 5, DEV)
+    wr = torch.zeros((E, H), dtype=torch.bfloat16, device=DEV)
+    wr[3] = 0.05
+    wr[11] = 0.04
+    h = h.abs()  # positive rows: experts 3 and 11 win for every token
+    w13 = I.normal_bf16((E, 2 * Im, H), 0.02, 0.0, 6, DEV)
+    w2 = I.normal_bf16((E, H, Im), 0.02, 0.0, 7, DEV)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    ws = lb.alloc_workspace(lb.moe_workspace_size(H, E, K, Im, T), DEV)
+    lb.moe_forward(h, wr, w13, w2, K, out, ws, ids)
+    torch.cuda.synchronize()
+    assert np.all(ids.cpu().numpy() == np.array([3, 11]))
+    ref, _, _, _ = O.moe_block(_f64(h), _f64(wr), _f64(w13), _f64(w2), K)
+    got = out.float().cpu().numpy()
+    assert np.max(np.abs(got - ref)) <= 2e-2 * np.max(np.abs(ref))
