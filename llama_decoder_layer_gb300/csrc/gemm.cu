@@ -81,14 +81,32 @@ struct GemmParams {
 
 struct Work {
   int tile, kb0, kb1;
+  int4 desc;  // grouped mode: the tile's list entry
 };
+
+// Grouped mode: the tile count is read once and every list entry one tile
+// ahead of its use, so no role waits on a global load at a tile boundary.
+struct Feed {
+  long long count;
+  int4 next;
+};
+
+__device__ __forceinline__ Feed feed_init(const GemmParams& p, long long cursor) {
+  Feed f{0, make_int4(0, 0, 0, 0)};
+  if (p.group_tiles != nullptr) {
+    f.count = *p.group_count;
+    if (cursor < f.count) f.next = p.group_tiles[cursor];
+  }
+  return f;
+}
 
 // A row, B rows, output tile coordinates and the row bound of a work item
 struct TileCoords {
   int tm, tn, arow, brow0, m_limit;
 };
 
-__device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor, long long end, Work& w) {
+__device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor, long long end, Work& w,
+                                          Feed& feed) {
   if (p.sk) {
     if (cursor >= end) return false;
     w.tile = static_cast<int>(cursor / p.kb);
@@ -99,12 +117,16 @@ __device__ __forceinline__ bool next_work(const GemmParams& p, long long& cursor
     cursor = e;
     return true;
   }
-  const long long n_tiles = p.group_tiles != nullptr ? *p.group_count : p.tiles;
-  if (cursor >= n_tiles) return false;
+  const bool grouped = p.group_tiles != nullptr;
+  if (cursor >= (grouped ? feed.count : p.tiles)) return false;
   w.tile = static_cast<int>(cursor);
   w.kb0 = 0;
   w.kb1 = p.kb;
   cursor += p.grid;
+  if (grouped) {
+    w.desc = feed.next;
+    if (cursor < feed.count) feed.next = p.group_tiles[cursor];
+  }
   return true;
 }
 
@@ -119,17 +141,17 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
   tn = r / gm;
 }
 
-__device__ __forceinline__ TileCoords resolve_tile(const GemmParams& p, int tile) {
+__device__ __forceinline__ TileCoords resolve_tile(const GemmParams& p, const Work& w) {
   TileCoords c;
   if (p.group_tiles != nullptr) {
-    const int4 t = p.group_tiles[tile];
+    const int4 t = w.desc;
     c.tm = t.x / BM;
     c.tn = t.z;
     c.arow = t.x;
     c.brow0 = t.y + t.z * p.b_tile_rows;
     c.m_limit = t.x + t.w;
   } else {
-    tile_coords(p, tile, c.tm, c.tn);
+    tile_coords(p, w.tile, c.tm, c.tn);
     c.arow = c.tm * BM;
     c.brow0 = c.tn * p.b_tile_rows;
     c.m_limit = p.M;
@@ -555,8 +577,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     Work w;
     bool ok = true;
     if (p.group_tiles != nullptr) finish_wait();  // the tile list itself comes from the previous kernel
-    while (ok && next_work(p, cursor, end, w)) {
-      const TileCoords tc = resolve_tile(p, w.tile);
+    Feed feed = feed_init(p, cursor);
+    while (ok && next_work(p, cursor, end, w, feed)) {
+      const TileCoords tc = resolve_tile(p, w);
       const int arow = tc.arow;
       const int brow0 = tc.brow0;
       const int brow1 = brow0 + p.b_row_step;
@@ -610,7 +633,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true, issued = false;
     Work w;
-    while (ok && next_work(p, cursor, end, w)) {
+    Feed feed = feed_init(p, cursor);
+    while (ok && next_work(p, cursor, end, w, feed)) {
       if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
         ok = false;
         break;
@@ -664,13 +688,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int nseg = 0;
     Work w;
     bool ok = true;
-    while (next_work(p, cursor, end, w)) {
+    Feed feed = feed_init(p, cursor);
+    while (next_work(p, cursor, end, w, feed)) {
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const TileCoords tc = resolve_tile(p, w.tile);
+      const TileCoords tc = resolve_tile(p, w);
       const int tm = tc.tm, tn = tc.tn;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       const bool valid = tm * BM + row_in_tile < tc.m_limit;

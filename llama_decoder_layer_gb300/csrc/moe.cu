@@ -120,6 +120,28 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* red) {
   return (w > 0 ? red[w - 1] : 0) + inc - v;
 }
 
+// Loads the expert ids of pairs [i0, i0 + 4 * kPlanBatch * kPlanThreads), every
+// load of a thread issued before any is used; ids beyond `pairs` read as -1.
+constexpr int kPlanBatch = 4;
+__device__ __forceinline__ void plan_load_ids(const int32_t* __restrict__ ids, int pairs, int i0,
+                                              int (&v)[kPlanBatch][4]) {
+  const int4* ids4 = reinterpret_cast<const int4*>(ids);
+#pragma unroll
+  for (int b = 0; b < kPlanBatch; ++b) {
+    const int i = i0 + 4 * (b * kPlanThreads + static_cast<int>(threadIdx.x));
+    if (i + 3 < pairs) {
+      const int4 q = ids4[i / 4];
+      v[b][0] = q.x;
+      v[b][1] = q.y;
+      v[b][2] = q.z;
+      v[b][3] = q.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[b][j] = i + j < pairs ? ids[i + j] : -1;
+    }
+  }
+}
+
 // One CTA: tokens per expert, the padded segment offsets, a zeroed fill
 // counter per expert, and the tile lists of both grouped GEMMs, {A row, B base
 // row of the expert, N tile, valid rows}; the list lengths go to counts[0..1].
@@ -134,10 +156,17 @@ __global__ void __launch_bounds__(kPlanThreads) k_moe_plan(const int32_t* __rest
   const int e = threadIdx.x;
   cnt[e] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < pairs; i += kPlanThreads) {
-    const int x = ids[i];
-    if (x >= 0 && x < E) atomicAdd(&cnt[x], 1);
-    else report_error(err, kErrGuard, kWhereMoe);
+  for (int i0 = 0; i0 < pairs; i0 += 4 * kPlanBatch * kPlanThreads) {
+    int v[kPlanBatch][4];
+    plan_load_ids(ids, pairs, i0, v);
+#pragma unroll
+    for (int b = 0; b < kPlanBatch; ++b)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int x = v[b][j];
+        if (x >= 0 && x < E) atomicAdd(&cnt[x], 1);
+        else if (i0 + 4 * (b * kPlanThreads + e) + j < pairs) report_error(err, kErrGuard, kWhereMoe);
+      }
   }
   __syncthreads();
   const int c = e < E ? cnt[e] : 0;
@@ -160,24 +189,41 @@ __global__ void __launch_bounds__(kPlanThreads) k_moe_plan(const int32_t* __rest
   }
 }
 
-// One CTA per (token, slot): place the pair in its expert's segment and copy
-// the token's row there.
-__global__ void __launch_bounds__(128) k_moe_scatter(const uint4* __restrict__ h, const int32_t* __restrict__ ids,
-                                                     int K, int E, int chunks, const int32_t* __restrict__ offset,
-                                                     int32_t* __restrict__ fill, int32_t* __restrict__ slot_row,
-                                                     uint4* __restrict__ x_perm) {
-  __shared__ int row_s;
+// One warp per (token, slot): place the pair in its expert's segment and copy
+// the token's row there, eight 16-byte loads in flight per lane.
+constexpr int kScatterWarps = 8;
+constexpr int kScatterUnroll = 8;
+__global__ void __launch_bounds__(kScatterWarps * 32) k_moe_scatter(
+    const uint4* __restrict__ h, const int32_t* __restrict__ ids, int pairs, int K, int E, int chunks,
+    const int32_t* __restrict__ offset, int32_t* __restrict__ fill, int32_t* __restrict__ slot_row,
+    uint4* __restrict__ x_perm) {
   pdl_wait();
-  const int i = blockIdx.x, t = i / K;
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
+  if (i >= pairs) return;
   const int e = ids[i];
   if (e < 0 || e >= E) return;  // reported by the planning kernel
-  if (threadIdx.x == 0) {
-    row_s = offset[e] + atomicAdd(&fill[e], 1);
-    slot_row[i] = row_s;
+  int row = 0;
+  if (lane == 0) {
+    row = offset[e] + atomicAdd(&fill[e], 1);
+    slot_row[i] = row;
   }
-  __syncthreads();
-  const size_t src = static_cast<size_t>(t) * chunks, dst = static_cast<size_t>(row_s) * chunks;
-  for (int c = threadIdx.x; c < chunks; c += blockDim.x) x_perm[dst + c] = h[src + c];
+  row = __shfl_sync(0xffffffffu, row, 0);
+  const uint4* src = h + static_cast<size_t>(i / K) * chunks;
+  uint4* dst = x_perm + static_cast<size_t>(row) * chunks;
+  for (int c0 = 0; c0 < chunks; c0 += 32 * kScatterUnroll) {
+    uint4 v[kScatterUnroll];
+#pragma unroll
+    for (int u = 0; u < kScatterUnroll; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < chunks) v[u] = src[c];
+    }
+#pragma unroll
+    for (int u = 0; u < kScatterUnroll; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < chunks) dst[c] = v[u];
+    }
+  }
 }
 
 // out[t] = sum_j w[t, j] * y[row(t, j)], fp32 in routing order, bf16 out.
@@ -299,8 +345,9 @@ int moe_launch(const MoeArgs& a, cudaStream_t s) {
   ce = launch_kernel(k_moe_plan, dim3(1), dim3(kPlanThreads), 0, s, true, ids, pairs, a.E, nt1, 2 * a.I, nt2, a.H,
                      offset, fill, tiles1, tiles2, counts, a.err);
   if (ce != cudaSuccess) return ce;
-  ce = launch_kernel(k_moe_scatter, dim3(pairs), dim3(128), 0, s, true, static_cast<const uint4*>(a.h), ids, a.K,
-                     a.E, chunks, offset, fill, slot_row, static_cast<uint4*>(x_perm));
+  ce = launch_kernel(k_moe_scatter, dim3((pairs + kScatterWarps - 1) / kScatterWarps), dim3(kScatterWarps * 32), 0, s,
+                     true, static_cast<const uint4*>(a.h), ids, pairs, a.K, a.E, chunks, offset, fill, slot_row,
+                     static_cast<uint4*>(x_perm));
   if (ce != cudaSuccess) return ce;
   // experts' gate/up projections + SiluAndMul over the permuted rows
   GemmArgs g1{};
