@@ -1139,20 +1139,23 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
     p.n_out = a.N;
   }
   p.tiles = p.tiles_m * p.tiles_n;
+  p.group_tiles = static_cast<const int4*>(a.group_tiles);
+  p.group_count = a.group_count;
+  const bool grouped = a.group_tiles != nullptr;
   // Raster: 24 M-tiles per group, so the 152 concurrent tiles cover 24
   // activation panels x ~6 weight panels, and weight loads are marked
   // evict-first so the activation panels of the group stay in L2 while the
   // weights stream past (measured on the 70B gate_up GEMM: 1.48 -> 1.73
   // PFLOP/s at 4128 rows, 1.48 -> 1.68 at 32768 rows, against 16-tile groups
   // with normal eviction).
-  p.b_evict_first = 1;
+  // Grouped mode: an expert's weight tiles are shared by the tiles of its
+  // other row blocks, running at about the same time, so they keep the normal
+  // policy (MoE block at 4096 tokens: 0.448 -> 0.423 ms).
+  p.b_evict_first = grouped ? 0 : 1;
   p.group_m = p.tiles_m < 24 ? p.tiles_m : 24;
   const int sms = num_sms();
   // At most sms / 2 tiles: split K over clusters of S CTAs (S as large as the
   // SMs allow, at least two k-blocks per CTA, all clusters resident at once).
-  p.group_tiles = static_cast<const int4*>(a.group_tiles);
-  p.group_count = a.group_count;
-  const bool grouped = a.group_tiles != nullptr;
   if (grouped && a.group_count == nullptr) return cudaErrorInvalidValue;
   int cluster = 0;
   if (!grouped && (a.force_mode == -1 || a.force_mode == 2) && p.tiles * 2 <= sms) {
