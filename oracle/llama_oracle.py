@@ -56,6 +56,9 @@ Parity status of each function:
   relabelling invariance, weights summing to one, brute-force top-k);
   R26..R29 are readings of pages that name the steps without their
   precision.
+* moe_decoder_layer: the decoder layer with the sparse MoE block in place of
+  the dense MLP; pinned by its reduction to decoder_layer (one expert, k = 1,
+  the dense MLP's weights), bit for bit.
 * decoder_layer / stack_forward: compositions of the pinned parts, cross-checked
   against the unfused form and brute force; no value on the pages fixes an
   end-to-end number, so end-to-end parity beyond composition is unpinned.
@@ -668,6 +671,32 @@ def moe_block(h, w_router, w13, w2, top_k: int, dtype=np.float64, bf16_tensors=T
         ys = [moe_expert(h[t:t + 1], w13[e], w2[e], dtype, bf16_tensors)[0] for e in ids[t]]
         out[t] = moe_combine(ys, wts[t], dtype)
     return store(out, bf16_tensors, dtype), ids, wts, gap
+
+
+def moe_decoder_layer(shape: LayerShape, w: LayerWeights, w_router, w13, w2, top_k: int, batch: Batch, hidden,
+                      residual, k_cache_bits, v_cache_bits, rows=None, dtype=np.float64, bf16_tensors=True):
+    """A Qwen3-MoE decoder layer as the pages describe it: the Llama layer's
+    input_layernorm, attention and post_attention_layernorm, then the sparse
+    MoE block ([LLAMA-70B] Qwen3MoeSparseMoeBlock, decoder_sparse_step 1 and
+    no mlp_only_layers: every layer is sparse) where the dense MLP was.  The
+    pages describe no other difference (R30).  ``w`` supplies ln1, w_qkv, w_o
+    and ln2; its MLP weights are unused.  Returns (hidden, residual, expert
+    ids, top-k gap) on ``rows`` (all rows if None)."""
+    h, r = fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype, bf16_tensors)
+    y = attention_block(shape, w, batch, h, k_cache_bits, v_cache_bits, rows=rows, dtype=dtype,
+                        bf16_tensors=bf16_tensors)
+    sel = np.arange(h.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    h2, r2 = fused_add_rms_norm(y[sel], r[sel], w.ln2, shape.rms_eps, dtype, bf16_tensors)
+    out = np.zeros_like(r)
+    res = np.zeros_like(r)
+    moe_out, ids, _, gap = moe_block(h2, w_router, w13, w2, top_k, dtype, bf16_tensors)
+    out[sel] = moe_out
+    res[sel] = r2
+    ids_all = np.full((h.shape[0], top_k), -1, dtype=np.int64)
+    gap_all = np.full(h.shape[0], np.nan)
+    ids_all[sel] = ids
+    gap_all[sel] = gap
+    return out, res, ids_all, gap_all
 
 
 def stack_forward(shape: LayerShape, layers: Sequence[LayerWeights], final_norm, lm_head, batch: Batch,

@@ -101,6 +101,49 @@ def test_block_equals_the_per_token_sum_over_its_experts():
         assert np.max(np.abs(out[t] - acc)) < 1e-10
 
 
+def _moe_layer_case(seed=51, residual=True):
+    from tests.test_oracle_pins import _paged_setup, tiny_shape, tiny_weights
+    sh = tiny_shape()
+    rng = np.random.default_rng(seed)
+    w = tiny_weights(sh, rng)
+    s = _paged_setup([6, 0, 3], [1, 7, 4], sh.n_kv_heads, sh.head_dim, bs=sh.block_size, seed=13)
+    batch = O.Batch(s["positions"], s["qsl"], s["seq_lens"], s["block_table"])
+    T = int(s["qsl"][-1])
+    x = O.round_to_bf16(rng.standard_normal((T, sh.hidden)))
+    res = O.round_to_bf16(rng.standard_normal((T, sh.hidden))) if residual else None
+    return sh, w, s, batch, x, res
+
+
+def test_moe_layer_with_one_expert_is_the_dense_layer():
+    """The Qwen3-MoE layer with a single expert, k = 1 and the dense MLP's
+    weights as that expert is the Llama layer, bit for bit (the routing weight
+    is exactly 1), with the module outputs stored in bf16."""
+    for residual in (True, False):
+        sh, w, s, batch, x, res = _moe_layer_case(residual=residual)
+        kc1, vc1 = s["k"].copy(), s["v"].copy()
+        want, want_r = O.decoder_layer(sh, w, batch, x, res, kc1, vc1)
+        kc2, vc2 = s["k"].copy(), s["v"].copy()
+        wr = np.ones((1, sh.hidden))
+        got, got_r, ids, _ = O.moe_decoder_layer(sh, w, wr, w.w_gate_up[None], w.w_down[None], 1, batch, x, res,
+                                                 kc2, vc2)
+        assert np.all(ids == 0)
+        assert np.array_equal(got, want) and np.array_equal(got_r, want_r)
+        assert np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2)
+
+
+def test_moe_layer_rows_subset_matches_the_full_layer():
+    sh, w, s, batch, x, res = _moe_layer_case(seed=52)
+    rng = np.random.default_rng(5)
+    E, I = 6, 20
+    w13, w2 = _experts(rng, E, sh.hidden, I)
+    wr = rng.normal(size=(E, sh.hidden))
+    full = O.moe_decoder_layer(sh, w, wr, w13, w2, 2, batch, x, res, s["k"].copy(), s["v"].copy())
+    rows = [0, 5, 11]
+    part = O.moe_decoder_layer(sh, w, wr, w13, w2, 2, batch, x, res, s["k"].copy(), s["v"].copy(), rows=rows)
+    assert np.array_equal(part[0][rows], full[0][rows]) and np.array_equal(part[1][rows], full[1][rows])
+    assert np.array_equal(part[2][rows], full[2][rows])
+
+
 # ----------------------------------------------------------- planted mistakes
 
 def _route_not_renormalised(router_logits, top_k):
@@ -131,16 +174,29 @@ def _expert_gate_up_swapped(x, w13_e, w2_e, dtype=np.float64, bf16_tensors=True)
 
 PINS = [test_page_worked_combine_example, test_single_expert_is_the_dense_mlp,
         test_routing_weights_are_the_softmax_of_the_selected_logits, test_ties_go_to_the_lower_expert_index,
-        test_relabelling_the_experts_changes_nothing, test_block_equals_the_per_token_sum_over_its_experts]
+        test_relabelling_the_experts_changes_nothing, test_block_equals_the_per_token_sum_over_its_experts,
+        test_moe_layer_with_one_expert_is_the_dense_layer]
 
 
 import pytest  # noqa: E402
 
 
+def _layer_moe_on_first_norm(shape, w, w_router, w13, w2, top_k, batch, hidden, residual, k_cache_bits,
+                             v_cache_bits, rows=None, dtype=np.float64, bf16_tensors=True):
+    # the MoE block fed from the input norm instead of the post-attention norm
+    h, r = O.fused_add_rms_norm(hidden, residual, w.ln1, shape.rms_eps, dtype, bf16_tensors)
+    y = O.attention_block(shape, w, batch, h, k_cache_bits, v_cache_bits, dtype=dtype, bf16_tensors=bf16_tensors)
+    _, r2 = O.fused_add_rms_norm(y, r, w.ln2, shape.rms_eps, dtype, bf16_tensors)
+    out, ids, _, gap = O.moe_block(h, w_router, w13, w2, top_k, dtype, bf16_tensors)
+    return out, r2, ids, gap
+
+
 @pytest.mark.parametrize("name,mutant", [("moe_route", _route_not_renormalised), ("moe_route", _route_ties_high),
                                          ("moe_combine", _combine_unweighted),
-                                         ("moe_expert", _expert_gate_up_swapped)],
-                         ids=["not_renormalised", "ties_high", "combine_unweighted", "gate_up_swapped"])
+                                         ("moe_expert", _expert_gate_up_swapped),
+                                         ("moe_decoder_layer", _layer_moe_on_first_norm)],
+                         ids=["not_renormalised", "ties_high", "combine_unweighted", "gate_up_swapped",
+                              "layer_moe_on_first_norm"])
 def test_planted_moe_mistake_is_caught(monkeypatch, name, mutant):
     monkeypatch.setattr(O, name, mutant)
     failed = 0
