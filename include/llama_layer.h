@@ -301,6 +301,37 @@ int llama_moe_forward(const LlamaMoeConfig* cfg, const void* h, int num_tokens, 
                       const void* w2, void* out, int32_t* out_expert_ids, float* out_expert_weights, void* workspace,
                       size_t workspace_bytes, llama_stream_t stream);
 
+/* Weights of one Qwen3-MoE decoder layer: the attention half of a Llama
+ * layer (same layouts as LlamaLayerWeights) and the MoE block's weights
+ * (same layouts as llama_moe_forward). */
+typedef struct {
+  const void* ln1_w;
+  const void* w_qkv;
+  const void* w_o;
+  const void* ln2_w;
+  const void* w_router;  /* [num_experts, hidden] */
+  const void* w13;       /* [num_experts, 2*moe_intermediate, hidden] */
+  const void* w2;        /* [num_experts, hidden, moe_intermediate] */
+} LlamaMoeLayerWeights;
+
+/* Workspace bytes of llama_moe_layer_forward (0 for an invalid config or a
+ * moe->hidden different from cfg->hidden). */
+size_t llama_moe_layer_workspace_size(const LlamaLayerConfig* cfg, const LlamaMoeConfig* moe, int max_tokens,
+                                      int max_seqs, int max_seq_len);
+
+/* One Qwen3-MoE decoder layer ([LLAMA-70B] Qwen3MoeForCausalLM config and
+ * Qwen3MoeSparseMoeBlock; decoder_sparse_step 1, no mlp_only_layers): the
+ * steps of llama_layer_forward up to and including the post-attention fused
+ * add+RMSNorm, then out = the sparse MoE block of llama_moe_forward applied
+ * to h2 in place of the dense MLP.  cfg->intermediate is not used.  Arguments
+ * and in-place rules as llama_layer_forward; out_expert_ids [num_tokens,
+ * top_k] int32 (or NULL) receives each token's chosen experts. */
+int llama_moe_layer_forward(const LlamaLayerConfig* cfg, const LlamaMoeConfig* moe,
+                            const LlamaMoeLayerWeights* weights, const LlamaBatch* batch, void* hidden_states,
+                            const void* residual_in, void* residual_out, void* k_cache, void* v_cache,
+                            int32_t* out_expert_ids, void* workspace, size_t workspace_bytes,
+                            llama_stream_t stream);
+
 /* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
  * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.
  * *detail (may be NULL) receives the code of the first place that reported. */

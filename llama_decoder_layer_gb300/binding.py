@@ -52,6 +52,12 @@ class LlamaMoeConfig(ctypes.Structure):
                 ("moe_intermediate", ctypes.c_int)]
 
 
+class LlamaMoeLayerWeights(ctypes.Structure):
+    _fields_ = [("ln1_w", ctypes.c_void_p), ("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("ln2_w", ctypes.c_void_p), ("w_router", ctypes.c_void_p), ("w13", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p)]
+
+
 class LlamaBatch(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_query_len", ctypes.c_int), ("max_seq_len", ctypes.c_int),
@@ -82,6 +88,9 @@ SIGNATURES = {
     "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
     "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "llama_moe_layer_workspace_size": (_SZ, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), _I, _I, _I]),
+    "llama_moe_layer_forward": (_I, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), ctypes.POINTER(LlamaMoeLayerWeights),
+                                     _P_B, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
 }
 
 _lib = None
@@ -320,6 +329,36 @@ def moe_forward(h: torch.Tensor, w_router: torch.Tensor, w13: torch.Tensor, w2: 
                                  _ptr(out), _ptr(out_ids), _ptr(out_weights), _ptr(workspace), workspace.numel(),
                                  _stream(stream))
     _check(st, "llama_moe_forward")
+
+
+def moe_layer_workspace_size(cfg: LayerConfig, num_experts: int, top_k: int, moe_intermediate: int,
+                             max_tokens: int, max_seqs: int, max_seq_len: int) -> int:
+    c = cfg.c()
+    m = LlamaMoeConfig(c.hidden, num_experts, top_k, moe_intermediate)
+    n = lib().llama_moe_layer_workspace_size(ctypes.byref(c), ctypes.byref(m), max_tokens, max_seqs, max_seq_len)
+    if n == 0:
+        raise LlamaError(LLAMA_ERR_ARG, "llama_moe_layer_workspace_size")
+    return int(n)
+
+
+def moe_layer_forward(cfg: LayerConfig, weights: dict, top_k: int, batch: Batch, hidden: torch.Tensor,
+                      residual_in: Optional[torch.Tensor], residual_out: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, workspace: torch.Tensor, out_ids: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
+    """One Qwen3-MoE decoder layer; weights holds ln1, w_qkv, w_o, ln2 (as
+    layer_forward) and w_router [E, H], w13 [E, 2I, H], w2 [E, H, I]; see
+    llama_moe_layer_forward in the header."""
+    c, b = cfg.c(), batch.c()
+    E, H = weights["w_router"].shape
+    m = LlamaMoeConfig(H, E, top_k, int(weights["w2"].shape[2]))
+    w = LlamaMoeLayerWeights(_ptr(weights["ln1"]), _ptr(weights["w_qkv"]), _ptr(weights["w_o"]),
+                             _ptr(weights["ln2"]), _ptr(weights["w_router"]), _ptr(weights["w13"]),
+                             _ptr(weights["w2"]))
+    st = lib().llama_moe_layer_forward(ctypes.byref(c), ctypes.byref(m), ctypes.byref(w), ctypes.byref(b),
+                                       _ptr(hidden), _ptr(residual_in), _ptr(residual_out), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(out_ids), _ptr(workspace), workspace.numel(),
+                                       _stream(stream))
+    _check(st, "llama_moe_layer_forward")
 
 
 def launch_count() -> int:

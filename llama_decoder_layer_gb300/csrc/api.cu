@@ -182,9 +182,18 @@ AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q
 // The kernels of one layer, in order.  chain: the first kernel may overlap the
 // kernel before it on the stream (one of this library's, inside a stack call);
 // every later kernel overlaps its predecessor in the layer.
+// The MLP of a Qwen3-MoE layer: the sparse block's config, weights and
+// workspace, and where the chosen experts go (or null).
+struct MoeMlp {
+  const LlamaMoeConfig* cfg;
+  const void *w_router, *w13, *w2;
+  uint8_t* ws;
+  int32_t* out_ids;
+};
+
 int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const LlamaBatch& b, void* hidden,
                const void* res_in, void* res_out, void* kc, void* vc, uint8_t* ws, const Layout& L, bool chain,
-               cudaStream_t s) {
+               cudaStream_t s, const MoeMlp* moe = nullptr) {
   const int T = b.num_tokens;
   if (T == 0) return LLAMA_OK;
   int* err = device_error_word();
@@ -254,6 +263,24 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
   e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, true, s);
   if (e) return cuda_status(e);
+  if (moe != nullptr) {  // the sparse MoE block in place of the dense MLP
+    MoeArgs m{};
+    m.h = h;
+    m.w_router = moe->w_router;
+    m.w13 = moe->w13;
+    m.w2 = moe->w2;
+    m.out = hidden;
+    m.out_ids = moe->out_ids;
+    m.T = T;
+    m.H = H;
+    m.E = moe->cfg->num_experts;
+    m.K = moe->cfg->top_k;
+    m.I = moe->cfg->moe_intermediate;
+    m.ws = moe->ws;
+    m.err = err;
+    m.chain = true;
+    return cuda_status(moe_launch(m, s));
+  }
   // gate_up_proj + SiluAndMul
   e = gemm_launch(gemm(kEpiSwiGlu, h, w.w_gate_up, 2 * I, H, a, I), s);
   if (e) return cuda_status(e);
@@ -530,6 +557,55 @@ int llama_moe_forward(const LlamaMoeConfig* cfg, const void* h, int num_tokens, 
   a.ws = ws_base(workspace);
   a.err = device_error_word();
   return cuda_status(moe_launch(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t llama_moe_layer_workspace_size(const LlamaLayerConfig* cfg, const LlamaMoeConfig* moe, int max_tokens,
+                                      int max_seqs, int max_seq_len) {
+  if (check_cfg(cfg) != LLAMA_OK || check_moe_cfg(moe) != LLAMA_OK || moe->hidden != cfg->hidden) return 0;
+  if (max_tokens < 0 || max_seqs < 0) return 0;
+  const size_t layer = align256(make_layout(*cfg, max_tokens, max_seqs, max_seq_len, 0).total);
+  return layer + moe_layout(max_tokens, moe->hidden, moe->num_experts, moe->top_k, moe->moe_intermediate, num_sms())
+                     .total;
+}
+
+int llama_moe_layer_forward(const LlamaLayerConfig* cfg, const LlamaMoeConfig* moe,
+                            const LlamaMoeLayerWeights* weights, const LlamaBatch* batch, void* hidden_states,
+                            const void* residual_in, void* residual_out, void* k_cache, void* v_cache,
+                            int32_t* out_expert_ids, void* workspace, size_t workspace_bytes,
+                            llama_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st) return st;
+  if ((st = check_moe_cfg(moe))) return st;
+  if (moe->hidden != cfg->hidden || weights == nullptr) return LLAMA_ERR_ARG;
+  const void* ps[7] = {weights->ln1_w, weights->w_qkv, weights->w_o, weights->ln2_w,
+                       weights->w_router, weights->w13, weights->w2};
+  for (const void* p : ps) {
+    if (p == nullptr) return LLAMA_ERR_ARG;
+    if (!a16(p)) return LLAMA_ERR_UNSUPPORTED;
+  }
+  if ((st = check_batch(batch, cfg))) return st;
+  if (batch->num_tokens == 0) return LLAMA_OK;
+  if (!hidden_states || !residual_out || !k_cache || !v_cache) return LLAMA_ERR_ARG;
+  if (residual_out == hidden_states) return LLAMA_ERR_ARG;
+  if (!a16(hidden_states) || !a16(residual_out) || !a16(k_cache) || !a16(v_cache) ||
+      (residual_in && !a16(residual_in)))
+    return LLAMA_ERR_UNSUPPORTED;
+  const int T = batch->num_tokens;
+  if (static_cast<long long>(T) * moe->top_k > 0x7fffffffLL) return LLAMA_ERR_UNSUPPORTED;
+  const Layout L = make_layout(*cfg, T, batch->num_seqs, batch->max_seq_len, 0);
+  const MoeLayout ML = moe_layout(T, moe->hidden, moe->num_experts, moe->top_k, moe->moe_intermediate, num_sms());
+  if (ML.rows > 0x7fffffffULL) return LLAMA_ERR_UNSUPPORTED;
+  const size_t layer_bytes = align256(L.total);
+  if (workspace == nullptr || workspace_bytes < layer_bytes + ML.total) return LLAMA_ERR_WORKSPACE;
+  uint8_t* base = ws_base(workspace);
+  LlamaLayerWeights w{};
+  w.ln1_w = weights->ln1_w;
+  w.w_qkv = weights->w_qkv;
+  w.w_o = weights->w_o;
+  w.ln2_w = weights->ln2_w;
+  MoeMlp mm{moe, weights->w_router, weights->w13, weights->w2, base + layer_bytes, out_expert_ids};
+  return layer_impl(*cfg, w, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache, base, L, false,
+                    reinterpret_cast<cudaStream_t>(stream), &mm);
 }
 
 int llama_get_device_error(llama_stream_t stream, int* detail) {

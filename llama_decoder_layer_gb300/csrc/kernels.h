@@ -126,6 +126,7 @@ struct MoeArgs {
   int T, H, E, K, I;
   uint8_t* ws;           // 256-aligned, moe_layout(...).total - 256 bytes
   int* err;
+  bool chain;            // the first kernel may overlap the kernel before it (one of this library's)
 };
 int moe_launch(const MoeArgs& a, cudaStream_t s);
 

@@ -328,7 +328,7 @@ int moe_launch(const MoeArgs& a, cudaStream_t s) {
   g.partials_bytes = L.gpart_bytes;
   g.err = a.err;
   g.force_mode = -1;
-  g.pdl = 0;
+  g.pdl = a.chain ? 1 : 0;
   int e = gemm_launch(g, s);
   if (e) return e;
   const int per_lane = (a.E + 31) / 32;

@@ -87,10 +87,23 @@ SPECS = {
     "decode_70b_80l": Spec("decode_70b_80l", 8192, 64, 8, 128, 28672, 1e-5, 500000.0, LLAMA3_SCALING,
                            groups=(("decode", 64, 1, 512, 4096),), residual_none=True, num_layers=80,
                            vocab=128256),
+    # Qwen3-30B-A3B (Qwen3MoeForCausalLM config): hidden 2048, 32 q heads, 4 KV
+    # heads, head_dim 128, rms_eps 1e-6, rope_theta 1e7 without scaling,
+    # 128 experts, top-8, moe_intermediate 768 (intermediate_size 6144 is the
+    # dense size, unused: every layer is sparse)
+    "qwen3_moe": Spec("qwen3_moe", 2048, 32, 4, 128, 6144, 1e-6, 10000000.0, None,
+                      groups=(("decode", 16, 1, 512, 4096), ("prefill", 1, 256, 0, 0)),
+                      extra={"num_experts": 128, "top_k": 8, "moe_intermediate": 768}),
+    "qwen3_moe_decode": Spec("qwen3_moe_decode", 2048, 32, 4, 128, 6144, 1e-6, 10000000.0, None,
+                             groups=(("decode", 64, 1, 512, 4096),),
+                             extra={"num_experts": 128, "top_k": 8, "moe_intermediate": 768}),
+    "qwen3_moe_prefill": Spec("qwen3_moe_prefill", 2048, 32, 4, 128, 6144, 1e-6, 10000000.0, None,
+                              groups=(("prefill", 4, 2048, 0, 0),),
+                              extra={"num_experts": 128, "top_k": 8, "moe_intermediate": 768}),
 }
 
 # seed offsets per tensor kind
-_OFF = {"ln1": 1, "w_qkv": 2, "w_o": 3, "ln2": 4, "w_gate_up": 5, "w_down": 6,
+_OFF = {"ln1": 1, "w_qkv": 2, "w_o": 3, "ln2": 4, "w_gate_up": 5, "w_down": 6, "w_router": 7, "w13": 8, "w2": 9,
         "hidden": 20, "residual": 21, "k_cache": 22, "v_cache": 23, "ctx": 24, "perm": 25,
         "embed": 30, "ids": 31, "lm_head": 32, "final_norm": 33}
 
@@ -125,6 +138,26 @@ def make_layer_weights(spec: Spec, seed: int = 0, layer: int = 0, device="cpu") 
         "ln2": normal_bf16((H,), 0.02, gmean, base + _OFF["ln2"], device),
         "w_gate_up": normal_bf16((2 * spec.intermediate, H), 0.02, 0.0, base + _OFF["w_gate_up"], device),
         "w_down": normal_bf16((H, spec.intermediate), 0.02, 0.0, base + _OFF["w_down"], device),
+    }
+
+
+def make_moe_layer_weights(spec: Spec, seed: int = 0, layer: int = 0, device="cpu") -> dict:
+    """bf16 weights of one Qwen3-MoE layer: the attention half of
+    make_layer_weights plus w_router [E, H], w13 [E, 2I, H] (gate rows then
+    up rows per expert) and w2 [E, H, I], all N(0, 0.02)."""
+    base = seed * 1000003 + layer * 101
+    H, d = spec.hidden, spec.head_dim
+    E, Im = spec.extra["num_experts"], spec.extra["moe_intermediate"]
+    nqkv = (spec.n_heads + 2 * spec.n_kv_heads) * d
+    gmean = 0.0 if spec.literal_gamma else 1.0
+    return {
+        "ln1": normal_bf16((H,), 0.02, gmean, base + _OFF["ln1"], device),
+        "w_qkv": normal_bf16((nqkv, H), 0.02, 0.0, base + _OFF["w_qkv"], device),
+        "w_o": normal_bf16((H, spec.n_heads * d), 0.02, 0.0, base + _OFF["w_o"], device),
+        "ln2": normal_bf16((H,), 0.02, gmean, base + _OFF["ln2"], device),
+        "w_router": normal_bf16((E, H), 0.02, 0.0, base + _OFF["w_router"], device),
+        "w13": normal_bf16((E, 2 * Im, H), 0.02, 0.0, base + _OFF["w13"], device),
+        "w2": normal_bf16((E, H, Im), 0.02, 0.0, base + _OFF["w2"], device),
     }
 
 

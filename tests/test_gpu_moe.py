@@ -85,3 +85,48 @@ def test_moe_routing_concentrated_on_few_experts():
     ref, _, _, _ = O.moe_block(_f64(h), _f64(wr), _f64(w13), _f64(w2), K)
     got = out.float().cpu().numpy()
     assert np.max(np.abs(got - ref)) <= 2e-2 * np.max(np.abs(ref))
+
+
+def test_qwen3_moe_layer_matches_the_oracle():
+    """One Qwen3-30B-A3B-shaped MoE decoder layer (16 decode sequences, contexts
+    U[512, 4096], plus a 256-token prefill chunk): residual and cache writes
+    on every row, expert choice and hidden output on the rows whose routing
+    is unambiguous (oracle top-k gap > 1e-2; the GPU routes on its own bf16
+    h2, which may differ from the oracle's by an ulp in some elements)."""
+    from tests.helpers import SubBatch, assert_close, bits, f32, oracle_shape
+
+    spec = I.SPECS["qwen3_moe"]
+    seed = 3
+    bl = I.make_batch(spec, seed, DEV)
+    w = I.make_moe_layer_weights(spec, seed, 0, DEV)
+    x, r = I.make_activations(spec, bl.num_tokens, seed, DEV)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, DEV)
+    sub = SubBatch(bl, range(bl.num_seqs), kc, vc)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    K = spec.extra["top_k"]
+    T = bl.num_tokens
+    ws = lb.alloc_workspace(lb.moe_layer_workspace_size(cfg, spec.extra["num_experts"], K,
+                                                        spec.extra["moe_intermediate"], T, bl.num_seqs,
+                                                        batch.max_seq_len), DEV)
+    hid = x.clone()
+    res = torch.empty_like(x)
+    ids = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    lb.moe_layer_forward(cfg, w, K, batch, hid, r, res, kc, vc, ws, ids)
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
+
+    ow = O.LayerWeights(f32(w["ln1"]), f32(w["w_qkv"]), f32(w["w_o"]), f32(w["ln2"]), None, None)
+    kref, vref = sub.kc.copy(), sub.vc.copy()
+    out, res_ref, ref_ids, gap = O.moe_decoder_layer(oracle_shape(spec), ow, f32(w["w_router"]), f32(w["w13"]),
+                                                     f32(w["w2"]), K, sub.batch, f32(x), f32(r), kref, vref)
+    assert_close(f32(res), res_ref, "qwen3 moe residual")
+    assert_close(O.bf16_bits_to_float(sub.gpu_written(bits(kc))), O.bf16_bits_to_float(sub.oracle_written(kref)),
+                 "qwen3 moe k written")
+    assert_close(O.bf16_bits_to_float(sub.gpu_written(bits(vc))), O.bf16_bits_to_float(sub.oracle_written(vref)),
+                 "qwen3 moe v written")
+    sure = gap > 1e-2
+    assert sure.sum() >= int(0.75 * T), sure.sum()  # 85% of these rows on the CPU reference
+    assert np.array_equal(ids.cpu().numpy()[sure], ref_ids[sure])
+    e = assert_close(f32(hid)[sure], out[sure], "qwen3 moe hidden")
+    print(f"qwen3 moe layer: {int(sure.sum())}/{T} rows with unambiguous routing, rel err hidden {e:.2e}")
