@@ -779,6 +779,73 @@ def run_moe(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_moe_layer(args, world, rank, local):
+    """One Qwen3-30B-A3B MoE decoder layer (llama_moe_layer_forward) per step:
+    qwen3_moe_decode = 64 decode sequences, contexts U[512, 4096];
+    qwen3_moe_prefill = 4 prefill sequences x 2048 tokens."""
+    import dataclasses
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    from llama_decoder_layer_gb300 import inputs as I
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    seed = 600 + rank
+    spec = I.SPECS[args.workload]
+    E, K, Im = spec.extra["num_experts"], spec.extra["top_k"], spec.extra["moe_intermediate"]
+    bl = I.make_batch(spec, seed, dev)
+    w = I.make_moe_layer_weights(spec, seed, 0, dev)
+    x, r = I.make_activations(spec, bl.num_tokens, seed, dev)
+    kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, dev)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T = bl.num_tokens
+    ws = lb.alloc_workspace(lb.moe_layer_workspace_size(cfg, E, K, Im, T, bl.num_seqs, batch.max_seq_len), dev)
+    hid = x.clone()
+    res = torch.empty_like(x)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    lb.moe_layer_forward(cfg, w, K, batch, hid, r, res, kc, vc, ws, ids)
+    torch.cuda.synchronize()
+    touched = int(torch.unique(ids).numel())
+
+    def step():  # as the dense single-layer workloads: each step's input is the previous step's output
+        lb.moe_layer_forward(cfg, w, K, batch, hid, r, res, kc, vc, ws)
+
+    sampler = ClockSampler(local)
+    ms, clocks = time_steps(step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
+    st, detail = lb.get_device_error()
+    if st != lb.LLAMA_OK:
+        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+    H = spec.hidden
+    alg = layer_algorithmic(dataclasses.replace(spec, intermediate=0), bl)  # norms, attention, o_proj
+    moe_bytes = (E * H + touched * 3 * Im * H) * 2
+    nbytes = alg["bytes"] + moe_bytes
+    flops = alg["flops"] + 2 * T * (E * H + K * 3 * Im * H)
+    if nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops_sustained"] * 1e12):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes": nbytes, "experts_touched": touched, "traffic": None}
+    else:
+        tf = flops / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": f"bf16_tflops_sustained ({peak_src})", "algorithmic_flops": flops, "traffic": None}
+    line = {
+        "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
+        "value": round(T * world / (ms / 1e3), 1), "unit": "tokens/s per Qwen3-MoE layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": f"{args.workload}: one Qwen3-30B-A3B MoE decoder layer (hidden 2048, 32/4 heads, "
+                               f"128 experts, top-8, moe_intermediate 768), {T} tokens in {bl.num_seqs} sequences",
+                   "tokens_per_step": T, "layers": 1},
+        "roofline": roof, "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     """Times the CPU oracle (fp32) on a bounded sample of the stack workload:
     each step runs one decode sequence through all layers + head."""
@@ -828,13 +895,14 @@ def main():
     ap.add_argument("--workload", default="stack_70b",
                     choices=["stack_70b", "decode_70b", "prefill_70b", "decode_8b", "tiny", "gemm_gate_up",
                              "attn_prefill", "attn_decode", "decode_70b_80l", "sample", "moe_decode",
-                             "moe_prefill"],
+                             "moe_prefill", "qwen3_moe_decode", "qwen3_moe_prefill"],
                     help="stack_70b (default), one single-layer workload, or gemm_gate_up: the stack's "
                          "dominant kernel alone (4128 x 57344 x 8192, for profiling); attn_prefill / "
                          "attn_decode: the paged attention of the 70B prefill / decode batch alone; "
                          "decode_70b_80l: the full-depth 70B decode step (~193 GB on the device); sample: "
                          "llama_sample on the stack's 34 x 128256 head; moe_decode / moe_prefill: the "
-                         "Qwen3-30B-A3B MoE block over 64 / 4096 tokens")
+                         "Qwen3-30B-A3B MoE block over 64 / 4096 tokens; qwen3_moe_decode / qwen3_moe_prefill: "
+                         "one Qwen3-30B-A3B MoE decoder layer, 64 decode sequences / 4 x 2048 prefill")
     ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -850,6 +918,8 @@ def main():
         run_sampler(args, world, rank, local)
     elif args.workload in ("moe_decode", "moe_prefill"):
         run_moe(args, world, rank, local)
+    elif args.workload in ("qwen3_moe_decode", "qwen3_moe_prefill"):
+        run_moe_layer(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

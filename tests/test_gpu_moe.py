@@ -90,9 +90,10 @@ def test_moe_routing_concentrated_on_few_experts():
 def test_qwen3_moe_layer_matches_the_oracle():
     """One Qwen3-30B-A3B-shaped MoE decoder layer (16 decode sequences, contexts
     U[512, 4096], plus a 256-token prefill chunk): residual and cache writes
-    on every row, expert choice and hidden output on the rows whose routing
-    is unambiguous (oracle top-k gap > 1e-2; the GPU routes on its own bf16
-    h2, which may differ from the oracle's by an ulp in some elements)."""
+    on every row, the chosen expert set and hidden output on the rows whose
+    routing is unambiguous (oracle top-k gap > 1e-2; the GPU routes on its
+    own bf16 h2, which may differ from the oracle's by an ulp in some
+    elements)."""
     from tests.helpers import SubBatch, assert_close, bits, f32, oracle_shape
 
     spec = I.SPECS["qwen3_moe"]
@@ -127,6 +128,10 @@ def test_qwen3_moe_layer_matches_the_oracle():
                  "qwen3 moe v written")
     sure = gap > 1e-2
     assert sure.sum() >= int(0.75 * T), sure.sum()  # 85% of these rows on the CPU reference
-    assert np.array_equal(ids.cpu().numpy()[sure], ref_ids[sure])
+    # the chosen set is fixed by the 8th/9th gap; the order inside it is not
+    # (two selected logits may lie closer than the GPU's ulp-level input shift)
+    got_sets = np.sort(ids.cpu().numpy()[sure], axis=1)
+    assert np.array_equal(got_sets, np.sort(ref_ids[sure], axis=1)), \
+        int(np.sum(np.any(got_sets != np.sort(ref_ids[sure], axis=1), axis=1)))
     e = assert_close(f32(hid)[sure], out[sure], "qwen3 moe hidden")
     print(f"qwen3 moe layer: {int(sure.sum())}/{T} rows with unambiguous routing, rel err hidden {e:.2e}")
