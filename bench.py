@@ -156,10 +156,12 @@ class Workload:
     """A device-resident workload and its step function."""
 
 
-def setup_stack(lb, I, seed, dev):
+def setup_stack(lb, I, seed, dev, fold=False):
     spec = I.SPECS["stack_70b"]
     bl = I.make_batch(spec, seed, dev)
     layers = [I.make_layer_weights(spec, seed, l, dev) for l in range(spec.num_layers)]
+    if fold:  # norm weights folded into w_qkv / w_gate_up (done once, before timing)
+        layers = [lb.folded_layer_weights(w) for w in layers]
     emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, seed, dev)
     caches = [I.make_kv_cache(spec, bl.num_blocks, seed, l, dev) for l in range(spec.num_layers)]
     cfg = lb.LayerConfig.from_spec(spec)
@@ -186,10 +188,12 @@ def setup_stack(lb, I, seed, dev):
     return W
 
 
-def setup_layer(lb, I, name, seed, dev, weights=None):
+def setup_layer(lb, I, name, seed, dev, weights=None, fold=False):
     spec = I.SPECS[name]
     bl = I.make_batch(spec, seed, dev)
     w = weights if weights is not None else I.make_layer_weights(spec, seed, 0, dev)
+    if fold and w["ln1"] is not None:
+        w = lb.folded_layer_weights(w)
     x, r = I.make_activations(spec, bl.num_tokens, seed, dev)
     kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, dev)
     cfg = lb.LayerConfig.from_spec(spec)
@@ -406,7 +410,7 @@ def run_ours(args, world, rank, local):
         return run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
     if args.workload != "stack_70b":
         return run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
-    W = setup_stack(lb, I, seed, dev)
+    W = setup_stack(lb, I, seed, dev, fold=args.fold_norms)
 
     # main line: the stack step
     sampler = ClockSampler(local)
@@ -442,7 +446,7 @@ def run_ours(args, world, rank, local):
     if not args.no_extra:
         # single-layer 70B decode and prefill (weights of the stack's layer 0; their own batches/caches)
         for name in ("decode_70b", "prefill_70b"):
-            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0])
+            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0], fold=args.fold_norms)
             steps = max(args.steps, 30) if name.startswith("decode") else args.steps
             lms, _ = time_steps(L.step, steps, args.warmup, world)
             alg = layer_algorithmic(L.spec, L.bl)
@@ -481,7 +485,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": "stack_70b: 8 x 70B-shaped layers + final norm + lm_head(128256) + greedy argmax; "
                                "32 decode seqs (ctx U[1024,16384]) + 2 prefill chunks x 2048; 4128 tokens",
                    "tokens_per_step": W.tokens_per_step, "layers": W.layers_n,
-                   "l2": "inputs larger than L2 (13.7 GB of weights per step)", "parallelism": f"replicas x{world}"},
+                   "l2": "inputs larger than L2 (13.7 GB of weights per step)", "parallelism": f"replicas x{world}",
+                   "norms": "folded into w_qkv / w_gate_up" if args.fold_norms else "separate"},
         "stack_tflops_per_s": round(stack_flops / (ms / 1e3) / 1e12, 1),
         "roofline": roofline,
         "clocks": clocks,
@@ -581,7 +586,7 @@ def run_attention(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
 
 def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed):
     """One decoder layer of the named workload per step (residual in, residual out)."""
-    L = setup_layer(lb, I, args.workload, seed, dev)
+    L = setup_layer(lb, I, args.workload, seed, dev, fold=args.fold_norms)
     sampler = ClockSampler(local)
     ms, clocks = time_steps(L.step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
     st, detail = lb.get_device_error()
@@ -596,7 +601,8 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
         "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
         "config": {"workload": args.workload, "tokens_per_step": L.tokens_per_step, "layers": 1,
                    "l2": "inputs larger than L2" if alg["bytes"] > L2_BYTES else "inputs smaller than L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "norms": "folded into w_qkv / w_gate_up" if args.fold_norms else "separate"},
         "roofline": layer_roofline(args.workload, alg, ms, peaks, peak_src),
         "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
     }
@@ -905,6 +911,8 @@ def main():
                          "one Qwen3-30B-A3B MoE decoder layer, 64 decode sequences / 4 x 2048 prefill")
     ap.add_argument("--gemm-tokens", type=int, default=4128, help="rows of the gemm_gate_up workload")
     ap.add_argument("--no-extra", action="store_true", help="skip the single-layer decode/prefill results")
+    ap.add_argument("--fold-norms", action="store_true",
+                    help="run the layers with the RMSNorm weights folded into w_qkv / w_gate_up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -120,6 +120,22 @@ typedef struct {
   const void* w_down;
 } LlamaLayerWeights;
 
+/* Folded norms.  ln1_w and ln2_w may both be NULL when w_qkv and w_gate_up
+ * carry the norm weights in their columns (llama_fold_norm_weights):
+ *   norm(r) W^T = rsqrt(mean(r^2) + eps) * (r (W diag(gamma))^T),
+ * so the norm kernels write only the residual r and each row's rsqrt, and the
+ * qkv and gate_up GEMMs read r and scale their rows by it before their
+ * epilogues (RoPE, SiluAndMul).  The normed activations h are then never
+ * stored; the rounding to bf16 moves from h to the folded weights.  One NULL
+ * and one non-NULL norm weight is LLAMA_ERR_ARG.  (The final norm of
+ * llama_stack_forward is not folded.) */
+
+/* w_folded[o, i] = bf16(w[o, i] * norm_weight[i]) for a weight w [rows, cols]
+ * bf16 (cols a multiple of 8) and a norm weight [cols] bf16; w_folded may
+ * equal w.  Asynchronous on stream. */
+int llama_fold_norm_weights(const void* norm_weight, const void* w, int rows, int cols, void* w_folded,
+                            llama_stream_t stream);
+
 /* One flat batch ([CODE-READING] section 2.1: tokens of many sequences, with
  * their positions).  Sequence b owns tokens [query_start_loc[b],
  * query_start_loc[b+1]).  Its context length seq_lens[b] counts the cached

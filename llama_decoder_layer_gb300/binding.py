@@ -88,6 +88,7 @@ SIGNATURES = {
     "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
     "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "llama_fold_norm_weights": (_I, [_VP, _VP, _I, _I, _VP, _VP]),
     "llama_moe_layer_workspace_size": (_SZ, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), _I, _I, _I]),
     "llama_moe_layer_forward": (_I, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), ctypes.POINTER(LlamaMoeLayerWeights),
                                      _P_B, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -359,6 +360,28 @@ def moe_layer_forward(cfg: LayerConfig, weights: dict, top_k: int, batch: Batch,
                                        _ptr(v_cache), _ptr(out_ids), _ptr(workspace), workspace.numel(),
                                        _stream(stream))
     _check(st, "llama_moe_layer_forward")
+
+
+def fold_norm_weights(norm_weight: torch.Tensor, w: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """bf16(w * norm_weight) column-wise, for a layer whose ln1/ln2 are None
+    (the norm weights folded into w_qkv and w_gate_up)."""
+    rows, cols = w.shape
+    out = torch.empty_like(w) if out is None else out
+    st = lib().llama_fold_norm_weights(_ptr(norm_weight), _ptr(w), rows, cols, _ptr(out), _stream(stream))
+    _check(st, "llama_fold_norm_weights")
+    return out
+
+
+def folded_layer_weights(weights: dict, stream=None) -> dict:
+    """The weights of a folded-norm layer: ln1/ln2 None, gamma folded into
+    w_qkv and w_gate_up."""
+    w = dict(weights)
+    w["w_qkv"] = fold_norm_weights(weights["ln1"], weights["w_qkv"], stream=stream)
+    w["w_gate_up"] = fold_norm_weights(weights["ln2"], weights["w_gate_up"], stream=stream)
+    w["ln1"] = None
+    w["ln2"] = None
+    return w
 
 
 def launch_count() -> int:

@@ -86,7 +86,7 @@ int check_batch(const LlamaBatch* b, const LlamaLayerConfig* c) {
 }
 
 struct Layout {
-  size_t slots, h, q, o, a, gpart, apart, hf, logits, total;
+  size_t slots, rscale, h, q, o, a, gpart, apart, hf, logits, total;
   size_t gpart_bytes, apart_bytes;
 };
 
@@ -96,6 +96,8 @@ Layout make_layout(const LlamaLayerConfig& c, int T, int B, int max_seq_len, int
   const size_t qsz = static_cast<size_t>(c.n_heads) * c.head_dim;
   size_t off = 0;
   L.slots = off;
+  off += align256(t * 4);
+  L.rscale = off;  // per-row rsqrt of a norm folded into the next GEMM
   off += align256(t * 4);
   L.h = off;
   off += align256(t * c.hidden * 2);
@@ -140,10 +142,15 @@ RopeParams rope_of(const LlamaLayerConfig& c) {
 
 int cuda_status(int e) { return e == 0 ? LLAMA_OK : LLAMA_ERR_CUDA; }
 
+// Both norm weights present, or both NULL (folded into w_qkv and w_gate_up).
 int check_weights(const LlamaLayerWeights* w) {
   if (w == nullptr) return LLAMA_ERR_ARG;
+  if ((w->ln1_w == nullptr) != (w->ln2_w == nullptr)) return LLAMA_ERR_ARG;
+  const bool folded = w->ln1_w == nullptr;
   const void* ps[6] = {w->ln1_w, w->w_qkv, w->w_o, w->ln2_w, w->w_gate_up, w->w_down};
-  for (const void* p : ps) {
+  for (int i = 0; i < 6; ++i) {
+    const void* p = ps[i];
+    if (folded && (i == 0 || i == 3)) continue;
     if (p == nullptr) return LLAMA_ERR_ARG;
     if (!a16(p)) return LLAMA_ERR_UNSUPPORTED;
   }
@@ -206,6 +213,11 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   auto a = ws + L.a;
   float* gpart = reinterpret_cast<float*>(ws + L.gpart);
   float* apart = reinterpret_cast<float*>(ws + L.apart);
+  // folded norms: the norm kernels write only r and the row's rsqrt, and the
+  // qkv / gate_up GEMMs read r and scale their rows by it (their weights carry
+  // the norm weights)
+  const bool folded = w.ln1_w == nullptr;
+  float* rscale = folded ? reinterpret_cast<float*>(ws + L.rscale) : nullptr;
   int e;
 
   const int32_t* slot_map = b.slot_mapping;
@@ -217,8 +229,9 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
     chain = true;
   }
   // input_layernorm
-  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, chain, s);
+  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, chain, s, rscale);
   if (e) return cuda_status(e);
+  const void* normed = folded ? res_out : h;  // the A operand of qkv (and, after the second norm, gate_up)
   auto gemm = [&](int epi, const void* A, const void* B, int N, int K, void* out, int ldo) {
     GemmArgs g{};
     g.epi = epi;
@@ -237,7 +250,8 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
     return g;
   };
   // qkv_proj + RoPE + cache update
-  GemmArgs g = gemm(kEpiQkv, h, w.w_qkv, qsz + 2 * kvsz, H, q, qsz);
+  GemmArgs g = gemm(kEpiQkv, normed, w.w_qkv, qsz + 2 * kvsz, H, q, qsz);
+  g.row_scale = rscale;
   g.qkv.q_size = qsz;
   g.qkv.kv_size = kvsz;
   g.qkv.head_dim = c.head_dim;
@@ -261,7 +275,7 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   e = gemm_launch(go, s);
   if (e) return cuda_status(e);
   // post_attention_layernorm: r2 = y + r (in res_out), h2 (in the h buffer)
-  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, true, s);
+  e = add_rmsnorm_launch(h, res_out, res_out, h, w.ln2_w, T, H, c.rms_eps, nullptr, true, s, rscale);
   if (e) return cuda_status(e);
   if (moe != nullptr) {  // the sparse MoE block in place of the dense MLP
     MoeArgs m{};
@@ -282,7 +296,9 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
     return cuda_status(moe_launch(m, s));
   }
   // gate_up_proj + SiluAndMul
-  e = gemm_launch(gemm(kEpiSwiGlu, h, w.w_gate_up, 2 * I, H, a, I), s);
+  GemmArgs gu = gemm(kEpiSwiGlu, normed, w.w_gate_up, 2 * I, H, a, I);
+  gu.row_scale = rscale;
+  e = gemm_launch(gu, s);
   if (e) return cuda_status(e);
   // down_proj -> hidden_states
   e = gemm_launch(gemm(kEpiBf16, a, w.w_down, H, I, hidden, H), s);
@@ -606,6 +622,13 @@ int llama_moe_layer_forward(const LlamaLayerConfig* cfg, const LlamaMoeConfig* m
   MoeMlp mm{moe, weights->w_router, weights->w13, weights->w2, base + layer_bytes, out_expert_ids};
   return layer_impl(*cfg, w, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache, base, L, false,
                     reinterpret_cast<cudaStream_t>(stream), &mm);
+}
+
+int llama_fold_norm_weights(const void* norm_weight, const void* w, int rows, int cols, void* w_folded,
+                            llama_stream_t stream) {
+  if (norm_weight == nullptr || w == nullptr || w_folded == nullptr || rows < 0 || cols <= 0) return LLAMA_ERR_ARG;
+  if (cols % 8 || !a16(norm_weight) || !a16(w) || !a16(w_folded)) return LLAMA_ERR_UNSUPPORTED;
+  return cuda_status(fold_norm_launch(norm_weight, w, rows, cols, w_folded, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_get_device_error(llama_stream_t stream, int* detail) {

@@ -77,6 +77,9 @@ struct GemmParams {
   // the device, {A row, B base row of the tile's expert, N tile, valid rows}
   const int4* group_tiles;
   const int* group_count;
+  // per-row scale of the product before the epilogue (an RMSNorm's rsqrt
+  // with its weights folded into B), or null
+  const float* row_scale;
 };
 
 struct Work {
@@ -453,6 +456,22 @@ struct TmemLoader {
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const { tmem_ld32(taddr + col, v); }
 };
 
+// A loader whose values are multiplied by the row's scale (1 without one).
+template <class Loader>
+struct ScaledLoader {
+  const Loader& ld;
+  float s;
+  __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
+    ld(col, v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] *= s;
+  }
+};
+
+__device__ __forceinline__ float row_scale_of(const GemmParams& p, int row, int m_limit) {
+  return p.row_scale != nullptr && row < m_limit ? p.row_scale[row] : 1.f;
+}
+
 // Partial tiles in the workspace: two slots per CTA (its first work item, and
 // the split tile that ends its range), each [BN / 4][BM] float4, so 32
 // consecutive rows of one 4-column group are 512 contiguous bytes.
@@ -700,7 +719,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       const bool valid = tm * BM + row_in_tile < tc.m_limit;
       if (w.kb0 == 0 && w.kb1 == p.kb) {
-        TmemLoader ld{taddr};
+        TmemLoader tl{taddr};
+        ScaledLoader<TmemLoader> ld{tl, row_scale_of(p, tm * BM + row_in_tile, tc.m_limit)};
         epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab, tc.m_limit);
         tc_fence_before();
         __syncwarp();
@@ -954,7 +974,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int g = 0; g < BM / 32; ++g, ++item) {
         if ((item & 3) != e || tm * BM + g * 32 >= p.M) continue;
         const int row_in_tile = g * 32 + lane;
-        ClusterLoader ld{sbase, S, row_in_tile};
+        ClusterLoader cl{sbase, S, row_in_tile};
+        ScaledLoader<ClusterLoader> ld{cl, row_scale_of(p, tm * BM + row_in_tile, p.M)};
         epilogue_unit<EPI>(p, tm, tn, row_in_tile, u, ld, rope_tab);
       }
     }
@@ -991,7 +1012,8 @@ __global__ void __launch_bounds__(EpiUnits<EPI>::kUnits * 32) k_gemm_fixup(const
   }
   const int unit = threadIdx.x >> 5;
   const int row_in_tile = blockIdx.y * kFixRows + (threadIdx.x & 31);
-  PartialLoader ld{p.partials, p.units, t0, p.grid, c_first, c_last, row_in_tile, tm * BM + row_in_tile < p.M};
+  PartialLoader pl{p.partials, p.units, t0, p.grid, c_first, c_last, row_in_tile, tm * BM + row_in_tile < p.M};
+  ScaledLoader<PartialLoader> ld{pl, row_scale_of(p, tm * BM + row_in_tile, p.M)};
   epilogue_unit<EPI>(p, tm, tn, row_in_tile, unit, ld, rope_tab);
 }
 
@@ -1141,6 +1163,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.tiles = p.tiles_m * p.tiles_n;
   p.group_tiles = static_cast<const int4*>(a.group_tiles);
   p.group_count = a.group_count;
+  p.row_scale = a.row_scale;
   const bool grouped = a.group_tiles != nullptr;
   // Raster: 24 M-tiles per group, so the 152 concurrent tiles cover 24
   // activation panels x ~6 weight panels, and weight loads are marked

@@ -51,6 +51,9 @@ struct GemmArgs {
   const void* group_tiles;
   const int* group_count;
   int b_rows;
+  // [M] fp32: row r of the product is multiplied by row_scale[r] before the
+  // epilogue (an RMSNorm's rsqrt, its weights folded into B); null = 1
+  const float* row_scale;
 };
 
 size_t gemm_partials_bytes(int num_sms);
@@ -58,10 +61,16 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s);  // returns 0 or a CUDA erro
 
 // fused residual add + RMSNorm over rows of length H
 //   r = x (+ res_in); h = r * rsqrt(mean(r^2) + eps) * gamma
+// With gamma null the norm is folded into the next GEMM: h is not written and
+// inv_out[row] receives rsqrt(mean(r^2) + eps).
 // row_index_qsl != nullptr: output row b reads input row qsl[b+1]-1 (last
 // token of sequence b), otherwise row b reads row b.
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma,
-                       int rows, int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s);
+                       int rows, int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s,
+                       float* inv_out = nullptr);
+
+// w_folded[o, i] = bf16(w[o, i] * gamma[i]) for a [rows, cols] weight
+int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void* w_folded, cudaStream_t s);
 
 int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
                         const int32_t* block_table, int T, int B, int max_blocks, int block_size, int num_blocks,

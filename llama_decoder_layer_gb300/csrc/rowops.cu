@@ -48,7 +48,8 @@ template <int MAXC>
 __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __restrict__ x, const uint4* res_in,
                                                               uint4* res_out, uint4* h_out,
                                                               const uint4* __restrict__ gamma, int H, float eps,
-                                                              const int32_t* __restrict__ qsl) {
+                                                              const int32_t* __restrict__ qsl,
+                                                              float* __restrict__ inv_out) {
   __shared__ float red[33];
   pdl_wait();
   const int out_row = blockIdx.x;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __res
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / static_cast<float>(H) + eps);
+  if (inv_out != nullptr && threadIdx.x == 0) inv_out[out_row] = inv;
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
     const int i = threadIdx.x + c * kNormThreads;
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __res
         r.w = pack_bf16x2(v[c][6], v[c][7]);
         res_out[obase + i] = r;
       }
+      if (gamma == nullptr) continue;  // folded: the next GEMM applies inv (and gamma is in its weights)
       const uint4 g = gamma[i];
       uint4 h;
       h.x = pack_bf16x2(v[c][0] * inv * bf16_lo(g.x), v[c][1] * inv * bf16_hi(g.x));
@@ -112,6 +115,22 @@ __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __res
       h.w = pack_bf16x2(v[c][6] * inv * bf16_lo(g.w), v[c][7] * inv * bf16_hi(g.w));
       h_out[obase + i] = h;
     }
+  }
+}
+
+// The norm weights folded into the columns of the projection that follows the
+// norm: w_folded[o, i] = bf16(w[o, i] * gamma[i]) (eight columns per thread).
+__global__ void k_fold_norm(const uint4* __restrict__ gamma, const uint4* __restrict__ w, long long chunks,
+                            int row_chunks, uint4* __restrict__ w_folded) {
+  for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < chunks;
+       c += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 a = w[c], g = gamma[c % row_chunks];
+    uint4 o;
+    o.x = pack_bf16x2(bf16_lo(a.x) * bf16_lo(g.x), bf16_hi(a.x) * bf16_hi(g.x));
+    o.y = pack_bf16x2(bf16_lo(a.y) * bf16_lo(g.y), bf16_hi(a.y) * bf16_hi(g.y));
+    o.z = pack_bf16x2(bf16_lo(a.z) * bf16_lo(g.z), bf16_hi(a.z) * bf16_hi(g.z));
+    o.w = pack_bf16x2(bf16_lo(a.w) * bf16_lo(g.w), bf16_hi(a.w) * bf16_hi(g.w));
+    w_folded[c] = o;
   }
 }
 
@@ -238,7 +257,7 @@ int grid_for(long long work, int threads) {
 }  // namespace
 
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma, int rows,
-                       int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s) {
+                       int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s, float* inv_out) {
   if (rows <= 0) return 0;
   const int nch = H / 8;
   const int per = (nch + kNormThreads - 1) / kNormThreads;
@@ -248,13 +267,22 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
   auto HO = static_cast<uint4*>(h_out);
   auto G = static_cast<const uint4*>(gamma);
   auto go = [&](auto kernel) {
-    return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl);
+    return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl,
+                         inv_out);
   };
   if (per <= 1) return go(k_add_rmsnorm<1>);
   if (per <= 2) return go(k_add_rmsnorm<2>);
   if (per <= 4) return go(k_add_rmsnorm<4>);
   if (per <= 8) return go(k_add_rmsnorm<8>);
   return cudaErrorInvalidValue;
+}
+
+int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void* w_folded, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return 0;
+  const long long chunks = static_cast<long long>(rows) * (cols / 8);
+  return launch_kernel(k_fold_norm, dim3(grid_for(chunks, 256)), dim3(256), 0, s, false,
+                       static_cast<const uint4*>(gamma), static_cast<const uint4*>(w), chunks, cols / 8,
+                       static_cast<uint4*>(w_folded));
 }
 
 int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,

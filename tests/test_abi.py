@@ -86,6 +86,14 @@ def test_host_argument_checks_without_a_gpu(lib):
     assert L.llama_linear(None, None, 4, 250, 256, None, 0, None, 0, None) == lb.LLAMA_ERR_ARG  # null pointers first
     # norm: H must be a multiple of 8 within 16384
     assert L.llama_fused_add_rmsnorm(None, None, None, None, None, 4, 100, 1e-5, None) == lb.LLAMA_ERR_ARG
+    # folded norms: both norm weights NULL or neither (fake aligned addresses; rejected before any launch)
+    fake = 256
+    half = lb.LlamaLayerWeights(None, fake, fake, fake, fake, fake)
+    assert L.llama_layer_forward(ctypes.byref(c), ctypes.byref(half), None, None, None, None, None, None, None, 0,
+                                 None) == lb.LLAMA_ERR_ARG
+    # fold: null pointers, then columns that are not a multiple of 8
+    assert L.llama_fold_norm_weights(None, None, 4, 64, None, None) == lb.LLAMA_ERR_ARG
+    assert L.llama_fold_norm_weights(fake, fake, 4, 60, fake, None) == lb.LLAMA_ERR_UNSUPPORTED
 
 
 

@@ -33,10 +33,13 @@ def _untouched_on_device(before: torch.Tensor, after: torch.Tensor, written: np.
     assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name}: slots outside the batch changed"
 
 
-def _layer_case(name, sample_seqs, rows_in_seq=None, seed=0, dtype=np.float64):
+def _layer_case(name, sample_seqs, rows_in_seq=None, seed=0, dtype=np.float64, folded=False):
     spec = I.SPECS[name]
     bl = I.make_batch(spec, seed, DEV)
     w = I.make_layer_weights(spec, seed, 0, DEV)
+    # folded norms: the GPU runs gamma folded into w_qkv / w_gate_up; the
+    # oracle runs the unfolded layer (the same mathematics, rounded elsewhere)
+    w_gpu = lb.folded_layer_weights(w) if folded else w
     x, r = I.make_activations(spec, bl.num_tokens, seed, DEV)
     kc, vc = I.make_kv_cache(spec, bl.num_blocks, seed, 0, DEV)
     kc0, vc0 = kc.clone(), vc.clone()
@@ -46,7 +49,7 @@ def _layer_case(name, sample_seqs, rows_in_seq=None, seed=0, dtype=np.float64):
     ws = lb.alloc_workspace(lb.workspace_size(cfg, bl.num_tokens, bl.num_seqs, batch.max_seq_len), DEV)
     hid = x.clone()
     res = torch.empty_like(x)
-    lb.layer_forward(cfg, w, batch, hid, r, res, kc, vc, ws)
+    lb.layer_forward(cfg, w_gpu, batch, hid, r, res, kc, vc, ws)
     torch.cuda.synchronize()
     st, where = lb.get_device_error()
     assert st == lb.LLAMA_OK, f"device error {st} at {where}"
@@ -68,7 +71,8 @@ def _layer_case(name, sample_seqs, rows_in_seq=None, seed=0, dtype=np.float64):
                       O.bf16_bits_to_float(sub.oracle_written(kref)), f"{name} k written")
     e4 = assert_close(O.bf16_bits_to_float(sub.gpu_written(bits(vc))),
                       O.bf16_bits_to_float(sub.oracle_written(vref)), f"{name} v written")
-    print(f"{name}: rel err hidden {e1:.2e} residual {e2:.2e} k {e3:.2e} v {e4:.2e}")
+    print(f"{name}{' (folded norms)' if folded else ''}: rel err hidden {e1:.2e} residual {e2:.2e} k {e3:.2e} "
+          f"v {e4:.2e}")
 
 
 def test_tiny_full_config():
@@ -89,6 +93,33 @@ def test_prefill_70b_one_sequence_seeded_rows():
     seq = int(rng.integers(0, 8))
     rows = sorted(set(rng.choice(4096, size=254, replace=False).tolist()) | {0, 4095})
     _layer_case("prefill_70b", sample_seqs=[seq], rows_in_seq=rows)
+
+
+def test_folded_norms_tiny_and_decode_70b():
+    """Folded norms (ln1/ln2 None, gamma in w_qkv / w_gate_up) against the
+    unfolded oracle layer, on the tiny config and a seeded 70B decode subset."""
+    _layer_case("tiny", sample_seqs=range(2), folded=True)
+    rng = np.random.default_rng(2025)
+    _layer_case("decode_70b", sample_seqs=sorted(rng.choice(128, size=4, replace=False).tolist()), folded=True)
+
+
+def test_folded_norms_prefill_70b_seeded_rows():
+    rng = np.random.default_rng(8)
+    seq = int(rng.integers(0, 8))
+    rows = sorted(set(rng.choice(4096, size=126, replace=False).tolist()) | {0, 4095})
+    _layer_case("prefill_70b", sample_seqs=[seq], rows_in_seq=rows, folded=True)
+
+
+def test_fold_norm_weights_is_the_rounded_product():
+    """llama_fold_norm_weights: bf16(w * gamma) column-wise, bit for bit
+    against the oracle's bf16 rounding of the product (ragged row count)."""
+    g = I.normal_bf16((520,), 0.02, 1.0, 91, DEV)
+    w = I.normal_bf16((37, 520), 0.02, 0.0, 92, DEV)
+    got = lb.fold_norm_weights(g, w)
+    torch.cuda.synchronize()
+    want = O.round_to_bf16(f32(w).astype(np.float64) * f32(g).astype(np.float64)[None, :])
+    # the product of two bf16 values is exact in fp64 and in fp32 (8-bit significands)
+    assert np.array_equal(f32(got), want.astype(np.float32))
 
 
 def test_stack_70b_subset_tokens_and_logits():
