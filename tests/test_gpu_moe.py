@@ -36,6 +36,7 @@ def _f64(t):
     (300, 2048, 128, 8, 768),   # prefill-sized, several tiles per expert
     (5, 128, 8, 8, 64),         # k = E: every expert for every token
     (1, 256, 32, 2, 96),        # one token; moe_intermediate not a multiple of 128
+    (7, 200, 12, 3, 40),        # hidden not a multiple of 64 (ragged K tail), 12 experts, k = 3
 ])
 def test_moe_block_matches_the_oracle(T, H, E, K, Im):
     seed = T * 7 + E
