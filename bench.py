@@ -719,8 +719,8 @@ def run_sampler(args, world, rank, local):
         "roofline": {"kernel": "k_sample", "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
                      "algorithmic_bytes": nbytes, "traffic": None,
-                     "note": "one CTA per row and up to 13 passes over its 513 KB (L2-resident after the first): "
-                             "latency-bound, not bandwidth-bound"},
+                     "note": "a cluster of 4 CTAs per row, two passes over its 513 KB (top-k candidates, then the "
+                             "selection in shared memory): latency-bound, not bandwidth-bound"},
         "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
     }
     if rank == 0:

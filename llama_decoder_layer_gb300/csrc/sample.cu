@@ -10,12 +10,23 @@
 //       kept mass exceeds u times the total kept mass
 //   logprob = l_token - log(sum_j exp(l_j))   (the unscaled logits)
 //
-// One CTA per row.  Thresholds are found on the logits' order-preserving
-// 32-bit keys (dividing by T > 0 keeps the order): top-k by a radix select on
-// counts, top-p by a radix descent on mass, digits of 12, 12 and 8 bits.  Masses are
-// 64-bit fixed point (w_i * 2^40, w_i in (0, 1]), so every histogram, sum and
-// scan is exact integer arithmetic: the result does not depend on the order of
-// the atomic adds, and the same call always returns the same tokens.
+// A row is split over a thread-block cluster of up to 8 CTAs.  Thresholds are
+// found on the logits' order-preserving 32-bit keys (dividing by T > 0 keeps
+// the order).  Masses are 64-bit fixed point (w_i * 2^40, w_i in (0, 1]), so
+// every histogram, sum and scan is exact integer arithmetic: the result does
+// not depend on the order of the atomic adds, and the same call always returns
+// the same tokens.
+//
+// Top-k rows with k <= 1024 (the fast path): one pass gives the row maximum,
+// its index, the log-normaliser (an online sum) and a histogram of the keys'
+// top 12 bits; the cluster sums its CTAs' histograms through distributed
+// shared memory.  Once the keys at or above the bin holding the k-th largest
+// number at most 1024, one more pass gathers them (else the next 12 and 8
+// bits refine the bin first), and the k-th largest key, the top-p threshold
+// and the inverse-CDF draw are taken exactly over those candidates.  Other
+// rows (no top-k, k > 1024, or more than 1024 keys tied at the k-th value)
+// take the general path in the cluster's first CTA: a radix select on counts
+// for top-k and a radix descent on mass for top-p over the whole row.
 //
 // Sources: [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", Sampler
 // (sample(): greedy rows take the argmax; temperature scaling; the top-k /
@@ -106,15 +117,37 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan_u64(unsigned 
 
 constexpr int kBinsMax = 4096;  // 12-bit digits
 
+constexpr int kCandMax = 1024;  // candidates of the fast path (one per thread)
+constexpr int kMaxCluster = 8;  // CTAs per row
+
+struct Cand {
+  int idx;
+  float logit;
+};
+
+// hist doubles as the fast path's storage: 4096 uint32 counts in its first
+// half and this CTA's candidate list (up to 2048) in its second half; after
+// the last histogram the first CTA assembles the cluster's candidates (index,
+// key, weight) in the first half.
 struct SampleShared {
   unsigned long long hist[kBinsMax];
   unsigned long long red_u[kSampWarps];
   float red_f[kSampWarps];
   float best_v[kSampWarps];
   int best_i[kSampWarps];
+  uint32_t red_k[kSampWarps];
   uint32_t digit;
   unsigned long long acc;
+  uint32_t bin_count;
   int token;
+  // this CTA's pass-one partials, read by the cluster: max, its index, and the
+  // online log-sum (m, s) with sum_i exp(x_i - m) = s
+  float part_best, part_m, part_s;
+  int part_bi;
+  int cand_n;
+  // the cluster's merged values
+  float lmax, log_z;
+  int amax;
 };
 
 // Every pass over a row goes through for_row: each thread loads kUnroll
@@ -124,20 +157,25 @@ struct SampleShared {
 constexpr int kUnroll = 8;
 
 template <class F>
-__device__ __forceinline__ void for_row(const float* __restrict__ row, int V, F&& f) {
-  for (int base = threadIdx.x; base < V; base += kSampThreads * kUnroll) {
+__device__ __forceinline__ void for_range(const float* __restrict__ row, int i0, int i1, F&& f) {
+  for (int base = i0 + static_cast<int>(threadIdx.x); base < i1; base += kSampThreads * kUnroll) {
     float x[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = base + u * kSampThreads;
-      x[u] = i < V ? __ldg(row + i) : 0.f;
+      x[u] = i < i1 ? __ldg(row + i) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = base + u * kSampThreads;
-      if (i < V) f(i, x[u]);
+      if (i < i1) f(i, x[u]);
     }
   }
+}
+
+template <class F>
+__device__ __forceinline__ void for_row(const float* __restrict__ row, int V, F&& f) {
+  for_range(row, 0, V, f);
 }
 
 // Largest key t with S(key >= t) >= need, where S counts the tokens (MASS
@@ -203,6 +241,173 @@ __device__ __forceinline__ unsigned long long kept_mass(const float* row, int V,
   return block_sum_u64(m, sh.red_u);
 }
 
+// (m, s) <- (m, s) + (m2, s2) for online log-sums: sum exp(x - m) = s
+__device__ __forceinline__ void lse_add(float& m, float& s, float m2, float s2) {
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;  // m = -inf: s is 0
+    m = m2;
+  } else if (m2 > -INFINITY) {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__device__ __forceinline__ void best_add(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
+  v = __reduce_max_sync(0xffffffffu, v);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  return __reduce_max_sync(0xffffffffu, lane < kSampWarps ? red[lane] : 0u);
+}
+
+// The bin of `bits` bits (below `shift`) where the count of keys from the top
+// reaches `need`, over the cluster's summed histograms; `above` counts the keys
+// above the current prefix range.  Sets sh.digit, sh.acc (the count above the
+// bin) and sh.bin_count.
+__device__ void select_bin(const uint32_t* cnt, int bits, unsigned long long above, unsigned long long need,
+                           uint32_t C, SampleShared& sh) {
+  const int nb = 1 << bits;
+  const int per = nb >= kSampThreads ? nb / kSampThreads : 1;
+  const int j0 = threadIdx.x * per;
+  uint32_t mine[kBinsMax / kSampThreads];
+  unsigned long long local = 0;
+  const uint32_t base = smem_u32(cnt);
+  // every remote load of the thread is issued before any is summed
+  uint32_t v[kBinsMax / kSampThreads][kMaxCluster];
+#pragma unroll
+  for (int q = 0; q < kBinsMax / kSampThreads; ++q)
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      v[q][r] = q < per && j0 < nb && r < static_cast<int>(C)
+                    ? ld_cluster_u32(mapa_shared(base + 4u * (nb - 1 - (j0 + q)), static_cast<uint32_t>(r)))
+                    : 0u;
+#pragma unroll
+  for (int q = 0; q < kBinsMax / kSampThreads; ++q) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) c += v[q][r];
+    mine[q] = c;
+    local += c;
+  }
+  const unsigned long long excl = above + block_exclusive_scan_u64(local, sh.red_u);
+  if (j0 < nb && excl < need && need <= excl + local) {
+    unsigned long long run = excl;
+#pragma unroll
+    for (int q = 0; q < kBinsMax / kSampThreads; ++q) {
+      if (q >= per) break;
+      if (run + mine[q] >= need) {
+        sh.digit = static_cast<uint32_t>(nb - 1 - (j0 + q));
+        sh.acc = run;
+        sh.bin_count = mine[q];
+        break;
+      }
+      run += mine[q];
+    }
+  }
+  __syncthreads();
+}
+
+// The general path over the whole row, by one CTA: top-k threshold key (0 for
+// none), top-p by a radix descent on mass above it, and the inverse-CDF draw in
+// index order.  Returns the token.
+__device__ int sample_general(const float* row, int V, float lmax, float inv_t, int k, float p, float u_in,
+                              int amax, SampleShared& sh) {
+  uint32_t t_key = 0;  // keep everything
+  if (k > 0 && k < V) t_key = threshold_key<false>(row, V, lmax, inv_t, static_cast<unsigned long long>(k), 0u, sh);
+  if (p < 1.f) {
+    const unsigned long long mass_k = kept_mass(row, V, lmax, inv_t, t_key, sh);
+    const double pc = p > 0.f ? static_cast<double>(p) : 0.0;
+    // at least one unit, so the threshold is the key of a token that has
+    // weight (p -> 0 keeps the maximum and its ties)
+    unsigned long long target = static_cast<unsigned long long>(pc * static_cast<double>(mass_k));
+    if (target < 1) target = 1;
+    const uint32_t t_p = threshold_key<true>(row, V, lmax, inv_t, target, t_key, sh);
+    if (t_p > t_key) t_key = t_p;
+  }
+  const unsigned long long total = kept_mass(row, V, lmax, inv_t, t_key, sh);
+  const float u = u_in > 0.f ? (u_in < 1.f ? u_in : 0.99999994f) : 0.f;
+  const unsigned long long target = static_cast<unsigned long long>(static_cast<double>(u) *
+                                                                    static_cast<double>(total));
+  // inverse CDF in index order: contiguous chunks per thread, block scan
+  const int chunk = (V + kSampThreads - 1) / kSampThreads;
+  const int c0 = threadIdx.x * chunk;
+  const int c1 = min(V, c0 + chunk);
+  unsigned long long cm = 0;
+  for (int i = c0; i < c1; ++i) {
+    const float l = row[i];
+    if (order_key(l) >= t_key) cm += fixed_weight(l, lmax, inv_t);
+  }
+  if (threadIdx.x == 0) sh.token = amax;
+  const unsigned long long excl = block_exclusive_scan_u64(cm, sh.red_u);
+  if (cm > 0 && excl <= target && target < excl + cm) {
+    unsigned long long acc = excl;
+    for (int i = c0; i < c1; ++i) {
+      const float l = row[i];
+      if (order_key(l) < t_key) continue;
+      acc += fixed_weight(l, lmax, inv_t);
+      if (acc > target) {
+        sh.token = i;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  return sh.token;
+}
+
+// The fast path's selection over n <= kCandMax candidates that include every
+// key >= the row's k-th largest (thread j owns candidate j): the exact top-k
+// threshold, top-p above it, and the inverse-CDF draw in index order.
+__device__ int sample_candidates(const int* idx_s, const uint32_t* key_s, const unsigned long long* w_s, int n, int k,
+                                 float p, float u_in, int amax, SampleShared& sh) {
+  const int j = threadIdx.x;
+  const bool mine = j < n;
+  const uint32_t kj = mine ? key_s[j] : 0u;
+  const unsigned long long wj = mine ? w_s[j] : 0ull;
+  // the k-th largest key: the largest key with at least k keys >= it
+  int ge = 0;
+  if (mine)
+    for (int i = 0; i < n; ++i) ge += key_s[i] >= kj;
+  uint32_t t_key = block_max_u32(mine && ge >= k ? kj : 0u, sh.red_k);
+  bool kept = mine && kj >= t_key;
+  if (p < 1.f) {
+    const unsigned long long mass_k = block_sum_u64(kept ? wj : 0ull, sh.red_u);
+    const double pc = p > 0.f ? static_cast<double>(p) : 0.0;
+    unsigned long long target = static_cast<unsigned long long>(pc * static_cast<double>(mass_k));
+    if (target < 1) target = 1;
+    // the largest kept key whose mass of kept keys >= it reaches the target
+    unsigned long long s_ge = 0;
+    if (kept)
+      for (int i = 0; i < n; ++i)
+        if (key_s[i] >= kj && key_s[i] >= t_key) s_ge += w_s[i];
+    const uint32_t t_p = block_max_u32(kept && s_ge >= target ? kj : 0u, sh.red_k);
+    if (t_p > t_key) t_key = t_p;
+    kept = mine && kj >= t_key;
+  }
+  const unsigned long long total = block_sum_u64(kept ? wj : 0ull, sh.red_u);
+  const float u = u_in > 0.f ? (u_in < 1.f ? u_in : 0.99999994f) : 0.f;
+  const unsigned long long target = static_cast<unsigned long long>(static_cast<double>(u) *
+                                                                    static_cast<double>(total));
+  if (threadIdx.x == 0) sh.token = amax;
+  __syncthreads();
+  if (kept && wj > 0) {  // inclusive running mass in index order
+    const int ij = idx_s[j];
+    unsigned long long run = 0;
+    for (int i = 0; i < n; ++i)
+      if (key_s[i] >= t_key && idx_s[i] <= ij) run += w_s[i];
+    if (run > target && run - wj <= target) sh.token = ij;
+  }
+  __syncthreads();
+  return sh.token;
+}
+
 __global__ void __launch_bounds__(kSampThreads, 1) k_sample(const float* __restrict__ logits, int V,
                                                           const float* __restrict__ temperature,
                                                           const int32_t* __restrict__ top_k,
@@ -212,102 +417,171 @@ __global__ void __launch_bounds__(kSampThreads, 1) k_sample(const float* __restr
                                                           float* __restrict__ out_logprobs) {
   __shared__ SampleShared sh;
   pdl_wait();
-  const int b = blockIdx.x;
+  const uint32_t C = cluster_nctarank(), rank = cluster_ctarank();
+  const int b = blockIdx.x / static_cast<int>(C);
   const float* row = logits + static_cast<size_t>(b) * V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_cta = (V + static_cast<int>(C) - 1) / static_cast<int>(C);
+  const int s0 = min(V, static_cast<int>(rank) * per_cta), s1 = min(V, s0 + per_cta);
 
-  // maximum and its lowest index
-  float best = -FLT_MAX;
+  const float t = temperature[b];
+  const bool greedy = !(t >= kGreedyTemperature);  // (a NaN temperature samples greedily)
+  const int k = top_k[b];
+  const float p = top_p[b];
+  const bool fast = !greedy && k > 0 && k < V && k <= kCandMax;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(sh.hist);
+  Cand* cand = reinterpret_cast<Cand*>(sh.hist + kBinsMax / 2);
+  if (fast)
+    for (int i = threadIdx.x; i < kBinsMax; i += kSampThreads) cnt[i] = 0;
+  if (threadIdx.x == 0) sh.cand_n = 0;
+  __syncthreads();
+
+  // pass one over this CTA's slice: maximum (lowest index), online log-sum,
+  // and the histogram of the keys' top 12 bits
+  float best = -FLT_MAX, m = -INFINITY, se = 0.f;
   int bi = 0x7fffffff;
-  for_row(row, V, [&](int i, float x) {  // i increases within a thread: strict > keeps the lowest
+  for_range(row, s0, s1, [&](int i, float x) {  // i increases within a thread: strict > keeps the lowest
     if (x > best) {
       best = x;
       bi = i;
     }
+    if (x > m) {
+      se = se * expf(m - x) + 1.f;
+      m = x;
+    } else if (x > -INFINITY) {
+      se += expf(x - m);
+    }
+    if (fast) atomicAdd(&cnt[order_key(x) >> 20], 1u);
   });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
-      best = ov;
-      bi = oi;
-    }
+    best_add(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+    lse_add(m, se, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, se, o));
   }
   if (lane == 0) {
     sh.best_v[warp] = best;
     sh.best_i[warp] = bi;
+    sh.red_f[warp] = m;
+    sh.red_u[warp] = __float_as_uint(se);
   }
   __syncthreads();
-  best = lane < kSampWarps ? sh.best_v[lane] : -FLT_MAX;
-  bi = lane < kSampWarps ? sh.best_i[lane] : 0x7fffffff;
+  if (threadIdx.x == 0) {
+    float bv = -FLT_MAX, mm = -INFINITY, ss = 0.f;
+    int bj = 0x7fffffff;
+    for (int w = 0; w < kSampWarps; ++w) {
+      best_add(bv, bj, sh.best_v[w], sh.best_i[w]);
+      lse_add(mm, ss, sh.red_f[w], __uint_as_float(static_cast<uint32_t>(sh.red_u[w])));
+    }
+    sh.part_best = bv;
+    sh.part_bi = bj;
+    sh.part_m = mm;
+    sh.part_s = ss;
+  }
+  cluster_sync();  // every CTA's partials and histogram are complete
+  if (warp == 0) {  // lane r reads CTA r's partials; a fixed shuffle tree merges them
+    float bv = -FLT_MAX, mm = -INFINITY, ss = 0.f;
+    int bj = 0x7fffffff;
+    if (lane < static_cast<int>(C)) {
+      const uint32_t r = static_cast<uint32_t>(lane);
+      bv = __uint_as_float(ld_cluster_u32(mapa_shared(smem_u32(&sh.part_best), r)));
+      bj = static_cast<int>(ld_cluster_u32(mapa_shared(smem_u32(&sh.part_bi), r)));
+      mm = __uint_as_float(ld_cluster_u32(mapa_shared(smem_u32(&sh.part_m), r)));
+      ss = __uint_as_float(ld_cluster_u32(mapa_shared(smem_u32(&sh.part_s), r)));
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
-      best = ov;
-      bi = oi;
+    for (int o = 16; o > 0; o >>= 1) {
+      best_add(bv, bj, __shfl_xor_sync(0xffffffffu, bv, o), __shfl_xor_sync(0xffffffffu, bj, o));
+      lse_add(mm, ss, __shfl_xor_sync(0xffffffffu, mm, o), __shfl_xor_sync(0xffffffffu, ss, o));
+    }
+    if (lane == 0) {
+      sh.lmax = bv;
+      sh.amax = bj == 0x7fffffff ? 0 : bj;
+      sh.log_z = mm + logf(ss);
     }
   }
-  const float lmax = best;
-  const int amax = bi == 0x7fffffff ? 0 : bi;
+  if (fast) select_bin(cnt, 12, 0ull, static_cast<unsigned long long>(k), C, sh);
+  __syncthreads();
+  cluster_sync();  // the cluster has read every CTA's pass-one results
+  const float lmax = sh.lmax;
+  const int amax = sh.amax;
+  const float log_z = sh.log_z;
 
-  // log of the raw normaliser
-  float se = 0.f;
-  for_row(row, V, [&](int, float x) { se += expf(x - lmax); });
-  const float log_z = lmax + logf(block_sum_f(se, sh.red_f));
-
-  const float t = temperature[b];
   int token = amax;
-  if (t >= kGreedyTemperature) {  // (a NaN temperature samples greedily)
-    const float inv_t = 1.f / t;
-    const int k = top_k[b];
-    uint32_t t_key = 0;  // keep everything
-    if (k > 0 && k < V)
-      t_key = threshold_key<false>(row, V, lmax, inv_t, static_cast<unsigned long long>(k), 0u, sh);
-    const float p = top_p[b];
-    if (p < 1.f) {
-      const unsigned long long mass_k = kept_mass(row, V, lmax, inv_t, t_key, sh);
-      const double pc = p > 0.f ? static_cast<double>(p) : 0.0;
-      // at least one unit, so the threshold is the key of a token that has
-      // weight (p -> 0 keeps the maximum and its ties)
-      unsigned long long target = static_cast<unsigned long long>(pc * static_cast<double>(mass_k));
-      if (target < 1) target = 1;
-      const uint32_t t_p = threshold_key<true>(row, V, lmax, inv_t, target, t_key, sh);
-      if (t_p > t_key) t_key = t_p;
+  bool general = !greedy && !fast;
+  if (fast) {
+    // refine the bin of the k-th largest key until the keys at or above it
+    // fit the candidate list (all CTAs take the same decisions)
+    uint32_t prefix = sh.digit << 20, mask = 0xFFF00000u;
+    unsigned long long above = sh.acc;
+    unsigned long long n_ge = sh.acc + sh.bin_count;
+#pragma unroll 1
+    for (int level = 1; level < 3 && n_ge > static_cast<unsigned long long>(kCandMax); ++level) {
+      const int bits = level == 1 ? 12 : 8;
+      const int shift = level == 1 ? 8 : 0;
+      for (int i = threadIdx.x; i < kBinsMax; i += kSampThreads) cnt[i] = 0;
+      __syncthreads();
+      for_range(row, s0, s1, [&](int, float x) {
+        const uint32_t key = order_key(x);
+        if ((key & mask) == prefix) atomicAdd(&cnt[(key >> shift) & ((1u << bits) - 1u)], 1u);
+      });
+      __syncthreads();
+      cluster_sync();
+      select_bin(cnt, bits, above, static_cast<unsigned long long>(k), C, sh);
+      cluster_sync();
+      prefix |= sh.digit << shift;
+      mask |= ((1u << bits) - 1u) << shift;
+      above = sh.acc;
+      n_ge = sh.acc + sh.bin_count;
     }
-    const unsigned long long total = kept_mass(row, V, lmax, inv_t, t_key, sh);
-    float u = uniform[b];
-    u = u > 0.f ? (u < 1.f ? u : 0.99999994f) : 0.f;
-    const unsigned long long target = static_cast<unsigned long long>(static_cast<double>(u) *
-                                                                      static_cast<double>(total));
-    // inverse CDF in index order: contiguous chunks per thread, block scan
-    const int chunk = (V + kSampThreads - 1) / kSampThreads;
-    const int c0 = threadIdx.x * chunk;
-    const int c1 = min(V, c0 + chunk);
-    unsigned long long cm = 0;
-    for (int i = c0; i < c1; ++i) {
-      const float l = row[i];
-      if (order_key(l) >= t_key) cm += fixed_weight(l, lmax, inv_t);
-    }
-    if (threadIdx.x == 0) sh.token = amax;
-    const unsigned long long excl = block_exclusive_scan_u64(cm, sh.red_u);
-    if (cm > 0 && excl <= target && target < excl + cm) {
-      unsigned long long acc = excl;
-      for (int i = c0; i < c1; ++i) {
-        const float l = row[i];
-        if (order_key(l) < t_key) continue;
-        acc += fixed_weight(l, lmax, inv_t);
-        if (acc > target) {
-          sh.token = i;
-          break;
+    if (n_ge > static_cast<unsigned long long>(kCandMax)) {
+      general = true;  // more than kCandMax keys tie at the k-th value
+    } else {
+      // gather every key >= prefix (the top-k and the rest of its bin)
+      for_range(row, s0, s1, [&](int i, float x) {
+        if (order_key(x) >= prefix) {
+          const int at = atomicAdd(&sh.cand_n, 1);
+          cand[at] = Cand{i, x};
+        }
+      });
+      __syncthreads();
+      cluster_sync();  // every candidate list is complete
+      int* idx_s = reinterpret_cast<int*>(sh.hist);
+      uint32_t* key_s = reinterpret_cast<uint32_t*>(idx_s + kCandMax);
+      unsigned long long* w_s = sh.hist + kCandMax;  // bytes 8 KB .. 16 KB, after idx_s and key_s
+      int n = 0;
+      if (rank == 0) {
+        // candidate j of the cluster: thread j reads it from its CTA's list
+        int nr[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          nr[r] = r < static_cast<int>(C)
+                      ? static_cast<int>(ld_cluster_u32(mapa_shared(smem_u32(&sh.cand_n), static_cast<uint32_t>(r))))
+                      : 0;
+        int base = 0, src = -1, at = 0;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (src < 0 && static_cast<int>(threadIdx.x) < base + nr[r]) {
+            src = r;
+            at = threadIdx.x - base;
+          }
+          base += nr[r];
+        }
+        n = base;
+        const float inv_t = 1.f / t;
+        if (src >= 0) {
+          const uint2 c = ld_cluster_u32x2(mapa_shared(smem_u32(&cand[at]), static_cast<uint32_t>(src)));
+          const float x = __uint_as_float(c.y);
+          idx_s[threadIdx.x] = static_cast<int>(c.x);
+          key_s[threadIdx.x] = order_key(x);
+          w_s[threadIdx.x] = fixed_weight(x, lmax, inv_t);
         }
       }
+      cluster_sync();  // the first CTA has copied every list; the others may leave
+      if (rank == 0) token = sample_candidates(idx_s, key_s, w_s, n, k, p, uniform[b], amax, sh);
     }
-    __syncthreads();
-    token = sh.token;
   }
+  if (rank != 0) return;
+  if (general) token = sample_general(row, V, lmax, 1.f / t, k, p, uniform[b], amax, sh);
   if (threadIdx.x == 0) {
     out_tokens[b] = token;
     if (out_logprobs != nullptr) out_logprobs[b] = row[token] - log_z;
@@ -320,8 +594,13 @@ int sample_launch(const float* logits, int rows, int vocab, const float* tempera
                   const float* top_p, const float* uniform, int32_t* out_tokens, float* out_logprobs, bool pdl,
                   cudaStream_t s) {
   if (rows <= 0) return 0;
-  return launch_kernel(k_sample, dim3(rows), dim3(kSampThreads), 0, s, pdl, logits, vocab, temperature, top_k, top_p,
-                       uniform, out_tokens, out_logprobs);
+  // CTAs per row: a power of two up to 8 while the rows' clusters fit the SMs
+  // once, and none for short rows
+  int C = 1;
+  const int sms = num_sms();
+  while (C < 8 && vocab >= 16384 * C && static_cast<long long>(rows) * C * 2 <= sms) C *= 2;
+  return launch_kernel_cluster(k_sample, dim3(rows * C), dim3(kSampThreads), 0, s, pdl, C, logits, vocab,
+                               temperature, top_k, top_p, uniform, out_tokens, out_logprobs);
 }
 
 }  // namespace llama

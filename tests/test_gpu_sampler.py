@@ -99,6 +99,22 @@ def test_sampler_full_vocabulary():
     assert exact >= B - 3
 
 
+def test_sampler_full_vocabulary_with_ties_at_the_k_boundary():
+    # integer logits over the full vocabulary: at k = 1000 more than 1024 keys
+    # tie at or above the k-th value (the general path), at k = 50 they do not
+    # (the candidate path); one row per cluster size as well
+    rng = np.random.default_rng(5)
+    B, V = 12, 128256
+    logits = np.round(rng.normal(size=(B, V)) * 2)
+    t = np.full(B, 0.9)
+    k = np.array([1000, 50] * (B // 2))
+    p = rng.choice([1.0, 0.9, 0.5], size=B)
+    u = rng.random(B)
+    _check(logits, t, k, p, u)
+    _check(logits[:1], t[:1], k[:1], p[:1], u[:1])
+    _check(logits[1:2], t[1:2], k[1:2], p[1:2], u[1:2])
+
+
 @pytest.mark.parametrize("V", [1, 7, 37, 1000])
 def test_sampler_small_and_ragged_vocabularies_with_ties(V):
     rng = np.random.default_rng(V)
