@@ -710,6 +710,11 @@ def run_sampler(args, world, rank, local):
                             world, sampler, counter=lb.launch_count)
     nbytes = rows * vocab * 4
     gbs = nbytes / (ms / 1e3) / 1e9
+    # the same rows with no truncation (top-k off, top-p 1): the draw over the whole vocabulary
+    top_k0 = torch.zeros_like(top_k)
+    top_p1 = torch.ones_like(top_p)
+    ms_full, _ = time_steps(lambda: lb.sample(logits, temp, top_k0, top_p1, u, tok, lp), args.steps, args.warmup,
+                            world)
     line = {
         "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
         "value": round(rows * world / (ms / 1e3), 1), "unit": "sampled tokens/s", "n_gpus": world,
@@ -722,6 +727,7 @@ def run_sampler(args, world, rank, local):
                      "note": "a cluster of 4 CTAs per row, two passes over its 513 KB (top-k candidates, then the "
                              "selection in shared memory): latency-bound, not bandwidth-bound"},
         "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
+        "no_truncation": {"ms_per_step": round(ms_full, 4), "config": "temperature 0.8, top-k off, top-p 1"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -17,6 +17,11 @@
 // not depend on the order of the atomic adds, and the same call always returns
 // the same tokens.
 //
+// Rows without truncation (top-k off, top-p >= 1): after the first pass, each
+// warp sums the weights of a contiguous segment of its CTA's slice, the cluster
+// exchanges its CTAs' sums, and the warp whose segment holds the draw finds
+// the token with 32-wide scans.
+//
 // Top-k rows with k <= 1024 (the fast path): one pass gives the row maximum,
 // its index, the log-normaliser (an online sum) and a histogram of the keys'
 // top 12 bits; the cluster sums its CTAs' histograms through distributed
@@ -24,9 +29,10 @@
 // number at most 1024, one more pass gathers them (else the next 12 and 8
 // bits refine the bin first), and the k-th largest key, the top-p threshold
 // and the inverse-CDF draw are taken exactly over those candidates.  Other
-// rows (no top-k, k > 1024, or more than 1024 keys tied at the k-th value)
-// take the general path in the cluster's first CTA: a radix select on counts
-// for top-k and a radix descent on mass for top-p over the whole row.
+// rows (top-p without top-k, k > 1024, or more than 1024 keys tied at the
+// k-th value) take the general path in the cluster's first CTA: a radix
+// select on counts for top-k and a radix descent on mass for top-p over the
+// whole row.
 //
 // Sources: [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", Sampler
 // (sample(): greedy rows take the argmax; temperature scaling; the top-k /
@@ -148,6 +154,11 @@ struct SampleShared {
   // the cluster's merged values
   float lmax, log_z;
   int amax;
+  // rows without truncation: the mass of each warp's segment and of this CTA
+  unsigned long long warp_mass[kSampWarps];
+  unsigned long long part_mass;
+  unsigned long long target;  // the draw, as a mass offset inside this CTA's slice
+  int owner;                  // 1 when the draw falls in this CTA's slice
 };
 
 // Every pass over a row goes through for_row: each thread loads kUnroll
@@ -507,7 +518,93 @@ __global__ void __launch_bounds__(kSampThreads, 1) k_sample(const float* __restr
   const float log_z = sh.log_z;
 
   int token = amax;
-  bool general = !greedy && !fast;
+  // no truncation (top-k off or >= V, top-p >= 1): the draw over the whole row
+  const bool full = !greedy && !(k > 0 && k < V) && !(p < 1.f);
+  bool general = !greedy && !fast && !full;
+  if (full) {
+    // every warp owns a contiguous segment of this CTA's slice, so (rank,
+    // warp, lane) order is index order
+    const float inv_t = 1.f / t;
+    const int seg = (s1 - s0 + kSampWarps - 1) / kSampWarps;
+    const int w0 = min(s1, s0 + warp * seg), w1 = min(s1, w0 + seg);
+    unsigned long long wm = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32 * kUnroll) {
+      float x[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = i0 + u * 32 + lane;
+        x[u] = i < w1 ? __ldg(row + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (i0 + u * 32 + lane < w1) wm += fixed_weight(x[u], lmax, inv_t);
+    }
+    wm = warp_sum(wm);
+    if (lane == 0) sh.warp_mass[warp] = wm;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long m = 0;
+      for (int w = 0; w < kSampWarps; ++w) m += sh.warp_mass[w];
+      sh.part_mass = m;
+    }
+    cluster_sync();  // every CTA's mass is complete
+    if (warp == 0) {  // lane r reads CTA r's mass
+      const uint32_t addr = smem_u32(&sh.part_mass);
+      unsigned long long m = 0;
+      if (lane < static_cast<int>(C)) {
+        const uint2 v = ld_cluster_u32x2(mapa_shared(addr, static_cast<uint32_t>(lane)));
+        m = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+      }
+      unsigned long long incl = m;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+      const unsigned long long excl = __shfl_sync(0xffffffffu, incl - m, static_cast<int>(rank));
+      const unsigned long long mine = __shfl_sync(0xffffffffu, m, static_cast<int>(rank));
+      float u = uniform[b];
+      u = u > 0.f ? (u < 1.f ? u : 0.99999994f) : 0.f;
+      const unsigned long long target =
+          static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
+      if (lane == 0) {
+        sh.owner = excl <= target && target < excl + mine ? 1 : 0;
+        sh.target = target - excl;
+      }
+    }
+    __syncthreads();
+    cluster_sync();  // the cluster has read every CTA's mass; CTAs may leave
+    if (!sh.owner) return;
+    // the warp whose segment holds the draw scans it 32 elements at a time
+    const unsigned long long tgt = sh.target;
+    unsigned long long wex = 0;
+    for (int w = 0; w < warp; ++w) wex += sh.warp_mass[w];
+    if (wex <= tgt && tgt < wex + sh.warp_mass[warp]) {
+      unsigned long long acc = wex;
+      for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned long long wi = i < w1 ? fixed_weight(row[i], lmax, inv_t) : 0ull;
+        unsigned long long incl = wi;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned int hit = __ballot_sync(0xffffffffu, acc + incl > tgt);
+        if (hit != 0u) {
+          const int first = __ffs(hit) - 1;
+          if (lane == first) {
+            out_tokens[b] = i;
+            if (out_logprobs != nullptr) out_logprobs[b] = row[i] - log_z;
+          }
+          break;
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    return;
+  }
   if (fast) {
     // refine the bin of the k-th largest key until the keys at or above it
     // fit the candidate list (all CTAs take the same decisions)

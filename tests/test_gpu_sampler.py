@@ -139,3 +139,24 @@ def test_sampler_frequencies_follow_the_distribution():
     keep = _kept_set(row, 0.8, 20, 0.9)
     w = np.where(keep, np.exp((row - row.max()) / 0.8), 0)
     assert np.max(np.abs(np.bincount(tok, minlength=V) / N - w / w.sum())) < 2.5 / N
+    # no truncation (top-k off, top-p 1): the whole softmax at temperature 0.8
+    tok, _ = _run(logits.astype(np.float32), np.full(N, 0.8), np.zeros(N), np.ones(N), u)
+    w = np.exp((row - row.max()) / 0.8)
+    assert np.max(np.abs(np.bincount(tok, minlength=V) / N - w / w.sum())) < 2.5 / N
+
+
+def test_sampler_no_truncation_full_vocabulary_frequencies():
+    # one 128256-wide row (a cluster of CTAs) under evenly spaced draws, no
+    # truncation: the cumulative frequencies follow the softmax's CDF
+    V, N = 128256, 64
+    rng = np.random.default_rng(10)
+    row = rng.normal(size=V) * 3
+    logits = np.repeat(row[None].astype(np.float32), N, axis=0)
+    u = (np.arange(N) + 0.5) / N
+    tok, _ = _run(logits, np.ones(N), np.zeros(N), np.ones(N), u)
+    x = row.astype(np.float32).astype(np.float64)
+    cdf = np.cumsum(np.exp(x - x.max()))
+    cdf /= cdf[-1]
+    # token n is where the CDF crosses u_n (to within the fixed-point and fp32-weight rounding)
+    want = np.searchsorted(cdf, u, side="right")
+    assert np.mean(tok == want) >= 0.95 and np.all(np.abs(cdf[tok] - u) < 1e-3)
