@@ -157,6 +157,8 @@ def test_sampler_no_truncation_full_vocabulary_frequencies():
     x = row.astype(np.float32).astype(np.float64)
     cdf = np.cumsum(np.exp(x - x.max()))
     cdf /= cdf[-1]
-    # token n is where the CDF crosses u_n (to within the fixed-point and fp32-weight rounding)
+    # token n is the first where the CDF exceeds u_n; a draw within rounding
+    # (fp32 weights, 40-bit fixed point) of a step may take the neighbouring token
     want = np.searchsorted(cdf, u, side="right")
-    assert np.mean(tok == want) >= 0.95 and np.all(np.abs(cdf[tok] - u) < 1e-3)
+    near = np.minimum(np.abs(cdf[want] - u), np.abs(cdf[np.maximum(want - 1, 0)] - u)) < 1e-5
+    assert np.all((tok == want) | near), np.nonzero((tok != want) & ~near)
