@@ -715,6 +715,9 @@ def run_sampler(args, world, rank, local):
     top_p1 = torch.ones_like(top_p)
     ms_full, _ = time_steps(lambda: lb.sample(logits, temp, top_k0, top_p1, u, tok, lp), args.steps, args.warmup,
                             world)
+    # top-p alone (top-k off, top-p 0.9)
+    ms_topp, _ = time_steps(lambda: lb.sample(logits, temp, top_k0, top_p, u, tok, lp), args.steps, args.warmup,
+                            world)
     line = {
         "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
         "value": round(rows * world / (ms / 1e3), 1), "unit": "sampled tokens/s", "n_gpus": world,
@@ -728,6 +731,7 @@ def run_sampler(args, world, rank, local):
                              "selection in shared memory): latency-bound, not bandwidth-bound"},
         "clocks": clocks, "gpu_launches": time_steps.launches, "cpu_baseline": None, "e2e": None,
         "no_truncation": {"ms_per_step": round(ms_full, 4), "config": "temperature 0.8, top-k off, top-p 1"},
+        "top_p_only": {"ms_per_step": round(ms_topp, 4), "config": "temperature 0.8, top-k off, top-p 0.9"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -144,7 +144,8 @@ struct SampleShared {
   uint32_t red_k[kSampWarps];
   uint32_t digit;
   unsigned long long acc;
-  uint32_t bin_count;
+  unsigned long long bin_count;
+  unsigned long long need;
   int token;
   // this CTA's pass-one partials, read by the cluster: max, its index, and the
   // online log-sum (m, s) with sum_i exp(x_i - m) = s
@@ -278,34 +279,52 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   return __reduce_max_sync(0xffffffffu, lane < kSampWarps ? red[lane] : 0u);
 }
 
-// The bin of `bits` bits (below `shift`) where the count of keys from the top
-// reaches `need`, over the cluster's summed histograms; `above` counts the keys
-// above the current prefix range.  Sets sh.digit, sh.acc (the count above the
-// bin) and sh.bin_count.
-__device__ void select_bin(const uint32_t* cnt, int bits, unsigned long long above, unsigned long long need,
-                           uint32_t C, SampleShared& sh) {
+__device__ __forceinline__ uint32_t ld_cluster_val(uint32_t addr, uint32_t rank, uint32_t) {
+  return ld_cluster_u32(mapa_shared(addr, rank));
+}
+
+__device__ __forceinline__ unsigned long long ld_cluster_val(uint32_t addr, uint32_t rank, unsigned long long) {
+  const uint2 v = ld_cluster_u32x2(mapa_shared(addr, rank));
+  return (static_cast<unsigned long long>(v.y) << 32) | v.x;
+}
+
+// The bin of `bits` bits where the sum of the histogram (counts of keys, or
+// their fixed-point masses) from the top reaches `need`, over the cluster's
+// summed histograms; `above` is the sum above the current prefix range.  With
+// p_frac >= 0 the need is max(1, floor(p_frac * total)) of this histogram's
+// total (left in sh.need).  Sets sh.digit, sh.acc (the sum above the bin) and
+// sh.bin_count (the bin's own sum).
+template <class T>
+__device__ void select_bin(const T* hist, int bits, unsigned long long above, unsigned long long need, uint32_t C,
+                           SampleShared& sh, float p_frac = -1.f) {
   const int nb = 1 << bits;
   const int per = nb >= kSampThreads ? nb / kSampThreads : 1;
   const int j0 = threadIdx.x * per;
-  uint32_t mine[kBinsMax / kSampThreads];
+  unsigned long long mine[kBinsMax / kSampThreads];
   unsigned long long local = 0;
-  const uint32_t base = smem_u32(cnt);
-  // every remote load of the thread is issued before any is summed
-  uint32_t v[kBinsMax / kSampThreads][kMaxCluster];
-#pragma unroll
-  for (int q = 0; q < kBinsMax / kSampThreads; ++q)
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      v[q][r] = q < per && j0 < nb && r < static_cast<int>(C)
-                    ? ld_cluster_u32(mapa_shared(base + 4u * (nb - 1 - (j0 + q)), static_cast<uint32_t>(r)))
-                    : 0u;
+  const uint32_t base = smem_u32(hist);
+  // a bin's remote loads (one per CTA) are all issued before they are summed
 #pragma unroll
   for (int q = 0; q < kBinsMax / kSampThreads; ++q) {
-    uint32_t c = 0;
+    T v[kMaxCluster];
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) c += v[q][r];
+    for (int r = 0; r < kMaxCluster; ++r)
+      v[r] = q < per && j0 < nb && r < static_cast<int>(C)
+                 ? ld_cluster_val(base + static_cast<uint32_t>(sizeof(T)) * (nb - 1 - (j0 + q)),
+                                  static_cast<uint32_t>(r), T{})
+                 : T{};
+    unsigned long long c = 0;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) c += v[r];
     mine[q] = c;
     local += c;
+  }
+  if (p_frac >= 0.f) {
+    const unsigned long long total = block_sum_u64(local, sh.red_u);
+    const double pc = p_frac > 0.f ? static_cast<double>(p_frac) : 0.0;
+    need = static_cast<unsigned long long>(pc * static_cast<double>(total));
+    if (need < 1) need = 1;  // at least one unit: the threshold is the key of a token with weight
+    if (threadIdx.x == 0) sh.need = need;
   }
   const unsigned long long excl = above + block_exclusive_scan_u64(local, sh.red_u);
   if (j0 < nb && excl < need && need <= excl + local) {
@@ -323,6 +342,89 @@ __device__ void select_bin(const uint32_t* cnt, int bits, unsigned long long abo
     }
   }
   __syncthreads();
+}
+
+// The inverse-CDF draw over the keys >= t_key of the whole row, on the
+// cluster: every warp sums the weights of a contiguous segment of its CTA's
+// slice (so rank, warp and lane order is index order), the CTAs exchange their
+// sums, and the warp whose segment holds the draw finds the token with
+// 32-wide scans and writes the outputs.  Every CTA of the cluster calls it.
+__device__ void draw_segmented(const float* row, int s0, int s1, float lmax, float inv_t, uint32_t t_key, float u_in,
+                               uint32_t C, uint32_t rank, float log_z, int32_t* out_token, float* out_logprob,
+                               SampleShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (s1 - s0 + kSampWarps - 1) / kSampWarps;
+  const int w0 = min(s1, s0 + warp * seg), w1 = min(s1, w0 + seg);
+  auto weight = [&](float x) { return order_key(x) >= t_key ? fixed_weight(x, lmax, inv_t) : 0ull; };
+  unsigned long long wm = 0;
+  for (int i0 = w0; i0 < w1; i0 += 32 * kUnroll) {
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * 32 + lane;
+      x[u] = i < w1 ? __ldg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (i0 + u * 32 + lane < w1) wm += weight(x[u]);
+  }
+  wm = warp_sum(wm);
+  if (lane == 0) sh.warp_mass[warp] = wm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = 0;
+    for (int w = 0; w < kSampWarps; ++w) m += sh.warp_mass[w];
+    sh.part_mass = m;
+  }
+  cluster_sync();  // every CTA's mass is complete
+  if (warp == 0) {  // lane r reads CTA r's mass
+    unsigned long long m = 0;
+    if (lane < static_cast<int>(C))
+      m = ld_cluster_val(smem_u32(&sh.part_mass), static_cast<uint32_t>(lane), 0ull);
+    unsigned long long incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+    const unsigned long long excl = __shfl_sync(0xffffffffu, incl - m, static_cast<int>(rank));
+    const unsigned long long mine = __shfl_sync(0xffffffffu, m, static_cast<int>(rank));
+    const float u = u_in > 0.f ? (u_in < 1.f ? u_in : 0.99999994f) : 0.f;
+    const unsigned long long target =
+        static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
+    if (lane == 0) {
+      sh.owner = excl <= target && target < excl + mine ? 1 : 0;
+      sh.target = target - excl;
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // the cluster has read every CTA's mass
+  if (!sh.owner) return;
+  const unsigned long long tgt = sh.target;
+  unsigned long long wex = 0;
+  for (int w = 0; w < warp; ++w) wex += sh.warp_mass[w];
+  if (!(wex <= tgt && tgt < wex + sh.warp_mass[warp])) return;
+  unsigned long long acc = wex;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const unsigned long long wi = i < w1 ? weight(row[i]) : 0ull;
+    unsigned long long incl = wi;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned int hit = __ballot_sync(0xffffffffu, acc + incl > tgt);
+    if (hit != 0u) {
+      if (lane == __ffs(hit) - 1) {
+        *out_token = i;
+        if (out_logprob != nullptr) *out_logprob = row[i] - log_z;
+      }
+      return;
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
 }
 
 // The general path over the whole row, by one CTA: top-k threshold key (0 for
@@ -518,91 +620,47 @@ __global__ void __launch_bounds__(kSampThreads, 1) k_sample(const float* __restr
   const float log_z = sh.log_z;
 
   int token = amax;
+  const bool topk_on = k > 0 && k < V;
   // no truncation (top-k off or >= V, top-p >= 1): the draw over the whole row
-  const bool full = !greedy && !(k > 0 && k < V) && !(p < 1.f);
-  bool general = !greedy && !fast && !full;
+  const bool full = !greedy && !topk_on && !(p < 1.f);
+  // top-p alone: a radix descent on mass over the cluster, then the draw
+  const bool topp = !greedy && !topk_on && p < 1.f;
+  bool general = !greedy && !fast && !full && !topp;
   if (full) {
-    // every warp owns a contiguous segment of this CTA's slice, so (rank,
-    // warp, lane) order is index order
+    draw_segmented(row, s0, s1, lmax, 1.f / t, 0u, uniform[b], C, rank, log_z, out_tokens + b,
+                   out_logprobs != nullptr ? out_logprobs + b : nullptr, sh);
+    return;
+  }
+  if (topp) {
+    // tau = the largest key whose mass of keys >= it reaches max(1, p * the
+    // row's mass), by 12, 12 and 8 bits of the key, the CTAs' mass histograms
+    // summed through distributed shared memory
     const float inv_t = 1.f / t;
-    const int seg = (s1 - s0 + kSampWarps - 1) / kSampWarps;
-    const int w0 = min(s1, s0 + warp * seg), w1 = min(s1, w0 + seg);
-    unsigned long long wm = 0;
-    for (int i0 = w0; i0 < w1; i0 += 32 * kUnroll) {
-      float x[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = i0 + u * 32 + lane;
-        x[u] = i < w1 ? __ldg(row + i) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (i0 + u * 32 + lane < w1) wm += fixed_weight(x[u], lmax, inv_t);
+    unsigned long long* mh = sh.hist;
+    uint32_t prefix = 0, mask = 0;
+    unsigned long long above = 0, need = 0;
+#pragma unroll 1
+    for (int level = 0; level < 3; ++level) {
+      const int bits = level < 2 ? 12 : 8;
+      const int shift = level == 0 ? 20 : (level == 1 ? 8 : 0);
+      const uint32_t nbm = (1u << bits) - 1u;
+      for (int i = threadIdx.x; i < kBinsMax; i += kSampThreads) mh[i] = 0;
+      __syncthreads();
+      for_range(row, s0, s1, [&](int, float x) {
+        const uint32_t key = order_key(x);
+        if ((key & mask) == prefix) atomicAdd(&mh[(key >> shift) & nbm], fixed_weight(x, lmax, inv_t));
+      });
+      __syncthreads();
+      cluster_sync();  // every CTA's histogram is complete
+      select_bin(mh, bits, above, need, C, sh, level == 0 ? p : -1.f);
+      cluster_sync();  // the cluster has read every histogram
+      if (level == 0) need = sh.need;
+      prefix |= sh.digit << shift;
+      mask |= nbm << shift;
+      above = sh.acc;
     }
-    wm = warp_sum(wm);
-    if (lane == 0) sh.warp_mass[warp] = wm;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long m = 0;
-      for (int w = 0; w < kSampWarps; ++w) m += sh.warp_mass[w];
-      sh.part_mass = m;
-    }
-    cluster_sync();  // every CTA's mass is complete
-    if (warp == 0) {  // lane r reads CTA r's mass
-      const uint32_t addr = smem_u32(&sh.part_mass);
-      unsigned long long m = 0;
-      if (lane < static_cast<int>(C)) {
-        const uint2 v = ld_cluster_u32x2(mapa_shared(addr, static_cast<uint32_t>(lane)));
-        m = (static_cast<unsigned long long>(v.y) << 32) | v.x;
-      }
-      unsigned long long incl = m;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
-      const unsigned long long excl = __shfl_sync(0xffffffffu, incl - m, static_cast<int>(rank));
-      const unsigned long long mine = __shfl_sync(0xffffffffu, m, static_cast<int>(rank));
-      float u = uniform[b];
-      u = u > 0.f ? (u < 1.f ? u : 0.99999994f) : 0.f;
-      const unsigned long long target =
-          static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(total));
-      if (lane == 0) {
-        sh.owner = excl <= target && target < excl + mine ? 1 : 0;
-        sh.target = target - excl;
-      }
-    }
-    __syncthreads();
-    cluster_sync();  // the cluster has read every CTA's mass; CTAs may leave
-    if (!sh.owner) return;
-    // the warp whose segment holds the draw scans it 32 elements at a time
-    const unsigned long long tgt = sh.target;
-    unsigned long long wex = 0;
-    for (int w = 0; w < warp; ++w) wex += sh.warp_mass[w];
-    if (wex <= tgt && tgt < wex + sh.warp_mass[warp]) {
-      unsigned long long acc = wex;
-      for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const unsigned long long wi = i < w1 ? fixed_weight(row[i], lmax, inv_t) : 0ull;
-        unsigned long long incl = wi;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const unsigned int hit = __ballot_sync(0xffffffffu, acc + incl > tgt);
-        if (hit != 0u) {
-          const int first = __ffs(hit) - 1;
-          if (lane == first) {
-            out_tokens[b] = i;
-            if (out_logprobs != nullptr) out_logprobs[b] = row[i] - log_z;
-          }
-          break;
-        }
-        acc += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
+    draw_segmented(row, s0, s1, lmax, inv_t, prefix, uniform[b], C, rank, log_z, out_tokens + b,
+                   out_logprobs != nullptr ? out_logprobs + b : nullptr, sh);
     return;
   }
   if (fast) {
