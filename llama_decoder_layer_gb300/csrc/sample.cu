@@ -20,7 +20,9 @@
 // Rows without truncation (top-k off, top-p >= 1): after the first pass, each
 // warp sums the weights of a contiguous segment of its CTA's slice, the cluster
 // exchanges its CTAs' sums, and the warp whose segment holds the draw finds
-// the token with 32-wide scans.
+// the token with 32-wide scans.  Top-p without top-k: a radix descent on mass
+// (histograms summed over the cluster) gives the threshold, then the same
+// draw over the keys above it.
 //
 // Top-k rows with k <= 1024 (the fast path): one pass gives the row maximum,
 // its index, the log-normaliser (an online sum) and a histogram of the keys'
@@ -29,10 +31,9 @@
 // number at most 1024, one more pass gathers them (else the next 12 and 8
 // bits refine the bin first), and the k-th largest key, the top-p threshold
 // and the inverse-CDF draw are taken exactly over those candidates.  Other
-// rows (top-p without top-k, k > 1024, or more than 1024 keys tied at the
-// k-th value) take the general path in the cluster's first CTA: a radix
-// select on counts for top-k and a radix descent on mass for top-p over the
-// whole row.
+// rows (k > 1024, or more than 1024 keys tied at the k-th value) take the
+// general path in the cluster's first CTA: a radix select on counts for top-k
+// and a radix descent on mass for top-p over the whole row.
 //
 // Sources: [LLAMA-70B] "LLama — DeepSeek-R1-Distill-Llama-70B", Sampler
 // (sample(): greedy rows take the argmax; temperature scaling; the top-k /
