@@ -348,6 +348,14 @@ int llama_moe_layer_forward(const LlamaLayerConfig* cfg, const LlamaMoeConfig* m
                             int32_t* out_expert_ids, void* workspace, size_t workspace_bytes,
                             llama_stream_t stream);
 
+/* Self-test of the device-side failure path: launches one thread that waits
+ * on a shared-memory barrier nothing arrives at, with the same bounded wait
+ * every kernel uses (a 2 s wall-clock limit).  The wait gives up, the timeout
+ * is recorded in the device error word (detail 64), and the kernel returns, so
+ * the context stays usable: llama_get_device_error then reports
+ * LLAMA_ERR_TIMEOUT.  Returns the launch status. */
+int llama_selftest_wait_timeout(llama_stream_t stream);
+
 /* Synchronises `stream`, returns LLAMA_OK, LLAMA_ERR_DEVICE_GUARD or
  * LLAMA_ERR_TIMEOUT for the current device's error word, and clears it.
  * *detail (may be NULL) receives the code of the first place that reported. */

@@ -89,6 +89,7 @@ SIGNATURES = {
     "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
     "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "llama_fold_norm_weights": (_I, [_VP, _VP, _I, _I, _VP, _VP]),
+    "llama_selftest_wait_timeout": (_I, [_VP]),
     "llama_moe_layer_workspace_size": (_SZ, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), _I, _I, _I]),
     "llama_moe_layer_forward": (_I, [_P_CFG, ctypes.POINTER(LlamaMoeConfig), ctypes.POINTER(LlamaMoeLayerWeights),
                                      _P_B, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -382,6 +383,12 @@ def folded_layer_weights(weights: dict, stream=None) -> dict:
     w["ln1"] = None
     w["ln2"] = None
     return w
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launches the bounded-wait self-test (a wait that runs out after ~2 s);
+    llama_get_device_error then reports the timeout."""
+    _check(lib().llama_selftest_wait_timeout(_stream(stream)), "llama_selftest_wait_timeout")
 
 
 def launch_count() -> int:

@@ -631,6 +631,10 @@ int llama_fold_norm_weights(const void* norm_weight, const void* w, int rows, in
   return cuda_status(fold_norm_launch(norm_weight, w, rows, cols, w_folded, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int llama_selftest_wait_timeout(llama_stream_t stream) {
+  return cuda_status(selftest_wait_launch(device_error_word(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int llama_get_device_error(llama_stream_t stream, int* detail) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LLAMA_ERR_CUDA;
   int* w = device_error_word();

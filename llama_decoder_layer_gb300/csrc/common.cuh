@@ -34,6 +34,7 @@ enum : int {
   kWhereAttnDecode = 32,
   kWhereAttnPrefill = 33,
   kWhereMoe = 48,
+  kWhereSelftest = 64,
 };
 
 __device__ __forceinline__ void report_error(int* err, int flag, int where) {

@@ -69,6 +69,9 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
                        int rows, int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s,
                        float* inv_out = nullptr);
 
+// one CTA whose bounded wait on a barrier nothing arrives at runs out
+int selftest_wait_launch(int* err, cudaStream_t s);
+
 // w_folded[o, i] = bf16(w[o, i] * gamma[i]) for a [rows, cols] weight
 int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void* w_folded, cudaStream_t s);
 

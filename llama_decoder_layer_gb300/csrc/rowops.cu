@@ -134,6 +134,17 @@ __global__ void k_fold_norm(const uint4* __restrict__ gamma, const uint4* __rest
   }
 }
 
+// Self-test of the bounded wait: one thread waits on a shared-memory barrier
+// that nothing arrives at.  The wait gives up after its wall-clock limit and
+// the timeout is recorded in the error word, as in every kernel's waits.
+__global__ void k_selftest_wait(int* err) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  if (!mbar_wait(b, 0, nullptr)) report_error(err, kErrTimeout, kWhereSelftest);
+}
+
 // slot = block_table[b][pos / bs] * bs + pos % bs for every token; the
 // sequence b of token t is found by binary search in query_start_loc.
 __global__ void k_slot_mapping(const int32_t* __restrict__ positions, const int32_t* __restrict__ qsl,
@@ -275,6 +286,10 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
   if (per <= 4) return go(k_add_rmsnorm<4>);
   if (per <= 8) return go(k_add_rmsnorm<8>);
   return cudaErrorInvalidValue;
+}
+
+int selftest_wait_launch(int* err, cudaStream_t s) {
+  return launch_kernel(k_selftest_wait, dim3(1), dim3(1), 0, s, false, err);
 }
 
 int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void* w_folded, cudaStream_t s) {
