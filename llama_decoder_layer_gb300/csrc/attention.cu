@@ -703,11 +703,7 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // One CTA per (sequence, KV head, 128/G query tokens): the 128 MMA rows are
 // those tokens x the G q heads of the group (row r = token r/G, head r%G), so
 // every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
-// 64 columns) and the 64-key K tiles, warp 6 the V tiles (2-stage rings each,
-// in separate warps so that a K tile is requested as soon as its stage frees,
-// not behind the V stage before it: 2.31 -> 1.91 ms on 8 x 4096 tokens of
-// the 70B shape; two lanes of one warp waiting on the two rings were slower,
-// 3.00 ms, as each lane's barrier wait held up the other); one thread of warp 1 issues
+// 64 columns) and 128-key K/V tiles (2-stage ring); one thread of warp 1 issues
 // S = Q K^T into a double-buffered TMEM accumulator and O += P V into a TMEM
 // accumulator (V is the MN-major B operand); warps 2-5 (one row each) read
 // each S tile from TMEM once, write P as bf16 pairs back over the first half
@@ -717,18 +713,13 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // pipe: S buffer j%2 is next written by S of tile j+2, which the MMA warp
 // issues after P V of tile j.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 224;  // warp 0 Q/K loads, 1 MMA, 2-5 softmax, 6 V loads
-constexpr int kTcWarpV = 6;
+constexpr int kTcThreads = 192;
 constexpr int kTcKeys = 64;                        // keys per K/V tile
 constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-column halves)
 constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
 constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
 constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
-// ring depths: a third K or V stage (115 KB per CTA) measured slower, 2.01 and
-// 1.97 ms against 1.91 on 8 x 4096 tokens of the 70B shape
-constexpr int kTcKStages = 2;                      // K ring depth
-constexpr int kTcVStages = 2;                      // V ring depth
-constexpr int kTcSmem = 2 * kTcQHalf + (kTcKStages + kTcVStages) * kTcTileBytes + 256 + kTcSlack;
+constexpr int kTcSmem = 2 * kTcQHalf + 2 * 2 * kTcTileBytes + 256 + kTcSlack;
 constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
 
 __global__ void __launch_bounds__(kTcThreads, 2)
@@ -746,19 +737,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t q_s = sb;                                   // Q: two 64-column halves
-  auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * kTcTileBytes; };
-  auto v_s = [&](int st) { return sb + 2u * kTcQHalf + (kTcKStages + st) * kTcTileBytes; };
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + (kTcKStages + kTcVStages) * kTcTileBytes);
+  auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes; };
+  auto v_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes + kTcTileBytes; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + 4 * kTcTileBytes);
   const uint32_t bar0 = smem_u32(bars);
-  // K and V have their own rings: a K stage is free as soon as its S = Q K^T
-  // is done, so the next K tile is fetched while P V still runs
-  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = k_full0 + 8 * kTcKStages,
-                 v_full0 = k_empty0 + 8 * kTcKStages, v_empty0 = v_full0 + 8 * kTcVStages,
-                 s_full0 = v_empty0 + 8 * kTcVStages, p_full = s_full0 + 16, o_done = p_full + 8,
-                 drain = o_done + 8;
-  constexpr int kTcBars = 1 + 2 * kTcKStages + 2 * kTcVStages + 2 + 3;
-  static_assert(kTcBars * 8 + 16 <= 256, "barrier area");
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kTcBars);
+  // K and V have their own 2-stage rings: a K stage is free as soon as its
+  // S = Q K^T is done, so the next K tile is fetched while P V still runs
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
+                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full = bar0 + 88, o_done = bar0 + 96,
+                 drain = bar0 + 104;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
   int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
@@ -797,15 +785,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kTcKStages; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(k_full0 + 8 * i, 1);
       mbar_init(k_empty0 + 8 * i, 1);
-    }
-    for (int i = 0; i < kTcVStages; ++i) {
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(v_empty0 + 8 * i, 1);
+      mbar_init(s_full0 + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(s_full0 + 8 * i, 1);
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -821,21 +807,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and kTcKeys, O at 2 * kTcKeys
 
-  if (warp == 0 || warp == kTcWarpV) {
-    // ---------------- TMA producers: warp 0 Q and K, the last warp V ----------------
-    // (separate warps, so a K tile is requested as soon as its stage is free
-    // instead of waiting behind the previous V stage)
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
     bool ok = true;
-    uint32_t uses[kTcKStages > kTcVStages ? kTcKStages : kTcVStages] = {};
+    uint32_t k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
     if (lane == 0) {
-      const bool is_k = warp == 0;
-      const int stages = is_k ? kTcKStages : kTcVStages;
       const uint64_t pol = policy_evict_normal();
-      if (is_k) {
-        mbar_arrive_expect_tx(q_full, 32768);
-        tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
-        tma_load_3d(q_s + kTcQHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
-      }
+      mbar_arrive_expect_tx(q_full, 32768);
+      tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
+      tma_load_3d(q_s + kTcQHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
       const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
       auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int j) {
         mbar_arrive_expect_tx(bar, kTcTileBytes);
@@ -852,28 +832,31 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           tma_load_2d(dst + kTcHalf + i * 2048, tm, bar, 64, row, pol);
         }
       };
-      const uint32_t empty0 = is_k ? k_empty0 : v_empty0, full0 = is_k ? k_full0 : v_full0;
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j % stages;
-        const uint32_t par = ((j / stages) & 1) ^ 1;
-        if (!mbar_wait(empty0 + 8 * st, par, abort_flag)) {
+        const int st = j & 1;
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        if (!mbar_wait(k_empty0 + 8 * st, par, abort_flag)) {
           ok = false;
           break;
         }
-        if (is_k)
-          load_tile(&tmK, k_s(st), full0 + 8 * st, j);
-        else
-          load_tile(&tmV, v_s(st), full0 + 8 * st, j);
-        uses[st]++;
+        load_tile(&tmK, k_s(st), k_full0 + 8 * st, j);
+        k_uses[st]++;
+        if (!mbar_wait(v_empty0 + 8 * st, par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        load_tile(&tmV, v_s(st), v_full0 + 8 * st, j);
+        v_uses[st]++;
       }
       if (!ok) {
         report_error(p.err, kErrTimeout, kWhereAttnPrefill);
         *abort_flag = 1;
       }
-      // wait for every load this thread issued to land before the CTA can exit
-      if (is_k) mbar_wait(q_full, 0, nullptr);
-      for (int st = 0; st < stages; ++st)
-        if (uses[st] > 0) mbar_wait(full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
+      mbar_wait(q_full, 0, nullptr);
+      for (int st = 0; st < 2; ++st) {
+        if (k_uses[st] > 0) mbar_wait(k_full0 + 8 * st, (k_uses[st] - 1) & 1u, nullptr);
+        if (v_uses[st] > 0) mbar_wait(v_full0 + 8 * st, (v_uses[st] - 1) & 1u, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -883,9 +866,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     bool ok = mbar_wait(q_full, 0, abort_flag);
     bool issued = false;
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;            // S buffer
-      const int kst = j % kTcKStages;  // K stage
-      if (!mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) return false;
+      const int st = j & 1;
+      if (!mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t d = tmem + st * kTcKeys;
@@ -893,10 +875,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
           const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(kst) + ck), idS, kk > 0 ? 1u : 0u);
+          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(st) + ck), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full0 + 8 * st);
-        tc_commit(k_empty0 + 8 * kst);
+        tc_commit(k_empty0 + 8 * st);
         issued = true;
       }
       __syncwarp();
@@ -908,9 +890,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ok = false;
         break;
       }
-      const int vst = j % kTcVStages;
-      if (!mbar_wait(p_full, j & 1, abort_flag) ||
-          !mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
+      if (!mbar_wait(p_full, j & 1, abort_flag) || !mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -919,10 +899,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int st = j & 1;
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
-          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(vst) + ks * 2048, kTcHalf, 1024);
+          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(st) + ks * 2048, kTcHalf, 1024);
           tc_mma_f16_ts(tmem + 2 * kTcKeys, tmem + st * kTcKeys + ks * 8, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(v_empty0 + 8 * vst);
+        tc_commit(v_empty0 + 8 * st);
         tc_commit(o_done);
       }
       __syncwarp();
@@ -1037,19 +1017,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // (P is zero there, but stale cache contents must not reach the MMA),
       // once the tile's V load has landed
       if (j == ntiles - 1) {
-        const int vst = j % kTcVStages;
-        if (!mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
+        if (!mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         const int valid = n_keys - kbase;
-        uint8_t* vg = smem + (v_s(vst) - sb);
+        uint8_t* vg = smem + (v_s(st) - sb);
         for (int i = threadIdx.x - 64; i < (kTcKeys - valid) * 2 * 8; i += 128) {
           const int rowv = valid + i / 16, hf = (i / 8) & 1, c16 = i & 7;
           *reinterpret_cast<uint4*>(vg + hf * kTcHalf + rowv * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();  // the zeroed rows, before P V reads them
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
