@@ -111,3 +111,46 @@ def test_sampler_host_argument_checks(lib):
     assert lib.llama_sample(fake, 4, 0, fake, fake, fake, fake, fake, None, None) == lb.LLAMA_ERR_ARG
     assert lib.llama_sample(fake, 4, 10, fake, None, fake, fake, fake, None, None) == lb.LLAMA_ERR_ARG
     assert lib.llama_sample(fake, 4, 10, fake, fake, fake, None, fake, None, None) == lb.LLAMA_ERR_ARG
+
+
+def test_moe_host_argument_checks(lib):
+    # rejected on the host, before anything touches the (fake) device pointers
+    fake = ctypes.c_void_p(256)
+    MC = lb.LlamaMoeConfig
+    good = MC(2048, 128, 8, 768)
+    assert lib.llama_moe_workspace_size(ctypes.byref(good), 64) > 0
+    assert lib.llama_moe_workspace_size(None, 64) == 0
+    assert lib.llama_moe_workspace_size(ctypes.byref(MC(2048, 8, 9, 768)), 64) == 0  # top_k > experts
+    assert lib.llama_moe_workspace_size(ctypes.byref(good), -1) == 0
+    args = (fake, fake, fake, fake, fake, None, None, fake, 1 << 30, None)
+    assert lib.llama_moe_forward(None, fake, 4, *args[1:]) == lb.LLAMA_ERR_ARG
+    assert lib.llama_moe_forward(ctypes.byref(MC(2048, 128, 0, 768)), fake, 4, *args[1:]) == lb.LLAMA_ERR_ARG
+    assert lib.llama_moe_forward(ctypes.byref(MC(2044, 128, 8, 768)), fake, 4, *args[1:]) == lb.LLAMA_ERR_UNSUPPORTED
+    assert lib.llama_moe_forward(ctypes.byref(MC(2048, 600, 8, 768)), fake, 4, *args[1:]) == lb.LLAMA_ERR_UNSUPPORTED
+    assert lib.llama_moe_forward(ctypes.byref(good), fake, 0, *args[1:]) == lb.LLAMA_OK  # no tokens
+    assert lib.llama_moe_forward(ctypes.byref(good), fake, -1, *args[1:]) == lb.LLAMA_ERR_ARG
+    assert lib.llama_moe_forward(ctypes.byref(good), None, 4, *args[1:]) == lb.LLAMA_ERR_ARG
+    # too small a workspace
+    assert lib.llama_moe_forward(ctypes.byref(good), fake, 4, fake, fake, fake, fake, None, None, fake, 16,
+                                 None) == lb.LLAMA_ERR_WORKSPACE
+
+
+def test_moe_layer_host_argument_checks(lib):
+    fake = 256
+    cfg = lb.LayerConfig(2048, 32, 4, 128, 6144, 1e-6, 1e7).c()
+    good = lb.LlamaMoeConfig(2048, 128, 8, 768)
+    assert lib.llama_moe_layer_workspace_size(ctypes.byref(cfg), ctypes.byref(good), 64, 64, 4096) > 0
+    # the block's hidden size must be the layer's
+    other = lb.LlamaMoeConfig(1024, 128, 8, 768)
+    assert lib.llama_moe_layer_workspace_size(ctypes.byref(cfg), ctypes.byref(other), 64, 64, 4096) == 0
+    w = lb.LlamaMoeLayerWeights(fake, fake, fake, fake, fake, fake, fake)
+    assert lib.llama_moe_layer_forward(ctypes.byref(cfg), ctypes.byref(other), ctypes.byref(w), None, None, None,
+                                       None, None, None, None, None, 0, None) == lb.LLAMA_ERR_ARG
+    # a missing expert weight
+    w_bad = lb.LlamaMoeLayerWeights(fake, fake, fake, fake, fake, None, fake)
+    assert lib.llama_moe_layer_forward(ctypes.byref(cfg), ctypes.byref(good), ctypes.byref(w_bad), None, None, None,
+                                       None, None, None, None, None, 0, None) == lb.LLAMA_ERR_ARG
+    # the MoE layer needs its norm weights (no folded form)
+    w_fold = lb.LlamaMoeLayerWeights(None, fake, fake, None, fake, fake, fake)
+    assert lib.llama_moe_layer_forward(ctypes.byref(cfg), ctypes.byref(good), ctypes.byref(w_fold), None, None, None,
+                                       None, None, None, None, None, 0, None) == lb.LLAMA_ERR_ARG
