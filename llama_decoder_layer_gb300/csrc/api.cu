@@ -524,7 +524,6 @@ int llama_sample(const float* logits, int rows, int vocab, const float* temperat
   if (rows == 0) return LLAMA_OK;
   if (!logits || !temperature || !top_k || !top_p || !uniform || !out_tokens) return LLAMA_ERR_ARG;
   if (static_cast<long long>(rows) * vocab > 0x7fffffffffffLL) return LLAMA_ERR_ARG;
-  if (rows > 0x7fffffff) return LLAMA_ERR_UNSUPPORTED;
   return cuda_status(sample_launch(logits, rows, vocab, temperature, top_k, top_p, uniform, out_tokens, out_logprobs,
                                    false, reinterpret_cast<cudaStream_t>(stream)));
 }
