@@ -1033,7 +1033,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && !mbar_wait(o_done, (ntiles - 1) & 1, abort_flag)) ok = false;
+    // every MMA of the CTA has completed before O is read: the drain barrier,
+    // committed once after the last P V, completes exactly once.  (o_done,
+    // committed after every P V and waited on by parity, cannot say so: a warp
+    // that finished the last tile may find P V of the tile before it still
+    // pending, a phase whose parity differs from the last one's.)
+    if (ok && !mbar_wait(drain, 0, abort_flag)) ok = false;
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
       *abort_flag = 1;
