@@ -743,10 +743,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t bar0 = smem_u32(bars);
   // K and V have their own 2-stage rings: a K stage is free as soon as its
   // S = Q K^T is done, so the next K tile is fetched while P V still runs
+  // P ready: one barrier per S buffer.  With one barrier for every tile a
+  // softmax warp that finished tile j could run through tile j+1 (its S is
+  // already there) and arrive again before a slower warp arrived for tile j,
+  // completing tile j's phase while part of P(j) was still being written.  A
+  // warp cannot reach tile j+2 before P V of tile j is issued, so the arrivals
+  // at p_full0 + 8 * (j % 2) all belong to tile j.
   const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
-                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full = bar0 + 88, o_done = bar0 + 96,
-                 drain = bar0 + 104;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full0 = bar0 + 88, o_done = bar0 + 104,
+                 drain = bar0 + 112;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
   int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
@@ -792,7 +798,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
     }
-    mbar_init(p_full, 4);
+    for (int i = 0; i < 2; ++i) mbar_init(p_full0 + 8 * i, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -890,7 +896,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         ok = false;
         break;
       }
-      if (!mbar_wait(p_full, j & 1, abort_flag) || !mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag)) {
+      if (!mbar_wait(p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag) ||
+          !mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -1031,7 +1038,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full0 + 8 * st);
     }
     // every MMA of the CTA has completed before O is read: the drain barrier,
     // committed once after the last P V, completes exactly once.  (o_done,
