@@ -12,6 +12,7 @@
 //   -> argmax.
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -310,14 +311,14 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
 std::atomic<unsigned long long> g_launch_count{0};
 
 int num_sms() {
-  static int sms[kMaxDevices] = {};
+  static std::atomic<int> sms[kMaxDevices];  // zero-initialised (static storage); filled once per device
   const int d = current_device();
-  if (sms[d] == 0) {
-    int v = 0;
+  int v = sms[d].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 1;
-    sms[d] = v;
+    sms[d].store(v, std::memory_order_relaxed);
   }
-  return sms[d];
+  return v;
 }
 
 }  // namespace llama
