@@ -703,15 +703,18 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // One CTA per (sequence, KV head, 128/G query tokens): the 128 MMA rows are
 // those tokens x the G q heads of the group (row r = token r/G, head r%G), so
 // every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
-// 64 columns) and 128-key K/V tiles (2-stage ring); one thread of warp 1 issues
-// S = Q K^T into a double-buffered TMEM accumulator and O += P V into a TMEM
-// accumulator (V is the MN-major B operand); warps 2-5 (one row each) read
-// each S tile from TMEM once, write P as bf16 pairs back over the first half
-// of that S buffer (tcgen05.st), and rescale O in TMEM only when a row's
-// running max grows by more than 2^8.  P V takes its A operand from tensor
-// memory, so the softmax of tile j+1 runs while P V of tile j is in the tensor
-// pipe: S buffer j%2 is next written by S of tile j+2, which the MMA warp
-// issues after P V of tile j.
+// 64 columns) and 64-key K and V tiles (a 2-stage ring each); one thread of
+// warp 1 issues S = Q K^T into a double-buffered TMEM accumulator and
+// O += P V into a TMEM accumulator (V is the MN-major B operand); warps 2-5
+// (one row each) read each S tile from TMEM once, write P as bf16 pairs back
+// over the first half of that S buffer (tcgen05.st), and rescale O in TMEM
+// only when a row's running max grows by more than 2^8.  P V takes its A
+// operand from tensor memory, so the softmax of tile j+1 runs while P V of
+// tile j is in the tensor pipe: S buffer j%2 is next written by S of tile
+// j+2, which the MMA warp issues after P V of tile j.  Each S buffer has its
+// own P-ready barrier, and O is read after the once-only drain barrier: the
+// softmax warps may drift a tile apart, and a single P-ready barrier or a
+// parity wait on the per-tile P V barrier would then mix up tiles.
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 192;
 constexpr int kTcKeys = 64;                        // keys per K/V tile
