@@ -25,6 +25,10 @@
 //     share of (tile, k-block) units, partial tiles in a workspace, and
 //     k_gemm_fixup summing them in CTA order (deterministic) spread over many
 //     CTAs.
+// Grouped mode (the experts of an MoE block): k_gemm_tc walks a tile list
+// built on the device, each entry naming its A rows, its expert's B rows and
+// how many of its rows are valid.  A row scale (an RMSNorm's rsqrt, its
+// weights folded into B) may multiply the product before any epilogue.
 // The kernels wait for the previous kernel of the call (pdl_wait) only where
 // they first need its results; the weight tiles of their first stages are
 // requested before that.

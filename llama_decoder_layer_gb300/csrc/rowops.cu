@@ -1,6 +1,8 @@
-// Row-wise and indexing kernels: fused residual-add + RMSNorm, cache slot
-// mapping, the standalone paged-cache write, the embedding gather and the
-// greedy argmax.  All are HBM-bound: 16-byte vector loads/stores, fp32
+// Row-wise and indexing kernels: fused residual-add + RMSNorm (or, with the
+// norm folded into the next projection, the add and each row's rsqrt), the
+// folding of norm weights into a projection, cache slot mapping, the
+// standalone paged-cache write, the embedding gather, the greedy argmax and
+// the self-test of the bounded wait.  All are HBM-bound: 16-byte vector loads/stores, fp32
 // arithmetic, warp-shuffle reductions.  They wait for the kernel before them
 // (pdl_wait) but do not trigger the next one early: a norm over thousands of
 // rows that let the following GEMM in early made the 70B prefill layer ~8%
