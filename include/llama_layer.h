@@ -9,7 +9,13 @@
  * for one Llama decoder layer (llama_layer_forward), for a stack of layers
  * followed by the final norm, lm_head and greedy sampling
  * (llama_stack_forward), and the paged KV-cache write on its own
- * (kv_cache_write).
+ * (kv_cache_write).  Past that path: the building blocks on their own
+ * (llama_linear, llama_gate_up_silu, llama_fused_add_rmsnorm,
+ * llama_paged_attention), sampling with temperature, top-k and top-p
+ * (llama_sample), the Qwen3-MoE sparse block and decoder layer
+ * (llama_moe_forward, llama_moe_layer_forward), norm weights folded into the
+ * projections (llama_fold_norm_weights) and a self-test of the device-side
+ * failure path (llama_selftest_wait_timeout).
  *
  * Sources (three web pages on vLLM's llama.py), cited by tag:
  *   [LLAMA-70B]    "LLama - DeepSeek-R1-Distill-Llama-70B" (hotelren.com
@@ -50,8 +56,11 @@
  *     recorded in a device error word and the access is skipped; a wait that
  *     runs past its limit (2 s) is recorded and the kernel winds down.
  *     llama_get_device_error() reports and clears the word.
- *   - The library keeps no other state than that error word (one per device)
- *     and cached kernel attributes.
+ *   - The library keeps no other state than that error word (one per device),
+ *     cached kernel attributes and SM counts, one non-blocking side stream
+ *     per device (decode attention beside prefill attention in mixed
+ *     batches), a fork/join event pair per host thread and device, a launch
+ *     counter, and the fixed scratch array of llama_paged_attention_noalloc.
  */
 #ifndef LLAMA_LAYER_H_
 #define LLAMA_LAYER_H_
