@@ -10,6 +10,10 @@
 //   embedding gather -> layers with the residual threaded (None at layer 0)
 //   -> final fused add+RMSNorm of each sequence's last token -> lm_head GEMM
 //   -> argmax.
+// Qwen3-MoE layer ([LLAMA-70B] Qwen3MoeSparseMoeBlock): the layer sequence up
+// to the post-attention norm, then the sparse MoE block in place of gate_up
+// and down.  With folded norms (null norm weights) the norm kernels write each
+// row's rsqrt and the qkv and gate_up GEMMs scale their rows by it.
 #include <stdint.h>
 
 #include <atomic>
