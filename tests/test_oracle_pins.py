@@ -648,3 +648,23 @@ def test_golden_config_matches_workloads():
         for k_, v_ in g["rope_scaling"].items():
             assert sc[k_] == v_
     assert SPECS["stack_70b"].vocab == g["vocab_size"]
+
+
+def test_golden_qwen3_moe_config_matches_workloads():
+    """Values printed on the 70B page's Qwen3MoeForCausalLM section against the
+    MoE workload definitions (every layer sparse, no rope scaling)."""
+    from llama_decoder_layer_gb300.inputs import SPECS
+    with open(os.path.join(GOLDEN, "qwen3_30b_a3b_config.json")) as f:
+        g = json.load(f)
+    assert g["num_attention_heads"] * g["head_dim"] == g["q_size"] == 4096
+    assert g["num_key_value_heads"] * g["head_dim"] == g["kv_size"] == 512
+    assert g["decoder_sparse_step"] == 1 and g["mlp_only_layers"] == [] and g["norm_topk_prob"] is True
+    for name in ("qwen3_moe", "qwen3_moe_decode", "qwen3_moe_prefill"):
+        sp = SPECS[name]
+        assert sp.hidden == g["hidden_size"] and sp.intermediate == g["intermediate_size"]
+        assert sp.n_heads == g["num_attention_heads"] and sp.n_kv_heads == g["num_key_value_heads"]
+        assert sp.head_dim == g["head_dim"] and sp.rms_eps == g["rms_norm_eps"]
+        assert sp.rope_theta == g["rope_theta"] and sp.rope_scaling is None and g["rope_scaling"] is None
+        assert sp.extra["num_experts"] == g["num_experts"]
+        assert sp.extra["top_k"] == g["num_experts_per_tok"]
+        assert sp.extra["moe_intermediate"] == g["moe_intermediate_size"]
