@@ -123,16 +123,21 @@ def test_fold_norm_weights_is_the_rounded_product():
 
 
 def test_stack_70b_subset_tokens_and_logits():
-    """The 8-layer stack, pinned in three parts:
+    """The 8-layer stack, pinned in four parts:
     (a) the stack call equals the composition of its layer calls, the final
         norm and lm_head, bit for bit (caches, logits, tokens);
     (b) every layer matches the oracle given that layer's inputs (teacher
         forcing), on 4 seeded decode sequences and one prefill chunk;
-    (c) the head matches the oracle given the final hidden/residual rows:
-        logits within tolerance, greedy tokens where the top-2 gap > 0.05.
-    The free-running difference across the 8 layers is printed, not asserted:
-    two oracles that differ only in fp32 vs fp64 accumulation drift apart by
-    the same amount (bf16 module outputs through random-init layers)."""
+    (c) the head matches the oracle given the final hidden/residual rows of
+        all 34 sequences: logits within tolerance, greedy tokens identical
+        wherever the oracle's top-2 gap exceeds 0.05;
+    (d) free running, the oracle's own 8-layer pass over the sampled
+        sequences picks the GPU's greedy token wherever its top-2 gap
+        exceeds 0.05.
+    The free-running difference of hidden_states across the 8 layers is
+    printed, not held to the 2e-2 bar: two oracles that differ only in fp32
+    vs fp64 accumulation drift past that bar by depth 8
+    (tests/test_oracle_depth_drift.py)."""
     spec = I.SPECS["stack_70b"]
     seed = 0
     bl = I.make_batch(spec, seed, DEV)
@@ -200,18 +205,33 @@ def test_stack_70b_subset_tokens_and_logits():
         print(f"stack layer {l}: same-input rel err hidden {eh:.2e} residual {er:.2e} k {ek:.2e} v {ev:.2e}; "
               f"free-running hidden {rel_err(gpu_after[l][0], x_free):.2e}")
 
-    # (c) the head on the same inputs
-    lrows = O.last_token_rows(subs[0].batch.query_start_loc)
-    hf_ref, _ = O.fused_add_rms_norm(f32(hid)[subs[0].rows][lrows], f32(res)[subs[0].rows][lrows], f32(fn),
-                                     sh.rms_eps, np.float32, bf16_tensors=True)
-    ref_logits = O.linear(hf_ref, f32(lm), np.float32)
+    # (c) the head on the same inputs, all sequences
+    last_all = bl.query_start_loc[1:].long().cpu().numpy() - 1
+    hf_ref, _ = O.fused_add_rms_norm(f32(hid)[last_all], f32(res)[last_all], f32(fn), sh.rms_eps, np.float32,
+                                     bf16_tensors=True)
+    lm_f = f32(lm)
+    ref_logits = O.linear(hf_ref, lm_f, np.float32)
     ref_tok, gap = O.greedy_argmax(ref_logits)
-    e = assert_close(f32(logits)[sample], ref_logits, "logits")
-    g_tok = tokens.cpu().numpy()[sample]
+    e = assert_close(f32(logits), ref_logits, "logits (all rows)")
+    g_tok_all = tokens.cpu().numpy()
     decided = gap > 0.05
-    assert np.array_equal(g_tok[decided], ref_tok[decided]), f"greedy tokens differ: {g_tok} vs {ref_tok} gap {gap}"
-    assert np.array_equal(tokens.cpu().numpy(), np.argmax(f32(logits), axis=-1))
-    print(f"stack head: logits rel err {e:.2e}, tokens compared on {int(decided.sum())}/{len(sample)} rows")
+    assert np.array_equal(g_tok_all[decided], ref_tok[decided]), \
+        f"greedy tokens differ: {g_tok_all} vs {ref_tok} gap {gap}"
+    assert np.array_equal(g_tok_all, np.argmax(f32(logits), axis=-1))
+    print(f"stack head: logits rel err {e:.2e} on {B} rows, tokens compared on {int(decided.sum())}/{B} rows")
+
+    # (d) free running: the oracle's own pass through all 8 layers and the head
+    lrows = O.last_token_rows(subs[0].batch.query_start_loc)
+    hf_free, _ = O.fused_add_rms_norm(x_free[lrows], r_free[lrows], f32(fn), sh.rms_eps, np.float32,
+                                      bf16_tensors=True)
+    free_logits = O.linear(hf_free, lm_f, np.float32)
+    free_tok, free_gap = O.greedy_argmax(free_logits)
+    g_tok = g_tok_all[sample]
+    free_decided = free_gap > 0.05
+    print(f"stack free running: logits rel err {rel_err(f32(logits)[sample], free_logits):.2e}, gaps "
+          f"{np.round(free_gap, 3).tolist()}, tokens gpu {g_tok.tolist()} oracle {free_tok.tolist()}")
+    assert np.array_equal(g_tok[free_decided], free_tok[free_decided]), \
+        f"free-running greedy tokens differ: {g_tok} vs {free_tok} gap {free_gap}"
 
 
 def test_max_position_decode():
