@@ -264,9 +264,13 @@ int llama_paged_attention(const LlamaLayerConfig* cfg, const LlamaBatch* batch, 
  * bytes (32 MiB) inside the library.  Every GPU that loads the library holds it
  * until the process exits.  A batch whose scratch needs more than that
  * (num_seqs * ceil(ceil(max_seq_len/16)/96) * n_heads * (head_dim+2) * 4
- * + 4 * (ceil(num_tokens/8) + num_seqs) + 256 bytes) is rejected with
- * LLAMA_ERR_SCRATCH_LIMIT before anything is launched.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * + 4 * (ceil(num_tokens/8) + num_seqs) + 512 bytes) is rejected with
+ * LLAMA_ERR_SCRATCH_LIMIT before anything is launched; an invalid configuration
+ * or batch is rejected first, with the status llama_paged_attention gives it.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.  The
+ * address is kept for the life of the device's context: after cudaDeviceReset,
+ * do not call this entry point again on that device.
  * All calls share the one array, so calls that overlap on the GPU race on it:
  * the caller must serialise them.  Nothing in it has to start at zero.
  * Arguments and results are those of llama_paged_attention. */

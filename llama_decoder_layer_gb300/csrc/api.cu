@@ -312,6 +312,11 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
 
 }  // namespace
 
+int attention_args_status(const LlamaLayerConfig* cfg, const LlamaBatch* batch) {
+  const int st = check_cfg(cfg);
+  return st ? st : check_batch(batch, cfg);
+}
+
 std::atomic<unsigned long long> g_launch_count{0};
 
 int num_sms() {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "llama_layer.h"
+
 namespace llama {
 
 enum GemmEpilogue : int {
@@ -143,5 +145,9 @@ struct MoeArgs {
 int moe_launch(const MoeArgs& a, cudaStream_t s);
 
 int num_sms();
+
+// The configuration and batch checks every attention entry point makes
+// (LLAMA_OK or the status it would return), with nothing launched.
+int attention_args_status(const LlamaLayerConfig* cfg, const LlamaBatch* batch);
 
 }  // namespace llama
