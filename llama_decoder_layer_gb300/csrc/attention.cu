@@ -703,8 +703,10 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // One CTA per (sequence, KV head, 128/G query tokens): the 128 MMA rows are
 // those tokens x the G q heads of the group (row r = token r/G, head r%G), so
 // every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
-// 64 columns) and 64-key K and V tiles (a 2-stage ring each); one thread of
-// warp 1 issues S = Q K^T into a double-buffered TMEM accumulator and
+// 64 columns) and the 64-key K tiles, warp 6 the 64-key V tiles (a 2-stage
+// ring each, so the next K tile never waits behind a V stage that P V still
+// holds); one thread of warp 1 issues S = Q K^T into a double-buffered TMEM
+// accumulator and
 // O += P V into a TMEM accumulator (V is the MN-major B operand); warps 2-5
 // (one row each) read each S tile from TMEM once, write P as bf16 pairs back
 // over the first half of that S buffer (tcgen05.st), and rescale O in TMEM
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // softmax warps may drift a tile apart, and a single P-ready barrier or a
 // parity wait on the per-tile P V barrier would then mix up tiles.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;  // warp 0 Q + K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
 constexpr int kTcKeys = 64;                        // keys per K/V tile
 constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-column halves)
 constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
@@ -816,17 +818,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and kTcKeys, O at 2 * kTcKeys
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    bool ok = true;
-    uint32_t k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers: Q and K (warp 0), V (warp 6) ----------------
+    const bool is_k = warp == 0;
     if (lane == 0) {
+      bool ok = true;
+      uint32_t uses[2] = {0, 0};
       const uint64_t pol = policy_evict_normal();
-      mbar_arrive_expect_tx(q_full, 32768);
-      tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
-      tma_load_3d(q_s + kTcQHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, 32768);
+        tma_load_3d(q_s, &tmQ, q_full, 0, kvh * G, tq, pol);
+        tma_load_3d(q_s + kTcQHalf, &tmQ, q_full, 64, kvh * G, tq, pol);
+      }
       const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-      auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int j) {
+      const CUtensorMap* tm = is_k ? &tmK : &tmV;
+      const uint32_t full0 = is_k ? k_full0 : v_full0, empty0 = is_k ? k_empty0 : v_empty0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = is_k ? k_s(st) : v_s(st);
+        const uint32_t bar = full0 + 8 * st;
         mbar_arrive_expect_tx(bar, kTcTileBytes);
         for (int i = 0; i < kTcKeys / kBS; ++i) {
           const int jb = j * (kTcKeys / kBS) + i;
@@ -840,32 +854,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           tma_load_2d(dst + i * 2048, tm, bar, 0, row, pol);
           tma_load_2d(dst + kTcHalf + i * 2048, tm, bar, 64, row, pol);
         }
-      };
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t par = ((j >> 1) & 1) ^ 1;
-        if (!mbar_wait(k_empty0 + 8 * st, par, abort_flag)) {
-          ok = false;
-          break;
-        }
-        load_tile(&tmK, k_s(st), k_full0 + 8 * st, j);
-        k_uses[st]++;
-        if (!mbar_wait(v_empty0 + 8 * st, par, abort_flag)) {
-          ok = false;
-          break;
-        }
-        load_tile(&tmV, v_s(st), v_full0 + 8 * st, j);
-        v_uses[st]++;
+        uses[st]++;
       }
       if (!ok) {
         report_error(p.err, kErrTimeout, kWhereAttnPrefill);
         *abort_flag = 1;
       }
-      mbar_wait(q_full, 0, nullptr);
-      for (int st = 0; st < 2; ++st) {
-        if (k_uses[st] > 0) mbar_wait(k_full0 + 8 * st, (k_uses[st] - 1) & 1u, nullptr);
-        if (v_uses[st] > 0) mbar_wait(v_full0 + 8 * st, (v_uses[st] - 1) & 1u, nullptr);
-      }
+      // every load this thread issued lands before the CTA can exit
+      if (is_k) mbar_wait(q_full, 0, nullptr);
+      for (int st = 0; st < 2; ++st)
+        if (uses[st] > 0) mbar_wait(full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -925,7 +923,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncwarp();
     if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain, 0, nullptr);
   } else {
-    // ---------------- softmax warps: one row each ----------------
+    // ---------------- softmax warps (2-5): one row each ----------------
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const int tok = r / G, hq = r % G;

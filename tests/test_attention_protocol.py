@@ -24,6 +24,12 @@ It pins the reasoning behind the kernel's barriers:
   pending;
 * one P-ready barrier per S buffer and the final read after the once-only
   drain barrier are safe in every interleaving (and neither fix alone is).
+
+A second model adds the K and V shared-memory rings and their TMA producers
+(one thread for both, or one each as the kernel runs them), loads landing in
+any order: no stage is overwritten before the MMA that reads it completes, S
+and P V read the tiles they expect, and the V rows past the context are zeroed
+after V lands and before P V reads them.
 """
 
 from collections import deque
@@ -195,3 +201,242 @@ def test_parity_wait_for_the_last_p_v_can_pass_early():
 def test_single_tile_is_safe_either_way():
     assert explore(1, per_buffer_p=False, final_on_drain=False) == set()
     assert explore(1, per_buffer_p=True, final_on_drain=True) == set()
+
+
+# ---------------------------------------------------------------------------
+# The same protocol with the K and V rings and their TMA producers
+# ---------------------------------------------------------------------------
+
+
+def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
+    """Every interleaving of the kernel's protocol including the K and V
+    shared-memory rings (two stages each) and their producers.  K(j) and V(j)
+    go to stage j % 2; a producer waits for the stage's empty barrier (parity
+    ((j >> 1) & 1) ^ 1), issues the TMA load, and the load lands at any later
+    point, in any order with the other loads in flight, arriving at the
+    stage's full barrier.  The MMA thread waits for K(j)'s full barrier before
+    S(j) and frees the K stage by a commit after it; it waits for P(j) and
+    V(j) before P V(j) and frees the V stage by a commit after it.  On the last
+    tile the softmax warps wait for V's full barrier and zero the V rows past
+    the context before they arrive with P.
+
+    split_producers: K from one thread and V from another (the kernel), or
+    both from one thread in the order K(0), V(0), K(1), V(1), ...
+    mistake: plant one error to show the model catches it:
+      "no_v_empty_wait"  the V producer does not wait for the stage to be free
+      "k_freed_late"     the K stage is freed after P V instead of after S
+                         (safe, only slower: no violation expected)
+      "no_v_full_wait"   the MMA thread issues P V without waiting for V
+      "zero_before_load" the softmax warps zero V rows without waiting for V
+    Returns the set of violations seen."""
+    last = n_tiles - 1
+    mma = [("wait_k", 0), ("issue_s", 0)]
+    for j in range(n_tiles):
+        if j + 1 < n_tiles:
+            mma += [("wait_k", j + 1), ("issue_s", j + 1)]
+        mma += [("wait_p", j)]
+        if mistake != "no_v_full_wait":
+            mma += [("wait_v", j)]
+        mma += [("issue_pv", j)]
+    mma.append(("commit_drain", None))
+    soft = []
+    for j in range(n_tiles):
+        soft += [("wait_s", j)]
+        if j > 0:
+            soft += [("maybe_rescale", j), ("rescale", j)]
+        soft += [("write_p", j)]
+        if j == last:
+            if mistake != "zero_before_load":
+                soft += [("wait_v_last", j)]
+            soft += [("zero_v", j)]
+        soft += [("arrive_p", j)]
+    soft += [("wait_final", None), ("read_o", None)]
+
+    def prod(kinds):
+        out = []
+        for j in range(n_tiles):
+            for kind in kinds:
+                if not (kind == "V" and mistake == "no_v_empty_wait"):
+                    out.append(("wait_empty", (kind, j)))
+                out.append(("load", (kind, j)))
+        return out
+
+    producers = [prod("K"), prod("V")] if split_producers else [prod("KV")]
+
+    def fresh_barriers():
+        b = {"o_done": Barrier(1), "drain": Barrier(1)}
+        for i in range(2):
+            for name in ("s", "kf", "ke", "vf", "ve"):
+                b["%s%d" % (name, i)] = Barrier(1)
+            b["p%d" % i] = Barrier(warps)
+        return b
+
+    def clone_bars(bars):
+        out = {}
+        for k, v in bars.items():
+            c = Barrier(v.count)
+            c.pending, c.phase = v.pending, v.phase
+            out[k] = c
+        return out
+
+    # state: mma pc, warp pcs, producer pcs, pipe, barriers, loads in flight,
+    # K stage contents, V stage contents, P written, S done, P V done, V rows zeroed
+    start = (0, (0,) * warps, (0,) * len(producers), (), fresh_barriers(), frozenset(), (None, None), (None, None),
+             frozenset(), frozenset(), frozenset(), frozenset())
+
+    def key(st):
+        m, w, pp, pipe, bars, fl, ks, vs, wr, sd, pvd, zr = st
+        return (m, w, pp, pipe, tuple(sorted((k, v.key()) for k, v in bars.items())), fl, ks, vs, wr, sd, pvd, zr)
+
+    seen, queue, violations = set(), deque([start]), set()
+    while queue:
+        st = queue.popleft()
+        k = key(st)
+        if k in seen:
+            continue
+        seen.add(k)
+        mpc, wpcs, ppcs, pipe, bars, flight, kst, vst, written, s_done, pv_done, zeroed = st
+        nexts = []
+
+        def with_(**kw):
+            d = dict(mpc=mpc, wpcs=wpcs, ppcs=ppcs, pipe=pipe, bars=bars, flight=flight, kst=kst, vst=vst,
+                     written=written, s_done=s_done, pv_done=pv_done, zeroed=zeroed)
+            d.update(kw)
+            return (d["mpc"], d["wpcs"], d["ppcs"], d["pipe"], d["bars"], d["flight"], d["kst"], d["vst"],
+                    d["written"], d["s_done"], d["pv_done"], d["zeroed"])
+
+        # the producers
+        for i, prog in enumerate(producers):
+            pc = ppcs[i]
+            if pc >= len(prog):
+                continue
+            kind, (kv, j) = prog[pc]
+            adv = ppcs[:i] + (pc + 1,) + ppcs[i + 1:]
+            e = ("ke%d" if kv == "K" else "ve%d") % (j & 1)
+            if kind == "wait_empty":
+                if bars[e].passed(((j >> 1) & 1) ^ 1):
+                    nexts.append(with_(ppcs=adv))
+            else:
+                nexts.append(with_(ppcs=adv, flight=flight | {(kv, j)}))
+        # a load in flight lands (any of them)
+        for (kv, j) in flight:
+            s = j & 1
+            nb = clone_bars(bars)
+            nb[("kf%d" if kv == "K" else "vf%d") % s].arrive()
+            if kv == "K":
+                if j >= 2 and (j - 2) not in s_done:
+                    violations.add("K load overwrites a tile S has not read")
+                nexts.append(with_(bars=nb, flight=flight - {(kv, j)}, kst=kst[:s] + (j,) + kst[s + 1:]))
+            else:
+                if j >= 2 and (j - 2) not in pv_done:
+                    violations.add("V load overwrites a tile P V has not read")
+                if j == last and zeroed:
+                    violations.add("V load lands over the zeroed rows")
+                nexts.append(with_(bars=nb, flight=flight - {(kv, j)}, vst=vst[:s] + (j,) + vst[s + 1:]))
+        # the MMA thread
+        if mpc < len(mma):
+            kind, j = mma[mpc]
+            s = (j or 0) & 1
+            if kind == "wait_k":
+                if bars["kf%d" % s].passed((j >> 1) & 1):
+                    nexts.append(with_(mpc=mpc + 1))
+            elif kind == "issue_s":
+                free_k = () if mistake == "k_freed_late" else (("commit", "ke%d" % s),)
+                nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("S", j), ("commit", "s%d" % s)) + free_k))
+            elif kind == "wait_p":
+                if bars["p%d" % s].passed((j >> 1) & 1):
+                    nexts.append(with_(mpc=mpc + 1))
+            elif kind == "wait_v":
+                if bars["vf%d" % s].passed((j >> 1) & 1):
+                    nexts.append(with_(mpc=mpc + 1))
+            elif kind == "issue_pv":
+                free_k = (("commit", "ke%d" % s),) if mistake == "k_freed_late" else ()
+                nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("PV", j), ("commit", "ve%d" % s), ("commit", "o_done"))
+                                   + free_k))
+            elif kind == "commit_drain":
+                nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("commit", "drain"),)))
+        # the tensor pipe completes its oldest operation
+        if pipe:
+            op, arg = pipe[0]
+            if op == "S":
+                if kst[arg & 1] != arg or any(f == ("K", arg) for f in flight):
+                    violations.add("S reads a K stage that does not hold its tile")
+                nexts.append(with_(pipe=pipe[1:], s_done=s_done | {arg}))
+            elif op == "PV":
+                if any((arg, w) not in written for w in range(warps)):
+                    violations.add("P V reads an incomplete P")
+                if vst[arg & 1] != arg:
+                    violations.add("P V reads a V stage that does not hold its tile")
+                if arg == last and len(zeroed) != warps:
+                    violations.add("P V reads V rows that are not zeroed")
+                nexts.append(with_(pipe=pipe[1:], pv_done=pv_done | {arg}))
+            else:
+                nb = clone_bars(bars)
+                nb[arg].arrive()
+                nexts.append(with_(pipe=pipe[1:], bars=nb))
+        # the softmax warps
+        for w in range(warps):
+            pc = wpcs[w]
+            if pc >= len(soft):
+                continue
+            kind, j = soft[pc]
+            adv = wpcs[:w] + (pc + 1,) + wpcs[w + 1:]
+            if kind == "wait_s":
+                if bars["s%d" % (j & 1)].passed((j >> 1) & 1):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "maybe_rescale":
+                nexts.append(with_(wpcs=adv))
+                nexts.append(with_(wpcs=wpcs[:w] + (pc + 2,) + wpcs[w + 1:]))
+            elif kind == "rescale":
+                if bars["o_done"].passed((j - 1) & 1):
+                    if (j - 1) not in pv_done:
+                        violations.add("O rescaled before P V(j-1)")
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "write_p":
+                if j >= 2 and (j - 2) not in pv_done:
+                    violations.add("P overwrites a P not yet read")
+                nexts.append(with_(wpcs=adv, written=written | {(j, w)}))
+            elif kind == "wait_v_last":
+                if bars["vf%d" % (j & 1)].passed((j >> 1) & 1):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "zero_v":
+                nexts.append(with_(wpcs=adv, zeroed=zeroed | {w}))
+            elif kind == "arrive_p":
+                nb = clone_bars(bars)
+                nb["p%d" % (j & 1)].arrive()
+                nexts.append(with_(wpcs=adv, bars=nb))
+            elif kind == "wait_final":
+                if bars["drain"].passed(0):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "read_o":
+                if len(pv_done) != n_tiles:
+                    violations.add("O read before the last P V")
+                nexts.append(with_(wpcs=adv))
+        done = (mpc == len(mma) and all(pc == len(soft) for pc in wpcs) and not pipe and not flight and
+                all(pc == len(prog) for pc, prog in zip(ppcs, producers)))
+        if not nexts and not done:
+            violations.add("deadlock")
+        queue.extend(nexts)
+    return violations
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3])
+@pytest.mark.parametrize("split", [False, True])
+def test_k_and_v_rings_are_safe_with_one_or_two_producers(n_tiles, split):
+    # the kernel: K and V from separate producer threads; the earlier
+    # single-producer form is checked too
+    assert explore_with_loads(n_tiles, split_producers=split) == set()
+
+
+@pytest.mark.parametrize("mistake,expected", [
+    ("no_v_empty_wait", "V load overwrites a tile P V has not read"),
+    ("no_v_full_wait", "P V reads a V stage that does not hold its tile"),
+    ("zero_before_load", "V load lands over the zeroed rows"),
+])
+def test_planted_ring_mistakes_are_caught(mistake, expected):
+    # each planted mistake shows up as its own violation (and may cause more)
+    assert expected in explore_with_loads(3, split_producers=True, mistake=mistake)
+
+
+def test_freeing_k_late_is_only_slower():
+    assert explore_with_loads(3, split_producers=True, mistake="k_freed_late") == set()
