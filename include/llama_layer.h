@@ -385,6 +385,24 @@ int llama_num_sms(void);
  * difference across a region counts that region's kernels. */
 uint64_t llama_launch_count(void);
 
+/* Overrides how every projection GEMM of this process is scheduled (a process-
+ * wide setting, read at each launch; for tests and benchmarks that need one
+ * schedule).  The pages have no counterpart: they call library GEMMs.
+ *   -1  automatic (the default): cluster split-K for at most half as many
+ *       128 x 256 output tiles as SMs, stream-K up to twice as many, and
+ *       whole tiles on single SMs above that;
+ *    0  whole 128 x 256 tiles on single SMs;
+ *    1  stream-K on single SMs (needs the linear workspace);
+ *    2  cluster split-K where the tiles fit, else as -1;
+ *    3  whole 256 x 256 tiles on SM pairs (2-CTA clusters issuing tcgen05
+ *       pair MMAs; the B operand is loaded once for both SMs).  Slower than 0
+ *       on GB300 at the 70B shapes, where the part is power-limited; kept as
+ *       an option.
+ * Every schedule gives the same results up to the order of fp32 summation
+ * across K (0 and 3 sum in the same order).  The grouped GEMMs of the MoE
+ * block are not affected.  Returns LLAMA_ERR_ARG for any other value. */
+int llama_set_gemm_schedule(int schedule);
+
 #ifdef __cplusplus
 }
 #endif

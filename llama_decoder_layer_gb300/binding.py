@@ -85,6 +85,7 @@ SIGNATURES = {
     "llama_status_string": (ctypes.c_char_p, [_I]),
     "llama_num_sms": (_I, []),
     "llama_launch_count": (ctypes.c_uint64, []),
+    "llama_set_gemm_schedule": (_I, [_I]),
     "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
     "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -291,6 +292,12 @@ def paged_attention_noalloc(cfg: LayerConfig, batch: Batch, q, k_cache, v_cache,
     st = lib().llama_paged_attention_noalloc(ctypes.byref(c), ctypes.byref(b), _ptr(q), _ptr(k_cache),
                                              _ptr(v_cache), _ptr(out), _stream(stream))
     _check(st, "llama_paged_attention_noalloc")
+
+
+def set_gemm_schedule(schedule: int) -> None:
+    """Process-wide GEMM schedule: -1 automatic, 0 single-SM tiles, 1 stream-K,
+    2 cluster split-K, 3 SM-pair tiles."""
+    _check(lib().llama_set_gemm_schedule(int(schedule)), "llama_set_gemm_schedule")
 
 
 def get_device_error(stream=None):

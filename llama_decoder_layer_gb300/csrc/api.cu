@@ -685,4 +685,10 @@ int llama_num_sms(void) { return num_sms(); }
 
 uint64_t llama_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
+int llama_set_gemm_schedule(int schedule) {
+  if (schedule < -1 || schedule > 3) return LLAMA_ERR_ARG;
+  g_gemm_schedule.store(schedule, std::memory_order_relaxed);
+  return LLAMA_OK;
+}
+
 }  // extern "C"

@@ -42,6 +42,7 @@
 
 #include <cmath>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -763,6 +764,251 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The persistent GEMM on SM pairs: a 2-CTA cluster computes 256 x 256 output
+// tiles with M = 256 pair MMAs (tcgen05.mma.cta_group::2).  CTA r loads rows
+// 128r..128r+127 of the tile's A rows and its half of the tile's B rows
+// (plain: B rows 128r.. of the tile; SwiGLU: the 128 gate rows on rank 0 and
+// the matching up rows on rank 1) and receives D rows 128r.. in its own
+// tensor memory, all 256 columns, so the epilogue of each CTA is the 1-CTA
+// kernel's over its 128 rows.  Per k-block each SM loads 32 KB instead of
+// 48 KB for the same MMA work: the B operand is shared by the pair.
+//   * both producers (warp 0) wait for their own stage's empty barrier and
+//     load into their own shared memory, signalling rank 0's full barrier
+//     (rank 0 expects the pair's 64 KB);
+//   * one thread of rank 0 issues the MMAs and commits to the empty, tfull
+//     and drain barriers of both CTAs at once (multicast commit);
+//   * the epilogue warps of both CTAs drain their own accumulator and arrive
+//     on rank 0's tempty barrier (8 arrivals).
+// ---------------------------------------------------------------------------
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = BM * BK * 2;              // 16 KB: this CTA's 128 rows of A
+constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;        // 16 KB: this CTA's 128 rows of B
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 2048;
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;
+
+  uint8_t* meta = smem + PAIR_STAGES * PAIR_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * PAIR_STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* rope_tab = reinterpret_cast<float2*>(meta + 512);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (PAIR_STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * PAIR_STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * PAIR_STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 or 1
+  const bool lead = rank == 0;
+  const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+  // this CTA and its peer stop waiting once either of them gives up
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(peer_abort, 1u);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);  // the four epilogue warps of each CTA
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if constexpr (EPI == kEpiQkv) {
+    if (warp >= 2) copy_rope_table(p, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int npairs = static_cast<int>(gridDim.x) >> 1;
+  const long long first = static_cast<long long>(blockIdx.x >> 1);
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    const uint64_t pol_a = policy_evict_last();
+    const uint64_t pol_b = p.b_evict_first ? policy_evict_first() : policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t uses[PAIR_STAGES];
+#pragma unroll
+    for (int s = 0; s < PAIR_STAGES; ++s) uses[s] = 0;
+    bool waited = false, ok = true;
+    int n_pre = 0;
+    int pre_kb[PAIR_STAGES], pre_row[PAIR_STAGES];
+    auto finish_wait = [&]() {
+      pdl_wait();
+      if (lane == 0)
+        for (int i = 0; i < n_pre; ++i)
+          tma_load_2d_pair(sbase + i * PAIR_STAGE_BYTES, &tmA, mapa_shared(full_bar(i), 0), pre_kb[i] * BK,
+                           pre_row[i], pol_a);
+      __syncwarp();
+      waited = true;
+    };
+    for (long long t = first; ok && t < p.tiles; t += npairs) {
+      int tm, tn;
+      tile_coords(p, static_cast<int>(t), tm, tn);
+      const int arow = tm * 2 * BM + static_cast<int>(rank) * BM;
+      const int brow = tn * p.b_tile_rows + static_cast<int>(rank) * p.b_row_step;
+      for (int kb = 0; kb < p.kb; ++kb) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t sa = sbase + stage * PAIR_STAGE_BYTES;
+          const uint32_t sb = sa + PAIR_A_BYTES;
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (lead) mbar_arrive_expect_tx(full_bar(stage), 2 * PAIR_STAGE_BYTES);
+          if (waited) tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow, pol_a);
+          tma_load_2d_pair(sb, &tmB, fb, kb * BK, brow, pol_b);
+        }
+        __syncwarp();
+        if (!waited) {
+          pre_kb[n_pre] = kb;
+          pre_row[n_pre] = arow;
+          ++n_pre;
+        }
+        uses[stage]++;
+        if (++stage == PAIR_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (!waited && n_pre == PAIR_STAGES) finish_wait();
+      }
+    }
+    if (!waited) finish_wait();
+    if (lane == 0) pdl_trigger();
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmProducer);
+      give_up();
+    }
+    // rank 0's full barriers count the bytes of both CTAs: once every last
+    // phase has completed, every load of the pair has landed
+    if (lead)
+      for (int s = 0; s < PAIR_STAGES; ++s)
+        if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (rank 0) ----------------
+    pdl_wait();
+    if (lead) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long t = first; ok && t < p.tiles; t += npairs) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = sbase + stage * PAIR_STAGE_BYTES;
+            const uint32_t sb = sa + PAIR_A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma_f16_pair(d_tmem, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k), idesc,
+                              (kb > 0 || k > 0) ? 1u : 0u);
+            tc_commit_pair(empty_bar(stage), 3);
+          }
+          __syncwarp();
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair(tfull_bar(acc), 3);
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmMma);
+        give_up();
+      }
+      // completes in both CTAs once every MMA issued above has (at once if none was)
+      if (lane == 0) tc_commit_pair(drain_bar, 3);
+      __syncwarp();
+    }
+    // no CTA frees tensor memory the pair's MMAs may still write
+    mbar_wait(drain_bar, 0, nullptr);
+  } else {
+    // ---------------- epilogue warps (both CTAs) ----------------
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t tempty_lead0 = mapa_shared(tempty_bar(0), 0);
+    pdl_wait();
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (long long t = first; t < p.tiles; t += npairs) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(p, static_cast<int>(t), tm, tn);
+      const int vtm = 2 * tm + static_cast<int>(rank);  // this CTA's 128-row block
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      TmemLoader tl{taddr};
+      ScaledLoader<TmemLoader> ld{tl, row_scale_of(p, vtm * BM + row_in_tile, p.M)};
+      epilogue_tile<EPI>(p, vtm, tn, row_in_tile, ld, rope_tab, p.M);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_lead0 + 8u * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmEpilogue);
+      give_up();
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // Split-K over a thread-block cluster, for problems with at most half as many
 // tiles as SMs (decode-sized M).  The S CTAs of a cluster compute one tile,
 // CTA rank r over k-blocks [r*kb/S, (r+1)*kb/S), and each leaves its fp32
@@ -1065,8 +1311,58 @@ cudaError_t set_smem_attrs() {
     err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_gemm_cluster<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_gemm_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
   });
   return err;
+}
+
+// 2-CTA clusters of k_gemm_pair<EPI> resident at once (one per TPC with both
+// SMs free); cached per device.
+template <int EPI>
+int max_active_pairs() {
+  constexpr int kDevs = 64;
+  static int cache[kDevs] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = -1;
+    if (set_smem_attrs<EPI>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(2 * 128);
+      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int v = 0;
+      if (cudaOccupancyMaxActiveClusters(&v, k_gemm_pair<EPI>, &cfg) == cudaSuccess && v > 0) n = v;
+      else cudaGetLastError();
+    }
+    cache[dev] = n;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
+}
+
+int max_active_pairs_of(int epi) {
+  switch (epi) {
+    case kEpiBf16:
+      return max_active_pairs<kEpiBf16>();
+    case kEpiQkv:
+      return max_active_pairs<kEpiQkv>();
+    case kEpiSwiGlu:
+      return max_active_pairs<kEpiSwiGlu>();
+    case kEpiF32:
+      return max_active_pairs<kEpiF32>();
+    default:
+      return 0;
+  }
 }
 
 // Clusters of S CTAs of k_gemm_cluster<EPI> that fit on the device at once
@@ -1118,10 +1414,13 @@ int max_active_clusters_of(int epi, int S) {
 }
 
 template <int EPI>
-int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pdl,
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pair, bool pdl,
                  cudaStream_t s) {
   const cudaError_t attr_err = set_smem_attrs<EPI>();
   if (attr_err != cudaSuccess) return attr_err;
+  if (pair)
+    return launch_kernel_cluster(k_gemm_pair<EPI>, dim3(p.grid), dim3(NUM_THREADS), PAIR_SMEM_BYTES, s, pdl, 2, ta,
+                                 tb, p);
   if (cluster > 1)
     return launch_kernel_cluster(k_gemm_cluster<EPI>, dim3(p.tiles * cluster), dim3(NUM_THREADS), SMEM_BYTES, s, pdl,
                                  cluster, ta, tb, p);
@@ -1134,6 +1433,9 @@ int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams&
 }  // namespace
 
 size_t gemm_partials_bytes(int sms) { return static_cast<size_t>(sms) * 2 * BM * BN * sizeof(float); }
+
+// process-wide schedule override (llama_set_gemm_schedule); -1 = automatic
+std::atomic<int> g_gemm_schedule{-1};
 
 int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return 0;
@@ -1169,6 +1471,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.group_count = a.group_count;
   p.row_scale = a.row_scale;
   const bool grouped = a.group_tiles != nullptr;
+  const int mode = a.force_mode != -1 ? a.force_mode : g_gemm_schedule.load(std::memory_order_relaxed);
   // Raster: 24 M-tiles per group, so the 152 concurrent tiles cover 24
   // activation panels x ~6 weight panels, and weight loads are marked
   // evict-first so the activation panels of the group stay in L2 while the
@@ -1185,7 +1488,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   // SMs allow, at least two k-blocks per CTA, all clusters resident at once).
   if (grouped && a.group_count == nullptr) return cudaErrorInvalidValue;
   int cluster = 0;
-  if (!grouped && (a.force_mode == -1 || a.force_mode == 2) && p.tiles * 2 <= sms) {
+  if (!grouped && (mode == -1 || mode == 2) && p.tiles * 2 <= sms) {
     for (int S = sms / p.tiles < 8 ? sms / p.tiles : 8; S >= 2; --S) {
       if (p.kb < 2 * S || max_active_clusters_of(a.epi, S) < p.tiles) continue;
       cluster = S;
@@ -1193,15 +1496,33 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
     }
   }
   bool sk = cluster == 0 && p.tiles < 2 * sms;
-  if (a.force_mode == 0) sk = false;
-  if (a.force_mode == 1) sk = true;
+  if (mode == 0 || mode == 3) sk = false;
+  if (mode == 1) sk = true;
   if (grouped) sk = false;
+  // SM pairs (k_gemm_pair) only when asked for (schedule 3).  On the 70B
+  // gate_up GEMM (4128 and 32768 rows) the pair kernel keeps the tensor pipe
+  // 89-90% busy against 78% for single-SM tiles, but the part is then held by
+  // its power limit: the SM clock drops from 1.85 to 1.62-1.65 GHz, its
+  // raster re-reads more weights from DRAM (4.9-9.8 GB against 2.4 GB per
+  // launch), and in a seconds-long loop single-SM tiles are faster (2.42 vs
+  // 2.46-2.63 ms at 4128 rows, 18.9 vs 19.5-21.2 ms at 32768).
+  const bool pair = mode == 3 && !grouped;
+  int npairs = 0;
+  if (pair) {
+    npairs = max_active_pairs_of(a.epi);
+    if (npairs <= 0) return cudaErrorInvalidConfiguration;
+    p.tiles_m = (a.M + 2 * BM - 1) / (2 * BM);
+    p.tiles = p.tiles_m * p.tiles_n;
+    p.group_m = p.tiles_m < 12 ? p.tiles_m : 12;  // 3072 activation rows per raster group, as above
+  }
   p.units = static_cast<long long>(p.tiles) * p.kb;
   if (sk) {
     long long g = p.units < sms ? p.units : sms;
     if (g < 1) g = 1;
     p.grid = static_cast<int>(g);
     if (gemm_partials_bytes(p.grid) > a.partials_bytes || a.partials == nullptr) return cudaErrorInvalidValue;
+  } else if (pair) {
+    p.grid = 2 * (p.tiles < npairs ? p.tiles : npairs);  // every pair has at least one tile
   } else {
     p.grid = grouped ? sms : (p.tiles < sms ? p.tiles : sms);  // grouped: the tile count is on the device
   }
@@ -1212,13 +1533,13 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   if (!make_tmap_bf16(&tb, a.B, a.b_rows > 0 ? a.b_rows : a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
   switch (a.epi) {
     case kEpiBf16:
-      return launch_typed<kEpiBf16>(ta, tb, p, cluster, a.pdl != 0, s);
+      return launch_typed<kEpiBf16>(ta, tb, p, cluster, pair, a.pdl != 0, s);
     case kEpiQkv:
-      return launch_typed<kEpiQkv>(ta, tb, p, cluster, a.pdl != 0, s);
+      return launch_typed<kEpiQkv>(ta, tb, p, cluster, pair, a.pdl != 0, s);
     case kEpiSwiGlu:
-      return launch_typed<kEpiSwiGlu>(ta, tb, p, cluster, a.pdl != 0, s);
+      return launch_typed<kEpiSwiGlu>(ta, tb, p, cluster, pair, a.pdl != 0, s);
     case kEpiF32:
-      return launch_typed<kEpiF32>(ta, tb, p, cluster, a.pdl != 0, s);
+      return launch_typed<kEpiF32>(ta, tb, p, cluster, pair, a.pdl != 0, s);
     default:
       return cudaErrorInvalidValue;
   }

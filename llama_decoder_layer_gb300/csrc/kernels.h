@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "llama_layer.h"
 
 namespace llama {
@@ -44,7 +46,8 @@ struct GemmArgs {
   float* partials;  // stream-K partial tiles (see gemm_partials_bytes)
   size_t partials_bytes;
   int* err;
-  int force_mode;  // -1 auto, 0 data-parallel, 1 stream-K (tests)
+  int force_mode;  // -1 auto (or the llama_set_gemm_schedule override), 0 data-parallel, 1 stream-K,
+                  // 2 cluster split-K where it fits, 3 SM pairs
   int pdl;         // 1: may start before the previous kernel on the stream (one of this library's) completes
   // Grouped mode (MoE experts): when group_tiles is set, the tiles are
   // {A row, B base row, N tile, valid rows} entries of a device list with
@@ -145,6 +148,9 @@ struct MoeArgs {
 int moe_launch(const MoeArgs& a, cudaStream_t s);
 
 int num_sms();
+
+// process-wide GEMM schedule override (-1 automatic); see llama_set_gemm_schedule
+extern std::atomic<int> g_gemm_schedule;
 
 // The configuration and batch checks every attention entry point makes
 // (LLAMA_OK or the status it would return), with nothing launched.
