@@ -20,6 +20,7 @@ bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -447,8 +448,9 @@ def run_ours(args, world, rank, local):
     extra = {}
     if not args.no_extra:
         # single-layer 70B decode and prefill (weights of the stack's layer 0; their own batches/caches)
-        for name in ("decode_70b", "prefill_70b"):
-            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0], fold=args.fold_norms)
+        for name in ("decode_70b", "prefill_70b", "decode_8b"):
+            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0] if name != "decode_8b" else None,
+                            fold=args.fold_norms)
             steps = max(args.steps, 30) if name.startswith("decode") else args.steps
             lms, _ = time_steps(L.step, steps, args.warmup, world)
             alg = layer_algorithmic(L.spec, L.bl)
@@ -479,6 +481,22 @@ def run_ours(args, world, rank, local):
     # algorithmic totals of the stack step
     alg_layers = [layer_algorithmic(W.spec, W.bl) for _ in range(1)][0]
     stack_flops = alg_layers["flops"] * W.layers_n + 2.0 * W.bl.num_seqs * W.spec.hidden * W.spec.vocab
+    tokens_per_step, layers_n = W.tokens_per_step, W.layers_n
+
+    if not args.no_extra and not args.fold_norms:
+        # the full-depth 80-layer decode step (193 GB on the device): the stack's buffers go first
+        del W
+        gc.collect()
+        torch.cuda.empty_cache()
+        r = deep_decode(args, world, rank, local, lb, I, dev, peaks, peak_src)
+        B, L = r["B"], r["layers"]
+        extra["decode_70b_80l"] = {
+            "tokens_per_s_per_layer": round(B * L * world / (r["ms"] / 1e3), 1), "step_ms": round(r["ms"], 4),
+            "roofline": r["roofline"],
+            "cuda_graph": {"step_ms": round(r["graph_ms"], 4),
+                           "tokens_per_s_per_layer": round(B * L * world / (r["graph_ms"] / 1e3), 1),
+                           "roofline": r["graph_roofline"]},
+            "config": f"embedding + {L} layers + final norm + lm_head + argmax, {B} decode seqs, ctx U[512,4096]"}
     line = {
         "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
         "value": round(value, 1), "unit": "tokens/s per layer", "n_gpus": world, "steps": args.steps,
@@ -486,7 +504,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights of the 70B shape)",
         "config": {"workload": "stack_70b: 8 x 70B-shaped layers + final norm + lm_head(128256) + greedy argmax; "
                                "32 decode seqs (ctx U[1024,16384]) + 2 prefill chunks x 2048; 4128 tokens",
-                   "tokens_per_step": W.tokens_per_step, "layers": W.layers_n,
+                   "tokens_per_step": tokens_per_step, "layers": layers_n,
                    "l2": "inputs larger than L2 (13.7 GB of weights per step)", "parallelism": f"replicas x{world}",
                    "norms": "folded into w_qkv / w_gate_up" if args.fold_norms else "separate"},
         "stack_tflops_per_s": round(stack_flops / (ms / 1e3) / 1e12, 1),
@@ -618,19 +636,13 @@ def run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed
         print(json.dumps(line), flush=True)
 
 
-def run_deep_decode(args, world, rank, local):
+def deep_decode(args, world, rank, local, lb, I, dev, peaks, peak_src):
     """The full-depth 70B decode step: embedding, 80 layers, final norm,
     lm_head and greedy sampling in one llama_stack_forward call, timed eager
     and replayed from a CUDA graph.  Every layer has its own weight and cache
     buffers (137 GB + 48 GB); their values are layer 0's, copied, since
-    drawing 68 G random numbers would dominate the run."""
-    from llama_decoder_layer_gb300 import binding as lb
-    from llama_decoder_layer_gb300 import build as lbuild
-    from llama_decoder_layer_gb300 import inputs as I
-    lbuild.build()
-    lb.lib()
-    dev = torch.device("cuda", local)
-    peaks, peak_src = load_peaks()
+    drawing 68 G random numbers would dominate the run.  Returns the timing
+    record (eager and graph, each with its HBM roofline)."""
     seed = 1000 + rank
     spec = I.SPECS["decode_70b_80l"]
     bl = I.make_batch(spec, seed, dev)
@@ -658,7 +670,7 @@ def run_deep_decode(args, world, rank, local):
     gms = time_graph(step, args.steps, args.warmup, world)
     st, detail = lb.get_device_error()
     if st != lb.LLAMA_OK:
-        raise RuntimeError(f"device error during the bench: {lb.status_string(st)} (detail {detail})")
+        raise RuntimeError(f"device error in the 80-layer decode: {lb.status_string(st)} (detail {detail})")
     alg = layer_algorithmic(spec, bl)
     head_bytes = spec.vocab * spec.hidden * 2 + B * spec.vocab * 4
     step_bytes = spec.num_layers * alg["bytes"] + head_bytes
@@ -669,20 +681,39 @@ def run_deep_decode(args, world, rank, local):
                 "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({peak_src})",
                 "algorithmic_bytes": step_bytes, "traffic": None}
 
+    rec = {"B": B, "T": T, "layers": spec.num_layers, "ms": ms, "graph_ms": gms, "clocks": clocks,
+           "launches": launches, "step_bytes": step_bytes, "roofline": roof(ms), "graph_roofline": roof(gms)}
+    del layers, caches, kcs, vcs, w0, kc0, vc0, emb, lm, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_deep_decode(args, world, rank, local):
+    """--workload decode_70b_80l: the full-depth decode step as its own line."""
+    from llama_decoder_layer_gb300 import binding as lb
+    from llama_decoder_layer_gb300 import build as lbuild
+    from llama_decoder_layer_gb300 import inputs as I
+    lbuild.build()
+    lb.lib()
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    r = deep_decode(args, world, rank, local, lb, I, dev, peaks, peak_src)
+    B, L = r["B"], r["layers"]
     line = {
         "metric": "tokens/s per 70B-shape decoder layer (decode, prefill) & % of HBM/TC roofline",
-        "value": round(B * spec.num_layers * world / (ms / 1e3), 1), "unit": "tokens/s per layer", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "value": round(B * L * world / (r["ms"] / 1e3), 1), "unit": "tokens/s per layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; every layer's buffers hold layer 0's random values)",
         "config": {"workload": f"decode_70b_80l: embedding + 80 x 70B-shaped layers + final norm + lm_head(128256) "
                                f"+ greedy argmax; {B} decode seqs, ctx U[512,4096]",
-                   "tokens_per_step": T, "layers": spec.num_layers,
-                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.0f} GB per step)",
+                   "tokens_per_step": r["T"], "layers": L,
+                   "l2": f"inputs larger than L2 ({r['step_bytes'] / 1e9:.0f} GB per step)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roof(ms), "clocks": clocks, "gpu_launches": launches, "cpu_baseline": None, "e2e": None,
-        "cuda_graph": {"ms_per_step": round(gms, 4), "value": round(B * spec.num_layers * world / (gms / 1e3), 1),
-                       "roofline": roof(gms)},
+        "roofline": r["roofline"], "clocks": r["clocks"], "gpu_launches": r["launches"], "cpu_baseline": None,
+        "e2e": None,
+        "cuda_graph": {"ms_per_step": round(r["graph_ms"], 4),
+                       "value": round(B * L * world / (r["graph_ms"] / 1e3), 1), "roofline": r["graph_roofline"]},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
