@@ -39,10 +39,10 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the gate_up
 # GEMM at the stack's shape (4128 x 57344 x 8192) from an ncu capture of the
-# current kernel, or None when the kernel has changed since the last capture
-# (the last one, 2.34 GB read + 0.18 GB written, predates the GEMM's grouped
-# mode and epilogue row scale).
-GATE_UP_DRAM_BYTES_PER_LAUNCH = None
+# current kernel (2.594 GB read + 0.183 GB written, one launch of
+# `bench.py --workload gemm_gate_up`, tensor pipe 78.3% active at 1837 MHz),
+# or None when the kernel has changed since that capture.
+GATE_UP_DRAM_BYTES_PER_LAUNCH = 2594396160 + 183139840
 
 
 def load_peaks():
