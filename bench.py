@@ -287,24 +287,31 @@ def time_graph(step, steps, warmup, world):
 
 def time_e2e(lb, W, steps, warmup, world, dev):
     """Same stack step through the public API with the step's inputs copied
-    from pinned host memory and the sampled tokens copied back, every step."""
+    from pinned host memory and the sampled tokens copied back, every step.
+    The inputs (token ids, positions, query_start_loc, seq_lens, block table:
+    all int32) sit in one pinned host buffer and go over in one copy; the
+    batch and the ids are views of the matching device buffer."""
     bl = W.bl
-    host = {
-        "ids": W.ids.cpu().pin_memory(), "positions": bl.positions.cpu().pin_memory(),
-        "qsl": bl.query_start_loc.cpu().pin_memory(), "seq_lens": bl.seq_lens.cpu().pin_memory(),
-        "block_table": bl.block_table.cpu().pin_memory(),
-    }
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    parts = [("ids", W.ids), ("positions", bl.positions), ("qsl", bl.query_start_loc),
+             ("seq_lens", bl.seq_lens), ("block_table", bl.block_table)]
+    sizes = [t.numel() for _, t in parts]
+    slots = [(n + 3) // 4 * 4 for n in sizes]  # each part starts on a 16-byte boundary
+    host = torch.zeros(sum(slots), dtype=torch.int32).pin_memory()
+    dev_buf = torch.empty(sum(slots), dtype=torch.int32, device=dev)
+    views, off = {}, 0
+    for (name, t), n, m in zip(parts, sizes, slots):
+        host[off:off + n].copy_(t.reshape(-1).to(torch.int32).cpu())
+        views[name] = dev_buf[off:off + n].view(t.shape)
+        off += m
     out_host = torch.empty(bl.num_seqs, dtype=torch.int32).pin_memory()
-    batch = lb.Batch(dev_in["positions"], dev_in["qsl"], dev_in["seq_lens"], dev_in["block_table"],
+    batch = lb.Batch(views["positions"], views["qsl"], views["seq_lens"], views["block_table"],
                      W.batch.num_blocks, W.batch.max_query_len, W.batch.max_seq_len)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = host.numel() * host.element_size()
     d2h = out_host.numel() * out_host.element_size()
 
     def step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        W.step(batch=batch, ids=dev_in["ids"])
+        dev_buf.copy_(host, non_blocking=True)
+        W.step(batch=batch, ids=views["ids"])
         out_host.copy_(W.tokens, non_blocking=True)
 
     ms, _ = time_steps(step, steps, warmup, world)

@@ -724,7 +724,10 @@ constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-colu
 constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
 constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
 constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
-constexpr int kTcSmem = 2 * kTcQHalf + 2 * 2 * kTcTileBytes + 256 + kTcSlack;
+constexpr int kTcKStages = 2;                     // K ring (three stages measured slower: 1.98 vs 1.87 ms)
+constexpr int kTcVStages = 2;                     // V ring (the code below indexes it with j & 1)
+static_assert(kTcVStages == 2, "the V ring is indexed by tile parity");
+constexpr int kTcSmem = 2 * kTcQHalf + (kTcKStages + kTcVStages) * kTcTileBytes + 256 + kTcSlack;
 constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
 
 __global__ void __launch_bounds__(kTcThreads, 2)
@@ -742,22 +745,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
   const uint32_t q_s = sb;                                   // Q: two 64-column halves
-  auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes; };
-  auto v_s = [&](int st) { return sb + 2u * kTcQHalf + st * 2u * kTcTileBytes + kTcTileBytes; };
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + 4 * kTcTileBytes);
+  auto k_s = [&](int st) { return sb + 2u * kTcQHalf + st * kTcTileBytes; };
+  auto v_s = [&](int st) { return sb + 2u * kTcQHalf + (kTcKStages + st) * kTcTileBytes; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcQHalf + (kTcKStages + kTcVStages) * kTcTileBytes);
   const uint32_t bar0 = smem_u32(bars);
-  // K and V have their own 2-stage rings: a K stage is free as soon as its
-  // S = Q K^T is done, so the next K tile is fetched while P V still runs
+  // K and V have their own rings: a K stage is free as soon as its S = Q K^T
+  // is done, so the next K tiles are fetched while P V still runs
   // P ready: one barrier per S buffer.  With one barrier for every tile a
   // softmax warp that finished tile j could run through tile j+1 (its S is
   // already there) and arrive again before a slower warp arrived for tile j,
   // completing tile j's phase while part of P(j) was still being written.  A
   // warp cannot reach tile j+2 before P V of tile j is issued, so the arrivals
   // at p_full0 + 8 * (j % 2) all belong to tile j.
-  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
-                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full0 = bar0 + 88, o_done = bar0 + 104,
-                 drain = bar0 + 112;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = k_full0 + 8 * kTcKStages,
+                 v_full0 = k_empty0 + 8 * kTcKStages, v_empty0 = v_full0 + 8 * kTcVStages,
+                 s_full0 = v_empty0 + 8 * kTcVStages, p_full0 = s_full0 + 16, o_done = p_full0 + 16,
+                 drain = o_done + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcKStages + 2 * kTcVStages + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
   int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
@@ -796,9 +800,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTcKStages; ++i) {
       mbar_init(k_full0 + 8 * i, 1);
       mbar_init(k_empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
@@ -823,7 +829,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const bool is_k = warp == 0;
     if (lane == 0) {
       bool ok = true;
-      uint32_t uses[2] = {0, 0};
+      uint32_t uses[kTcKStages > kTcVStages ? kTcKStages : kTcVStages] = {};
+      const int nst = is_k ? kTcKStages : kTcVStages;
       const uint64_t pol = policy_evict_normal();
       if (is_k) {
         mbar_arrive_expect_tx(q_full, 32768);
@@ -834,8 +841,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const CUtensorMap* tm = is_k ? &tmK : &tmV;
       const uint32_t full0 = is_k ? k_full0 : v_full0, empty0 = is_k ? k_empty0 : v_empty0;
       for (int j = 0; j < ntiles; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag)) {
+        const int st = j % nst;
+        if (!mbar_wait(empty0 + 8 * st, ((j / nst) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -862,7 +869,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       // every load this thread issued lands before the CTA can exit
       if (is_k) mbar_wait(q_full, 0, nullptr);
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < nst; ++st)
         if (uses[st] > 0) mbar_wait(full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
     }
     __syncwarp();
@@ -873,8 +880,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     bool ok = mbar_wait(q_full, 0, abort_flag);
     bool issued = false;
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag)) return false;
+      const int st = j & 1;             // S buffer
+      const int kst = j % kTcKStages;   // K stage
+      if (!mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t d = tmem + st * kTcKeys;
@@ -882,10 +890,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
           const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(st) + ck), idS, kk > 0 ? 1u : 0u);
+          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(kst) + ck), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full0 + 8 * st);
-        tc_commit(k_empty0 + 8 * st);
+        tc_commit(k_empty0 + 8 * kst);
         issued = true;
       }
       __syncwarp();

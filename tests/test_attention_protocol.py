@@ -208,11 +208,12 @@ def test_single_tile_is_safe_either_way():
 # ---------------------------------------------------------------------------
 
 
-def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
+def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages=2):
     """Every interleaving of the kernel's protocol including the K and V
-    shared-memory rings (two stages each) and their producers.  K(j) and V(j)
-    go to stage j % 2; a producer waits for the stage's empty barrier (parity
-    ((j >> 1) & 1) ^ 1), issues the TMA load, and the load lands at any later
+    shared-memory rings (k_stages K stages, two V stages) and their producers.
+    K(j) goes to stage j % k_stages, V(j) to stage j % 2; a producer waits for
+    the stage's empty barrier (parity ((j // stages) & 1) ^ 1), issues the TMA
+    load, and the load lands at any later
     point, in any order with the other loads in flight, arriving at the
     stage's full barrier.  The MMA thread waits for K(j)'s full barrier before
     S(j) and frees the K stage by a commit after it; it waits for P(j) and
@@ -224,6 +225,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
     both from one thread in the order K(0), V(0), K(1), V(1), ...
     mistake: plant one error to show the model catches it:
       "no_v_empty_wait"  the V producer does not wait for the stage to be free
+      "no_k_empty_wait"  the K producer does not wait for the stage to be free
       "k_freed_late"     the K stage is freed after P V instead of after S
                          (safe, only slower: no violation expected)
       "no_v_full_wait"   the MMA thread issues P V without waiting for V
@@ -256,7 +258,9 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
         out = []
         for j in range(n_tiles):
             for kind in kinds:
-                if not (kind == "V" and mistake == "no_v_empty_wait"):
+                skip_wait = (kind == "V" and mistake == "no_v_empty_wait") or \
+                    (kind == "K" and mistake == "no_k_empty_wait")
+                if not skip_wait:
                     out.append(("wait_empty", (kind, j)))
                 out.append(("load", (kind, j)))
         return out
@@ -266,9 +270,11 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
     def fresh_barriers():
         b = {"o_done": Barrier(1), "drain": Barrier(1)}
         for i in range(2):
-            for name in ("s", "kf", "ke", "vf", "ve"):
+            for name in ("s", "vf", "ve"):
                 b["%s%d" % (name, i)] = Barrier(1)
             b["p%d" % i] = Barrier(warps)
+        for i in range(k_stages):
+            b["kf%d" % i], b["ke%d" % i] = Barrier(1), Barrier(1)
         return b
 
     def clone_bars(bars):
@@ -281,8 +287,8 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
 
     # state: mma pc, warp pcs, producer pcs, pipe, barriers, loads in flight,
     # K stage contents, V stage contents, P written, S done, P V done, V rows zeroed
-    start = (0, (0,) * warps, (0,) * len(producers), (), fresh_barriers(), frozenset(), (None, None), (None, None),
-             frozenset(), frozenset(), frozenset(), frozenset())
+    start = (0, (0,) * warps, (0,) * len(producers), (), fresh_barriers(), frozenset(), (None,) * k_stages,
+             (None, None), frozenset(), frozenset(), frozenset(), frozenset())
 
     def key(st):
         m, w, pp, pipe, bars, fl, ks, vs, wr, sd, pvd, zr = st
@@ -312,19 +318,20 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
                 continue
             kind, (kv, j) = prog[pc]
             adv = ppcs[:i] + (pc + 1,) + ppcs[i + 1:]
-            e = ("ke%d" if kv == "K" else "ve%d") % (j & 1)
+            n = k_stages if kv == "K" else 2
+            e = ("ke%d" if kv == "K" else "ve%d") % (j % n)
             if kind == "wait_empty":
-                if bars[e].passed(((j >> 1) & 1) ^ 1):
+                if bars[e].passed(((j // n) & 1) ^ 1):
                     nexts.append(with_(ppcs=adv))
             else:
                 nexts.append(with_(ppcs=adv, flight=flight | {(kv, j)}))
         # a load in flight lands (any of them)
         for (kv, j) in flight:
-            s = j & 1
+            s = j % (k_stages if kv == "K" else 2)
             nb = clone_bars(bars)
             nb[("kf%d" if kv == "K" else "vf%d") % s].arrive()
             if kv == "K":
-                if j >= 2 and (j - 2) not in s_done:
+                if j >= k_stages and (j - k_stages) not in s_done:
                     violations.add("K load overwrites a tile S has not read")
                 nexts.append(with_(bars=nb, flight=flight - {(kv, j)}, kst=kst[:s] + (j,) + kst[s + 1:]))
             else:
@@ -337,11 +344,12 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
         if mpc < len(mma):
             kind, j = mma[mpc]
             s = (j or 0) & 1
+            ks = (j or 0) % k_stages
             if kind == "wait_k":
-                if bars["kf%d" % s].passed((j >> 1) & 1):
+                if bars["kf%d" % ks].passed((j // k_stages) & 1):
                     nexts.append(with_(mpc=mpc + 1))
             elif kind == "issue_s":
-                free_k = () if mistake == "k_freed_late" else (("commit", "ke%d" % s),)
+                free_k = () if mistake == "k_freed_late" else (("commit", "ke%d" % ks),)
                 nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("S", j), ("commit", "s%d" % s)) + free_k))
             elif kind == "wait_p":
                 if bars["p%d" % s].passed((j >> 1) & 1):
@@ -350,7 +358,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
                 if bars["vf%d" % s].passed((j >> 1) & 1):
                     nexts.append(with_(mpc=mpc + 1))
             elif kind == "issue_pv":
-                free_k = (("commit", "ke%d" % s),) if mistake == "k_freed_late" else ()
+                free_k = (("commit", "ke%d" % ks),) if mistake == "k_freed_late" else ()
                 nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("PV", j), ("commit", "ve%d" % s), ("commit", "o_done"))
                                    + free_k))
             elif kind == "commit_drain":
@@ -359,7 +367,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
         if pipe:
             op, arg = pipe[0]
             if op == "S":
-                if kst[arg & 1] != arg or any(f == ("K", arg) for f in flight):
+                if kst[arg % k_stages] != arg or any(f == ("K", arg) for f in flight):
                     violations.add("S reads a K stage that does not hold its tile")
                 nexts.append(with_(pipe=pipe[1:], s_done=s_done | {arg}))
             elif op == "PV":
@@ -423,9 +431,21 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None):
 @pytest.mark.parametrize("n_tiles", [1, 2, 3])
 @pytest.mark.parametrize("split", [False, True])
 def test_k_and_v_rings_are_safe_with_one_or_two_producers(n_tiles, split):
-    # the kernel: K and V from separate producer threads; the earlier
-    # single-producer form is checked too
+    # K and V from separate producer threads, or (the earlier form) from one
     assert explore_with_loads(n_tiles, split_producers=split) == set()
+
+
+@pytest.mark.parametrize("n_tiles", [2, 4])
+def test_three_stage_k_ring_is_safe(n_tiles):
+    # the kernel's ring depth is a constant: three K stages (measured slower
+    # than two on GB300) and two V stages, separate producers
+    assert explore_with_loads(n_tiles, split_producers=True, k_stages=3) == set()
+
+
+
+def test_planted_k_ring_mistake_with_three_stages():
+    assert "K load overwrites a tile S has not read" in explore_with_loads(
+        4, split_producers=True, k_stages=3, mistake="no_k_empty_wait")
 
 
 @pytest.mark.parametrize("mistake,expected", [
