@@ -389,8 +389,8 @@ uint64_t llama_launch_count(void);
  * wide setting, read at each launch; for tests and benchmarks that need one
  * schedule).  The pages have no counterpart: they call library GEMMs.
  *   -1  automatic (the default): cluster split-K for at most half as many
- *       128 x 256 output tiles as SMs, stream-K up to twice as many, and
- *       whole tiles on single SMs above that;
+ *       128 x 256 output tiles as SMs, stream-K below as many tiles as SMs,
+ *       and whole tiles on single SMs from there on;
  *    0  whole 128 x 256 tiles on single SMs;
  *    1  stream-K on single SMs (needs the linear workspace);
  *    2  cluster split-K where the tiles fit, else as -1;

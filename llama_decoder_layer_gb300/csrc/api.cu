@@ -225,16 +225,18 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   float* rscale = folded ? reinterpret_cast<float*>(ws + L.rscale) : nullptr;
   int e;
 
+  // cache slots: the caller's, or derived on the device by the input norm
+  // kernel (its CTA of row t writes token t's slot)
   const int32_t* slot_map = b.slot_mapping;
+  SlotMapArgs sm{};
   if (slot_map == nullptr) {
-    e = slot_mapping_launch(b.positions, b.query_start_loc, b.seq_lens, b.block_table, T, b.num_seqs,
-                            b.max_blocks_per_seq, c.block_size, b.num_blocks, slots, err, chain, s);
-    if (e) return cuda_status(e);
+    sm = SlotMapArgs{b.positions, b.query_start_loc, b.seq_lens, b.block_table, b.num_seqs,
+                     b.max_blocks_per_seq, c.block_size, b.num_blocks, slots, err};
     slot_map = slots;
-    chain = true;
   }
   // input_layernorm
-  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, chain, s, rscale);
+  e = add_rmsnorm_launch(hidden, res_in, res_out, h, w.ln1_w, T, H, c.rms_eps, nullptr, chain, s, rscale,
+                         sm.slots != nullptr ? &sm : nullptr);
   if (e) return cuda_status(e);
   const void* normed = folded ? res_out : h;  // the A operand of qkv (and, after the second norm, gate_up)
   auto gemm = [&](int epi, const void* A, const void* B, int N, int K, void* out, int ldo) {

@@ -15,16 +15,17 @@
 // before SiluAndMul, exactly where the unfused modules would store it.
 //
 // Three schedules, by the number of output tiles against the SM count:
-//   * many tiles (prefill): k_gemm_tc, persistent (one CTA per SM), whole
+//   * at least one wave of tiles (prefill, the 70B decode gate_up): k_gemm_tc,
+//     persistent (one CTA per SM), whole
 //     tiles in a grouped raster for L2 reuse, the accumulator double-buffered
 //     so the epilogue of one tile overlaps the MMAs of the next;
 //   * at most half as many tiles as SMs (decode qkv, o_proj, down_proj):
 //     k_gemm_cluster, split-K over a thread-block cluster whose CTAs sum their
 //     fp32 slices through distributed shared memory;
-//   * in between (decode gate_up): k_gemm_tc stream-K, every CTA an equal
-//     share of (tile, k-block) units, partial tiles in a workspace, and
-//     k_gemm_fixup summing them in CTA order (deterministic) spread over many
-//     CTAs.
+//   * in between, below one wave of tiles (the 8B decode gate_up): k_gemm_tc
+//     stream-K, every CTA an equal share of (tile, k-block) units, partial
+//     tiles in a workspace, and k_gemm_fixup summing them in CTA order
+//     (deterministic) spread over many CTAs.
 // Grouped mode (the experts of an MoE block): k_gemm_tc walks a tile list
 // built on the device, each entry naming its A rows, its expert's B rows and
 // how many of its rows are valid.  A row scale (an RMSNorm's rsqrt, its
@@ -1495,7 +1496,11 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
       break;
     }
   }
-  bool sk = cluster == 0 && p.tiles < 2 * sms;
+  // stream-K below one wave of whole tiles (the 8B decode gate_up, 112 tiles:
+  // 48.8 us against 49.5 for whole tiles); from one wave up whole tiles win
+  // (the 70B decode gate_up, 224 tiles: 162.9 us against 168.3 for stream-K
+  // and its fixup)
+  bool sk = cluster == 0 && p.tiles < sms;
   if (mode == 0 || mode == 3) sk = false;
   if (mode == 1) sk = true;
   if (grouped) sk = false;

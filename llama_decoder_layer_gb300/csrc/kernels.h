@@ -67,22 +67,32 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s);  // returns 0 or a CUDA erro
 // fused residual add + RMSNorm over rows of length H
 //   r = x (+ res_in); h = r * rsqrt(mean(r^2) + eps) * gamma
 // With gamma null the norm is folded into the next GEMM: h is not written and
+// Cache-slot mapping of a batch: slot[t] = block_table[b][pos/bs]*bs + pos%bs
+// for token t of sequence b at position pos (-1 when out of range).
+struct SlotMapArgs {
+  const int32_t* positions;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int B, max_blocks, bs, num_blocks;
+  int32_t* slots;  // [T] output; null: no slot mapping
+  int* err;
+};
+
 // inv_out[row] receives rsqrt(mean(r^2) + eps).
 // row_index_qsl != nullptr: output row b reads input row qsl[b+1]-1 (last
 // token of sequence b), otherwise row b reads row b.
+// slot_map != nullptr: the kernel also writes the batch's cache slots (one per
+// row; rows must be the batch's tokens).
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma,
                        int rows, int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s,
-                       float* inv_out = nullptr);
+                       float* inv_out = nullptr, const SlotMapArgs* slot_map = nullptr);
 
 // one CTA whose bounded wait on a barrier nothing arrives at runs out
 int selftest_wait_launch(int* err, cudaStream_t s);
 
 // w_folded[o, i] = bf16(w[o, i] * gamma[i]) for a [rows, cols] weight
 int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void* w_folded, cudaStream_t s);
-
-int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
-                        const int32_t* block_table, int T, int B, int max_blocks, int block_size, int num_blocks,
-                        int32_t* slots, int* err, bool pdl, cudaStream_t s);
 
 int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, int n_kv, int head_dim,
                     int block_size, int num_blocks, void* k_cache, void* v_cache, int* err, cudaStream_t s);

@@ -43,18 +43,44 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return red[32];
 }
 
+// The cache slot of token t: block_table[b][pos / bs] * bs + pos % bs, b the
+// token's sequence (found in query_start_loc); -1 (and the error word) for a
+// position outside its sequence or a block-table entry outside the cache.
+__device__ __forceinline__ int32_t token_slot(const SlotMapArgs& m, int t) {
+  int lo = 0, hi = m.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (m.qsl[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int pos = m.positions[t];
+  const int j = pos / m.bs;
+  if (pos < 0 || pos >= m.seq_lens[b] || j >= m.max_blocks) {
+    report_error(m.err, kErrGuard, kWhereSlot);
+    return -1;
+  }
+  const int blk = m.block_table[static_cast<size_t>(b) * m.max_blocks + j];
+  if (blk < 0 || blk >= m.num_blocks) {
+    report_error(m.err, kErrGuard, kWhereBlockTable);
+    return -1;
+  }
+  return blk * m.bs + pos % m.bs;
+}
+
 // One CTA per output row.  Every thread holds up to MAXC 16-byte chunks of the
 // row in registers, so the row is fully read before anything is written:
-// res_out may alias x or res_in and h_out may alias x.
+// res_out may alias x or res_in and h_out may alias x.  With sm.slots set (the
+// input norm of a layer), the CTA of row t also writes token t's cache slot.
 template <int MAXC>
 __global__ void __launch_bounds__(kNormThreads) k_add_rmsnorm(const uint4* __restrict__ x, const uint4* res_in,
                                                               uint4* res_out, uint4* h_out,
                                                               const uint4* __restrict__ gamma, int H, float eps,
                                                               const int32_t* __restrict__ qsl,
-                                                              float* __restrict__ inv_out) {
+                                                              float* __restrict__ inv_out, const SlotMapArgs sm) {
   __shared__ float red[33];
   pdl_wait();
   const int out_row = blockIdx.x;
+  if (sm.slots != nullptr && threadIdx.x == 0) sm.slots[out_row] = token_slot(sm, out_row);
   const int in_row = qsl != nullptr ? qsl[out_row + 1] - 1 : out_row;
   const int nch = H >> 3;
   const size_t ibase = static_cast<size_t>(in_row) * nch;
@@ -145,36 +171,6 @@ __global__ void k_selftest_wait(int* err) {
   mbar_init(b, 1);
   fence_mbar_init();
   if (!mbar_wait(b, 0, nullptr)) report_error(err, kErrTimeout, kWhereSelftest);
-}
-
-// slot = block_table[b][pos / bs] * bs + pos % bs for every token; the
-// sequence b of token t is found by binary search in query_start_loc.
-__global__ void k_slot_mapping(const int32_t* __restrict__ positions, const int32_t* __restrict__ qsl,
-                               const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table, int T,
-                               int B, int max_blocks, int bs, int num_blocks, int32_t* __restrict__ slots, int* err) {
-  pdl_wait();
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (qsl[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int b = lo;
-    const int pos = positions[t];
-    const int j = pos / bs;
-    int slot = -1;
-    if (pos < 0 || pos >= seq_lens[b] || j >= max_blocks) {
-      report_error(err, kErrGuard, kWhereSlot);
-    } else {
-      const int blk = block_table[static_cast<size_t>(b) * max_blocks + j];
-      if (blk < 0 || blk >= num_blocks) {
-        report_error(err, kErrGuard, kWhereBlockTable);
-      } else {
-        slot = blk * bs + pos % bs;
-      }
-    }
-    slots[t] = slot;
-  }
 }
 
 // Standalone cache write: one thread per 16-byte chunk of one (token, head)
@@ -270,7 +266,8 @@ int grid_for(long long work, int threads) {
 }  // namespace
 
 int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h_out, const void* gamma, int rows,
-                       int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s, float* inv_out) {
+                       int H, float eps, const int32_t* row_index_qsl, bool pdl, cudaStream_t s, float* inv_out,
+                       const SlotMapArgs* slot_map) {
   if (rows <= 0) return 0;
   const int nch = H / 8;
   const int per = (nch + kNormThreads - 1) / kNormThreads;
@@ -279,9 +276,11 @@ int add_rmsnorm_launch(const void* x, const void* res_in, void* res_out, void* h
   auto RO = static_cast<uint4*>(res_out);
   auto HO = static_cast<uint4*>(h_out);
   auto G = static_cast<const uint4*>(gamma);
+  SlotMapArgs sm{};
+  if (slot_map != nullptr) sm = *slot_map;
   auto go = [&](auto kernel) {
     return launch_kernel(kernel, dim3(rows), dim3(kNormThreads), 0, s, pdl, X, R, RO, HO, G, H, eps, row_index_qsl,
-                         inv_out);
+                         inv_out, sm);
   };
   if (per <= 1) return go(k_add_rmsnorm<1>);
   if (per <= 2) return go(k_add_rmsnorm<2>);
@@ -300,14 +299,6 @@ int fold_norm_launch(const void* gamma, const void* w, int rows, int cols, void*
   return launch_kernel(k_fold_norm, dim3(grid_for(chunks, 256)), dim3(256), 0, s, false,
                        static_cast<const uint4*>(gamma), static_cast<const uint4*>(w), chunks, cols / 8,
                        static_cast<uint4*>(w_folded));
-}
-
-int slot_mapping_launch(const int32_t* positions, const int32_t* qsl, const int32_t* seq_lens,
-                        const int32_t* block_table, int T, int B, int max_blocks, int block_size, int num_blocks,
-                        int32_t* slots, int* err, bool pdl, cudaStream_t s) {
-  if (T <= 0) return 0;
-  return launch_kernel(k_slot_mapping, dim3(grid_for(T, 256)), dim3(256), 0, s, pdl, positions, qsl, seq_lens,
-                       block_table, T, B, max_blocks, block_size, num_blocks, slots, err);
 }
 
 int kv_write_launch(const void* k, const void* v, const int32_t* slots, int T, int n_kv, int head_dim,

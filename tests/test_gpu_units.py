@@ -32,13 +32,13 @@ def _ws(n):
 
 
 # tiles = ceil(M/128) * ceil(N/256) against the SM count (152 on GB300): at most
-# half of it -> split-K over a cluster, up to twice it -> stream-K + fixup,
-# more -> data-parallel.  Ragged M, N and K tails throughout.
+# half of it -> split-K over a cluster, below it -> stream-K + fixup, from it
+# on -> data-parallel.  Ragged M, N and K tails throughout.
 @pytest.mark.parametrize("M,N,K", [
     (37, 768, 512), (128, 1024, 1376), (300, 1000, 512),      # cluster split-K (S = 4, 8, 4)
-    (1, 256, 64), (64, 40960, 512), (200, 20480, 256),        # stream-K (one k-block; 160 tiles; 2 M-tiles)
-    (2500, 2304, 192),                                        # stream-K, 180 tiles of 20 M-tiles
-    (4096, 4096, 256),                                        # data-parallel
+    (1, 256, 64), (64, 30720, 512), (200, 15360, 256),        # stream-K (one k-block; 120 tiles; 2 M-tiles)
+    (1500, 2304, 192),                                        # stream-K, 108 tiles of 12 M-tiles
+    (64, 40960, 512), (4096, 4096, 256),                      # data-parallel (160 tiles: one and a bit waves)
 ])
 def test_linear_bf16(M, N, K):
     x = I.normal_bf16((M, K), 1.0, 0.0, 11 + M, DEV)
