@@ -436,20 +436,37 @@ def run_ours(args, world, rank, local):
     e2e_ms, h2d, d2h = time_e2e(lb, W, args.steps, args.warmup, world, dev)
     e2e_value = tok_layers * world / (e2e_ms / 1e3)
 
-    # dominant kernel: the gate_up GEMM with SiluAndMul (one layer's worth), timed alone
+    # dominant kernel: the gate_up GEMM with SiluAndMul.  Timed inside the stack
+    # step: a pass of its own after the timed region, with CUDA events around
+    # each of its launches in the layer loop (llama_gate_up_timer_*); being
+    # part of a long step, it is compared with the sustained peak.
     spec, T = W.spec, W.tokens_per_step
+    W.step()
+    torch.cuda.synchronize()
+    lb.gate_up_timer_start(args.steps * W.layers_n)
+    for _ in range(args.steps):
+        W.step()
+    torch.cuda.synchronize()
+    tot_ms, n_timed = lb.gate_up_timer_stop()
+    in_ms = tot_ms / max(n_timed, 1)
+    # the same launch timed alone, for reference against the burst peak
     xin = I.normal_bf16((T, spec.hidden), 1.0, 0.0, 77, dev)
     aout = torch.empty((T, spec.intermediate), dtype=torch.bfloat16, device=dev)
     gws = lb.alloc_workspace(lb.linear_workspace_size(), dev)
     wgu = W.layers[0]["w_gate_up"]
     k_ms = time_kernel(lambda: lb.gate_up_silu(xin, wgu, aout, gws), reps=max(args.steps, 10))
     k_flops = 2.0 * T * 2 * spec.intermediate * spec.hidden
+    in_tflops = k_flops / (in_ms / 1e3) / 1e12
     k_tflops = k_flops / (k_ms / 1e3) / 1e12
     roofline = {"kernel": "k_gemm_tc<SwiGLU> (gate_up_proj + SiluAndMul)", "bound": "tensor",
-                "achieved": round(k_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(k_tflops / peaks["bf16_tflops"], 4), "peak_source": f"bf16_tflops ({peak_src}, burst)",
-                "flops_per_launch": k_flops, "launch_ms": round(k_ms, 4),
-                "traffic": GATE_UP_DRAM_BYTES_PER_LAUNCH}
+                "achieved": round(in_tflops, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(in_tflops / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": f"bf16_tflops_sustained ({peak_src}): the kernel is timed inside the stack step",
+                "flops_per_launch": k_flops, "launch_ms": round(in_ms, 4), "launches_timed": n_timed,
+                "traffic": GATE_UP_DRAM_BYTES_PER_LAUNCH,
+                "alone": {"launch_ms": round(k_ms, 4), "achieved": round(k_tflops, 1), "peak": peaks["bf16_tflops"],
+                          "frac": round(k_tflops / peaks["bf16_tflops"], 4),
+                          "peak_source": f"bf16_tflops ({peak_src}, burst)"}}
     del xin, aout, gws
 
     extra = {}

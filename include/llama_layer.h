@@ -385,6 +385,19 @@ int llama_num_sms(void);
  * difference across a region counts that region's kernels. */
 uint64_t llama_launch_count(void);
 
+/* Timing of the dominant kernel inside the layer and stack calls: between
+ * llama_gate_up_timer_start and llama_gate_up_timer_stop, every gate_up GEMM
+ * launch that llama_layer_forward or llama_stack_forward makes (up to
+ * max_launches) is bracketed by a pair of CUDA events on its stream.  _stop
+ * synchronises those events and returns the summed elapsed time (ms) and the
+ * number of launches timed.  A process-wide setting for benchmarks; the pages
+ * have no counterpart.  The events cost a little: the launch after them no
+ * longer overlaps its predecessor's prologue.  Not for use during stream
+ * capture.  Returns LLAMA_ERR_ARG for a bad count or when already running
+ * (start) / not running (stop), LLAMA_ERR_CUDA if an event call fails. */
+int llama_gate_up_timer_start(int max_launches);
+int llama_gate_up_timer_stop(float* total_ms, int* launches);
+
 /* Overrides how every projection GEMM of this process is scheduled (a process-
  * wide setting, read at each launch; for tests and benchmarks that need one
  * schedule).  The pages have no counterpart: they call library GEMMs.

@@ -86,6 +86,8 @@ SIGNATURES = {
     "llama_num_sms": (_I, []),
     "llama_launch_count": (ctypes.c_uint64, []),
     "llama_set_gemm_schedule": (_I, [_I]),
+    "llama_gate_up_timer_start": (_I, [_I]),
+    "llama_gate_up_timer_stop": (_I, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]),
     "llama_sample": (_I, [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "llama_moe_workspace_size": (_SZ, [ctypes.POINTER(LlamaMoeConfig), _I]),
     "llama_moe_forward": (_I, [ctypes.POINTER(LlamaMoeConfig), _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -298,6 +300,18 @@ def set_gemm_schedule(schedule: int) -> None:
     """Process-wide GEMM schedule: -1 automatic, 0 single-SM tiles, 1 stream-K,
     2 cluster split-K, 3 SM-pair tiles."""
     _check(lib().llama_set_gemm_schedule(int(schedule)), "llama_set_gemm_schedule")
+
+
+def gate_up_timer_start(max_launches: int) -> None:
+    """Time every gate_up GEMM launch of the layer and stack calls from now on."""
+    _check(lib().llama_gate_up_timer_start(int(max_launches)), "llama_gate_up_timer_start")
+
+
+def gate_up_timer_stop():
+    """(total ms, launches) of the gate_up launches timed since the start."""
+    ms, n = ctypes.c_float(0.0), ctypes.c_int(0)
+    _check(lib().llama_gate_up_timer_stop(ctypes.byref(ms), ctypes.byref(n)), "llama_gate_up_timer_stop")
+    return float(ms.value), int(n.value)
 
 
 def get_device_error(stream=None):

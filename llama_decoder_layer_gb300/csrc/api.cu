@@ -18,6 +18,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -36,6 +37,39 @@ int current_device() {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
   return d;
+}
+
+// Optional timing of the gate_up GEMM launches inside the layer calls
+// (llama_gate_up_timer_start / _stop): a pair of CUDA events around each
+// launch, on the launching stream.
+struct GateUpTimer {
+  std::mutex mu;
+  std::atomic<bool> on{false};
+  int used = 0;
+  std::vector<cudaEvent_t> ev;  // start, stop of launch i at 2i, 2i + 1
+};
+
+GateUpTimer& gate_up_timer() {
+  static GateUpTimer t;
+  return t;
+}
+
+// the event pair of the next timed launch (its start recorded), or -1
+int gate_up_timer_begin(cudaStream_t s) {
+  GateUpTimer& t = gate_up_timer();
+  if (!t.on.load(std::memory_order_relaxed)) return -1;
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.on.load(std::memory_order_relaxed) || 2 * (t.used + 1) > static_cast<int>(t.ev.size())) return -1;
+  const int i = t.used++;
+  cudaEventRecord(t.ev[2 * i], s);
+  return i;
+}
+
+void gate_up_timer_end(int i, cudaStream_t s) {
+  if (i < 0) return;
+  GateUpTimer& t = gate_up_timer();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (2 * i + 1 < static_cast<int>(t.ev.size())) cudaEventRecord(t.ev[2 * i + 1], s);
 }
 
 int* device_error_word() {
@@ -305,7 +339,9 @@ int layer_impl(const LlamaLayerConfig& c, const LlamaLayerWeights& w, const Llam
   // gate_up_proj + SiluAndMul
   GemmArgs gu = gemm(kEpiSwiGlu, normed, w.w_gate_up, 2 * I, H, a, I);
   gu.row_scale = rscale;
+  const int timed = gate_up_timer_begin(s);
   e = gemm_launch(gu, s);
+  gate_up_timer_end(timed, s);
   if (e) return cuda_status(e);
   // down_proj -> hidden_states
   e = gemm_launch(gemm(kEpiBf16, a, w.w_down, H, I, hidden, H), s);
@@ -686,6 +722,52 @@ const char* llama_status_string(int status) {
 int llama_num_sms(void) { return num_sms(); }
 
 uint64_t llama_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
+
+int llama_gate_up_timer_start(int max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20)) return LLAMA_ERR_ARG;
+  GateUpTimer& t = gate_up_timer();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (t.on.load()) return LLAMA_ERR_ARG;
+  for (cudaEvent_t e : t.ev) cudaEventDestroy(e);
+  t.ev.assign(2 * static_cast<size_t>(max_launches), nullptr);
+  for (auto& e : t.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      cudaGetLastError();
+      for (cudaEvent_t x : t.ev)
+        if (x) cudaEventDestroy(x);
+      t.ev.clear();
+      return LLAMA_ERR_CUDA;
+    }
+  }
+  t.used = 0;
+  t.on.store(true);
+  return LLAMA_OK;
+}
+
+int llama_gate_up_timer_stop(float* total_ms, int* launches) {
+  GateUpTimer& t = gate_up_timer();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.on.load()) return LLAMA_ERR_ARG;
+  t.on.store(false);
+  float total = 0.f;
+  int st = LLAMA_OK;
+  for (int i = 0; i < t.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      st = LLAMA_ERR_CUDA;
+      break;
+    }
+    total += ms;
+  }
+  if (total_ms) *total_ms = total;
+  if (launches) *launches = t.used;
+  for (cudaEvent_t e : t.ev) cudaEventDestroy(e);
+  t.ev.clear();
+  t.used = 0;
+  return st;
+}
 
 int llama_set_gemm_schedule(int schedule) {
   if (schedule < -1 || schedule > 3) return LLAMA_ERR_ARG;

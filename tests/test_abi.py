@@ -104,6 +104,17 @@ def test_launch_counter_counts_only_accepted_launches(lib):
     assert lb.launch_count() == before
 
 
+def test_gate_up_timer_and_schedule_argument_checks(lib):
+    # both are rejected on the host before any CUDA call
+    assert lib.llama_gate_up_timer_start(0) == lb.LLAMA_ERR_ARG
+    assert lib.llama_gate_up_timer_start(-5) == lb.LLAMA_ERR_ARG
+    ms, n = ctypes.c_float(0.0), ctypes.c_int(0)
+    assert lib.llama_gate_up_timer_stop(ctypes.byref(ms), ctypes.byref(n)) == lb.LLAMA_ERR_ARG  # not running
+    assert lib.llama_set_gemm_schedule(7) == lb.LLAMA_ERR_ARG
+    assert lib.llama_set_gemm_schedule(-2) == lb.LLAMA_ERR_ARG
+    assert lib.llama_set_gemm_schedule(-1) == lb.LLAMA_OK
+
+
 def test_sampler_host_argument_checks(lib):
     fake = ctypes.c_void_p(256)
     assert lib.llama_sample(None, 0, 10, None, None, None, None, None, None, None) == lb.LLAMA_OK  # no rows

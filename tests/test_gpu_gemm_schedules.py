@@ -142,3 +142,39 @@ def test_schedule_override_rejects_unknown_values():
         lb.set_gemm_schedule(4)
     with pytest.raises(lb.LlamaError):
         lb.set_gemm_schedule(-2)
+
+
+def test_gate_up_timer_counts_the_layer_launches():
+    """llama_gate_up_timer_*: one timed launch per layer of each stack call,
+    with a positive duration; none once stopped."""
+    spec = dataclasses.replace(I.SPECS["tiny"], num_layers=3, vocab=512, residual_none=True,
+                               groups=(("decode", 2, 1, 10, 40), ("prefill", 1, 30, 0, 0)))
+    bl = I.make_batch(spec, 2, DEV)
+    layers = [I.make_layer_weights(spec, 2, l, DEV) for l in range(spec.num_layers)]
+    caches = [I.make_kv_cache(spec, bl.num_blocks, 2, l, DEV) for l in range(spec.num_layers)]
+    emb, ids, lm, fn = I.make_stack_extras(spec, bl.num_tokens, 2, DEV)
+    cfg = lb.LayerConfig.from_spec(spec)
+    batch = lb.Batch.from_layout(bl)
+    T, B = bl.num_tokens, bl.num_seqs
+    ws = lb.alloc_workspace(lb.workspace_size(cfg, T, B, batch.max_seq_len, spec.vocab), DEV)
+    hidden = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device=DEV)
+    residual = torch.empty_like(hidden)
+    tokens = torch.empty(B, dtype=torch.int32, device=DEV)
+
+    def call():
+        lb.stack_forward(cfg, layers, fn, lm, batch, hidden, residual, [c[0] for c in caches],
+                         [c[1] for c in caches], tokens, ws, embed=emb, input_ids=ids)
+
+    call()
+    lb.gate_up_timer_start(100)
+    for _ in range(2):
+        call()
+    ms, n = lb.gate_up_timer_stop()
+    assert n == 2 * spec.num_layers and ms > 0
+    call()  # not timed
+    lb.gate_up_timer_start(1)  # the cap: further launches go untimed
+    call()
+    ms1, n1 = lb.gate_up_timer_stop()
+    assert n1 == 1 and ms1 > 0
+    torch.cuda.synchronize()
+    assert lb.get_device_error()[0] == lb.LLAMA_OK
