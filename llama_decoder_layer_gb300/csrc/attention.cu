@@ -719,14 +719,17 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // parity wait on the per-tile P V barrier would then mix up tiles.
 // ---------------------------------------------------------------------------
 constexpr int kTcThreads = 224;  // warp 0 Q + K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
-constexpr int kTcKeys = 64;                        // keys per K/V tile
-constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // 16 KB (K or V, two 64-column halves)
-constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V (8 KB)
+constexpr int kTcKeys = 64;                        // keys per K/V tile (64 or 128; 128-key tiles with one S
+                                                   // buffer and one-stage rings measured 2.23 vs 1.88 ms)
+constexpr int kTcSBufs = 2;                        // S buffers in tensor memory (2, or 1 with 128-key tiles)
+constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // K or V tile: two 64-column halves
+constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V
 constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
 constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
 constexpr int kTcKStages = 2;                     // K ring (three stages measured slower: 1.98 vs 1.87 ms)
-constexpr int kTcVStages = 2;                     // V ring (the code below indexes it with j & 1)
-static_assert(kTcVStages == 2, "the V ring is indexed by tile parity");
+constexpr int kTcVStages = 2;                     // V ring
+static_assert(kTcSBufs * kTcKeys + 128 <= 256, "S buffers and O must fit 256 tensor-memory columns");
+static_assert(kTcKeys == 64 || kTcKeys == 128, "the softmax handles 64- or 128-key tiles");
 constexpr int kTcSmem = 2 * kTcQHalf + (kTcKStages + kTcVStages) * kTcTileBytes + 256 + kTcSlack;
 constexpr float kRescaleLog2 = 8.0f;               // lazy rescale threshold (factor 256)
 
@@ -756,12 +759,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // already there) and arrive again before a slower warp arrived for tile j,
   // completing tile j's phase while part of P(j) was still being written.  A
   // warp cannot reach tile j+2 before P V of tile j is issued, so the arrivals
-  // at p_full0 + 8 * (j % 2) all belong to tile j.
+  // at p_full0 + 8 * (j % 2) all belong to tile j.  (With one S buffer a warp
+  // cannot reach tile j+1 before P V of tile j is issued either.)
   const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = k_full0 + 8 * kTcKStages,
                  v_full0 = k_empty0 + 8 * kTcKStages, v_empty0 = v_full0 + 8 * kTcVStages,
-                 s_full0 = v_empty0 + 8 * kTcVStages, p_full0 = s_full0 + 16, o_done = p_full0 + 16,
-                 drain = o_done + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcKStages + 2 * kTcVStages + 6);
+                 s_full0 = v_empty0 + 8 * kTcVStages, p_full0 = s_full0 + 8 * kTcSBufs,
+                 o_done = p_full0 + 8 * kTcSBufs, drain = o_done + 8;
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcKStages + 2 * kTcVStages + 2 * kTcSBufs + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
   int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
@@ -804,12 +809,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(k_full0 + 8 * i, 1);
       mbar_init(k_empty0 + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTcVStages; ++i) {
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(v_empty0 + 8 * i, 1);
-      mbar_init(s_full0 + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(p_full0 + 8 * i, 4);
+    for (int i = 0; i < kTcSBufs; ++i) {
+      mbar_init(s_full0 + 8 * i, 1);
+      mbar_init(p_full0 + 8 * i, 4);
+    }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -822,7 +829,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and kTcKeys, O at 2 * kTcKeys
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 (and kTcKeys), O at kTcSBufs * kTcKeys
+  constexpr int kOCol = kTcSBufs * kTcKeys;
 
   if (warp == 0 || warp == 6) {
     // ---------------- TMA producers: Q and K (warp 0), V (warp 6) ----------------
@@ -880,7 +888,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     bool ok = mbar_wait(q_full, 0, abort_flag);
     bool issued = false;
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;             // S buffer
+      const int st = j % kTcSBufs;      // S buffer
       const int kst = j % kTcKStages;   // K stage
       if (!mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) return false;
       tc_fence_after();
@@ -901,27 +909,33 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     };
     if (ok) ok = issue_s(0);
     for (int j = 0; j < ntiles && ok; ++j) {
-      if (j + 1 < ntiles && !issue_s(j + 1)) {
+      // with two S buffers S(j+1) goes ahead of P V(j); with one it must follow
+      // P V(j), which reads P(j) out of the same buffer
+      if (kTcSBufs > 1 && j + 1 < ntiles && !issue_s(j + 1)) {
         ok = false;
         break;
       }
-      if (!mbar_wait(p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag) ||
-          !mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag)) {
+      const int sbuf = j % kTcSBufs, vst = j % kTcVStages;
+      if (!mbar_wait(p_full0 + 8 * sbuf, (j / kTcSBufs) & 1, abort_flag) ||
+          !mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (lane == 0) {
-        const int st = j & 1;
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
-          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(st) + ks * 2048, kTcHalf, 1024);
-          tc_mma_f16_ts(tmem + 2 * kTcKeys, tmem + st * kTcKeys + ks * 8, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(vst) + ks * 2048, kTcHalf, 1024);
+          tc_mma_f16_ts(tmem + kOCol, tmem + sbuf * kTcKeys + ks * 8, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(v_empty0 + 8 * st);
+        tc_commit(v_empty0 + 8 * vst);
         tc_commit(o_done);
       }
       __syncwarp();
+      if (kTcSBufs == 1 && j + 1 < ntiles && !issue_s(j + 1)) {
+        ok = false;
+        break;
+      }
     }
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
@@ -941,29 +955,33 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float m_run = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait(s_full0 + 8 * st, (j >> 1) & 1, abort_flag)) {
+      const int st = j % kTcSBufs;
+      if (!mbar_wait(s_full0 + 8 * st, (j / kTcSBufs) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // S of this tile, read once: masked, scaled row maximum (eight
-      // independent max chains)
+      // S of this tile: masked, scaled row maximum (eight independent max
+      // chains), 64 columns per load; t keeps the last 64 columns read
       const int kbase = j * kTcKeys;
       const bool full_tile = kbase + kTcKeys - 1 <= pos_lo;  // CTA-uniform
       const int lim = pos - kbase;                           // column e is visible when e <= lim
-      float t[kTcKeys];
-      tmem_ld64(lane_addr + st * kTcKeys, t);
+      const uint32_t s_addr = lane_addr + st * kTcKeys;
+      float t[64];
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-      if (full_tile) {  // the softmax warps are issue-bound: two scores per max instruction
 #pragma unroll
-        for (int c2 = 0; c2 < kTcKeys / 2; ++c2) mx8[c2 & 7] = fmax3(mx8[c2 & 7], t[2 * c2], t[2 * c2 + 1]);
-      } else {
+      for (int h = 0; h < kTcKeys / 64; ++h) {
+        tmem_ld64(s_addr + h * 64, t);
+        if (full_tile) {  // the softmax warps are issue-bound: two scores per max instruction
 #pragma unroll
-        for (int e = 0; e < kTcKeys; ++e)
-          if (e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+          for (int c2 = 0; c2 < 32; ++c2) mx8[c2 & 7] = fmax3(mx8[c2 & 7], t[2 * c2], t[2 * c2 + 1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (h * 64 + e <= lim) mx8[e & 7] = fmaxf(mx8[e & 7], t[e]);
+        }
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -985,44 +1003,67 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float o[32];
-          tmem_ld32(lane_addr + 2 * kTcKeys + c * 32, o);
+          tmem_ld32(lane_addr + kOCol + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(lane_addr + 2 * kTcKeys + c * 32, o);
+          tmem_st32(lane_addr + kOCol + c * 32, o);
         }
         l *= alpha;
         m_run = m_new;
       }
       const float base = m_run == -INFINITY ? 0.f : m_run;
-      // P = exp2(S - max) as bf16 pairs over the first 32 columns of this S
-      // buffer; scale-and-shift and the row sum run as paired fp32 operations
-      float pw[kTcKeys / 2];
+      // P = exp2(S - max) as bf16 pairs, 32 scores at a time: packed column c
+      // holds keys 2c and 2c + 1, written over S column c.  Scale-and-shift and
+      // the row sum run as paired fp32 operations.
       uint64_t ls2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) ls2[i] = f2_pack(0.f, 0.f);
       const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
       const uint64_t nbase2 = f2_pack(-base, -base);
-      auto emit = [&](auto masked) {
+      auto emit32 = [&](const float* v, int c0, float* pw, auto masked) {
 #pragma unroll
-        for (int c2 = 0; c2 < kTcKeys / 2; ++c2) {
+        for (int c2 = 0; c2 < 16; ++c2) {
           const int e = 2 * c2;
           float a0, a1;
-          f2_unpack(f2_fma(f2_pack(t[e], t[e + 1]), scale2, nbase2), a0, a1);
+          f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), scale2, nbase2), a0, a1);
           float x0 = fast_exp2(a0);
           float x1 = fast_exp2(a1);
           if (decltype(masked)::value) {
-            x0 = e <= lim ? x0 : 0.f;
-            x1 = e + 1 <= lim ? x1 : 0.f;
+            x0 = c0 + e <= lim ? x0 : 0.f;
+            x1 = c0 + e + 1 <= lim ? x1 : 0.f;
           }
           ls2[c2 & 3] = f2_add(ls2[c2 & 3], f2_pack(x0, x1));
           pw[c2] = __uint_as_float(pack_bf16x2(x0, x1));
         }
       };
+      auto emit_tile = [&](auto masked) {
+        if constexpr (kTcKeys == 64) {
+          float pw[32];
+          emit32(t, 0, pw, masked);
+          emit32(t + 32, 32, pw + 16, masked);
+          tmem_st32(s_addr, pw);
+        } else {
+          // columns 0-63 are read again (t holds 64-127); chunk q's weights
+          // go to columns 16q..16q+15, all of them read by then
+#pragma unroll 1
+          for (int q = 0; q < 2; ++q) {
+            float u[32], pw[16];
+            tmem_ld32(s_addr + q * 32, u);
+            emit32(u, q * 32, pw, masked);
+            tmem_st16(s_addr + q * 16, pw);
+          }
+#pragma unroll
+          for (int q = 2; q < 4; ++q) {
+            float pw[16];
+            emit32(t + (q - 2) * 32, q * 32, pw, masked);
+            tmem_st16(s_addr + q * 16, pw);
+          }
+        }
+      };
       if (full_tile)
-        emit(std::false_type{});
+        emit_tile(std::false_type{});
       else
-        emit(std::true_type{});
-      tmem_st32(lane_addr + st * kTcKeys, pw);
+        emit_tile(std::true_type{});
       {
         float s[8];
 #pragma unroll
@@ -1033,12 +1074,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // (P is zero there, but stale cache contents must not reach the MMA),
       // once the tile's V load has landed
       if (j == ntiles - 1) {
-        if (!mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag)) {
+        const int vst = j % kTcVStages;
+        if (!mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
           ok = false;
           break;
         }
         const int valid = n_keys - kbase;
-        uint8_t* vg = smem + (v_s(st) - sb);
+        uint8_t* vg = smem + (v_s(vst) - sb);
         for (int i = threadIdx.x - 64; i < (kTcKeys - valid) * 2 * 8; i += 128) {
           const int rowv = valid + i / 16, hf = (i / 8) & 1, c16 = i & 7;
           *reinterpret_cast<uint4*>(vg + hf * kTcHalf + rowv * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
@@ -1065,7 +1107,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[32];
-        tmem_ld32(lane_addr + 2 * kTcKeys + c * 32, o);
+        tmem_ld32(lane_addr + kOCol + c * 32, o);
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= inv;

@@ -208,7 +208,7 @@ def test_single_tile_is_safe_either_way():
 # ---------------------------------------------------------------------------
 
 
-def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages=2):
+def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages=2, v_stages=2, s_bufs=2):
     """Every interleaving of the kernel's protocol including the K and V
     shared-memory rings (k_stages K stages, two V stages) and their producers.
     K(j) goes to stage j % k_stages, V(j) to stage j % 2; a producer waits for
@@ -223,9 +223,13 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
 
     split_producers: K from one thread and V from another (the kernel), or
     both from one thread in the order K(0), V(0), K(1), V(1), ...
+    s_bufs: S buffers in tensor memory.  With two, S(j+1) is issued before the
+    MMA thread waits for P(j); with one (128-key tiles), after P V(j), which
+    reads P(j) out of that buffer.
     mistake: plant one error to show the model catches it:
       "no_v_empty_wait"  the V producer does not wait for the stage to be free
       "no_k_empty_wait"  the K producer does not wait for the stage to be free
+      "s_ahead"          with one S buffer, S(j+1) issued before P V(j)
       "k_freed_late"     the K stage is freed after P V instead of after S
                          (safe, only slower: no violation expected)
       "no_v_full_wait"   the MMA thread issues P V without waiting for V
@@ -234,12 +238,14 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
     last = n_tiles - 1
     mma = [("wait_k", 0), ("issue_s", 0)]
     for j in range(n_tiles):
-        if j + 1 < n_tiles:
+        if (s_bufs > 1 or mistake == "s_ahead") and j + 1 < n_tiles:
             mma += [("wait_k", j + 1), ("issue_s", j + 1)]
         mma += [("wait_p", j)]
         if mistake != "no_v_full_wait":
             mma += [("wait_v", j)]
         mma += [("issue_pv", j)]
+        if s_bufs == 1 and mistake != "s_ahead" and j + 1 < n_tiles:
+            mma += [("wait_k", j + 1), ("issue_s", j + 1)]
     mma.append(("commit_drain", None))
     soft = []
     for j in range(n_tiles):
@@ -269,10 +275,10 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
 
     def fresh_barriers():
         b = {"o_done": Barrier(1), "drain": Barrier(1)}
-        for i in range(2):
-            for name in ("s", "vf", "ve"):
-                b["%s%d" % (name, i)] = Barrier(1)
-            b["p%d" % i] = Barrier(warps)
+        for i in range(s_bufs):
+            b["s%d" % i], b["p%d" % i] = Barrier(1), Barrier(warps)
+        for i in range(v_stages):
+            b["vf%d" % i], b["ve%d" % i] = Barrier(1), Barrier(1)
         for i in range(k_stages):
             b["kf%d" % i], b["ke%d" % i] = Barrier(1), Barrier(1)
         return b
@@ -288,7 +294,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
     # state: mma pc, warp pcs, producer pcs, pipe, barriers, loads in flight,
     # K stage contents, V stage contents, P written, S done, P V done, V rows zeroed
     start = (0, (0,) * warps, (0,) * len(producers), (), fresh_barriers(), frozenset(), (None,) * k_stages,
-             (None, None), frozenset(), frozenset(), frozenset(), frozenset())
+             (None,) * v_stages, frozenset(), frozenset(), frozenset(), frozenset())
 
     def key(st):
         m, w, pp, pipe, bars, fl, ks, vs, wr, sd, pvd, zr = st
@@ -318,7 +324,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
                 continue
             kind, (kv, j) = prog[pc]
             adv = ppcs[:i] + (pc + 1,) + ppcs[i + 1:]
-            n = k_stages if kv == "K" else 2
+            n = k_stages if kv == "K" else v_stages
             e = ("ke%d" if kv == "K" else "ve%d") % (j % n)
             if kind == "wait_empty":
                 if bars[e].passed(((j // n) & 1) ^ 1):
@@ -327,7 +333,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
                 nexts.append(with_(ppcs=adv, flight=flight | {(kv, j)}))
         # a load in flight lands (any of them)
         for (kv, j) in flight:
-            s = j % (k_stages if kv == "K" else 2)
+            s = j % (k_stages if kv == "K" else v_stages)
             nb = clone_bars(bars)
             nb[("kf%d" if kv == "K" else "vf%d") % s].arrive()
             if kv == "K":
@@ -335,7 +341,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
                     violations.add("K load overwrites a tile S has not read")
                 nexts.append(with_(bars=nb, flight=flight - {(kv, j)}, kst=kst[:s] + (j,) + kst[s + 1:]))
             else:
-                if j >= 2 and (j - 2) not in pv_done:
+                if j >= v_stages and (j - v_stages) not in pv_done:
                     violations.add("V load overwrites a tile P V has not read")
                 if j == last and zeroed:
                     violations.add("V load lands over the zeroed rows")
@@ -343,8 +349,9 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
         # the MMA thread
         if mpc < len(mma):
             kind, j = mma[mpc]
-            s = (j or 0) & 1
+            s = (j or 0) % s_bufs
             ks = (j or 0) % k_stages
+            vs = (j or 0) % v_stages
             if kind == "wait_k":
                 if bars["kf%d" % ks].passed((j // k_stages) & 1):
                     nexts.append(with_(mpc=mpc + 1))
@@ -352,14 +359,14 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
                 free_k = () if mistake == "k_freed_late" else (("commit", "ke%d" % ks),)
                 nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("S", j), ("commit", "s%d" % s)) + free_k))
             elif kind == "wait_p":
-                if bars["p%d" % s].passed((j >> 1) & 1):
+                if bars["p%d" % s].passed((j // s_bufs) & 1):
                     nexts.append(with_(mpc=mpc + 1))
             elif kind == "wait_v":
-                if bars["vf%d" % s].passed((j >> 1) & 1):
+                if bars["vf%d" % vs].passed((j // v_stages) & 1):
                     nexts.append(with_(mpc=mpc + 1))
             elif kind == "issue_pv":
                 free_k = (("commit", "ke%d" % ks),) if mistake == "k_freed_late" else ()
-                nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("PV", j), ("commit", "ve%d" % s), ("commit", "o_done"))
+                nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("PV", j), ("commit", "ve%d" % vs), ("commit", "o_done"))
                                    + free_k))
             elif kind == "commit_drain":
                 nexts.append(with_(mpc=mpc + 1, pipe=pipe + (("commit", "drain"),)))
@@ -369,11 +376,13 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
             if op == "S":
                 if kst[arg % k_stages] != arg or any(f == ("K", arg) for f in flight):
                     violations.add("S reads a K stage that does not hold its tile")
+                if arg >= s_bufs and (arg - s_bufs) not in pv_done:
+                    violations.add("S overwrites a P that P V has not read")
                 nexts.append(with_(pipe=pipe[1:], s_done=s_done | {arg}))
             elif op == "PV":
                 if any((arg, w) not in written for w in range(warps)):
                     violations.add("P V reads an incomplete P")
-                if vst[arg & 1] != arg:
+                if vst[arg % v_stages] != arg:
                     violations.add("P V reads a V stage that does not hold its tile")
                 if arg == last and len(zeroed) != warps:
                     violations.add("P V reads V rows that are not zeroed")
@@ -390,7 +399,7 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
             kind, j = soft[pc]
             adv = wpcs[:w] + (pc + 1,) + wpcs[w + 1:]
             if kind == "wait_s":
-                if bars["s%d" % (j & 1)].passed((j >> 1) & 1):
+                if bars["s%d" % (j % s_bufs)].passed((j // s_bufs) & 1):
                     nexts.append(with_(wpcs=adv))
             elif kind == "maybe_rescale":
                 nexts.append(with_(wpcs=adv))
@@ -401,17 +410,17 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
                         violations.add("O rescaled before P V(j-1)")
                     nexts.append(with_(wpcs=adv))
             elif kind == "write_p":
-                if j >= 2 and (j - 2) not in pv_done:
+                if j >= s_bufs and (j - s_bufs) not in pv_done:
                     violations.add("P overwrites a P not yet read")
                 nexts.append(with_(wpcs=adv, written=written | {(j, w)}))
             elif kind == "wait_v_last":
-                if bars["vf%d" % (j & 1)].passed((j >> 1) & 1):
+                if bars["vf%d" % (j % v_stages)].passed((j // v_stages) & 1):
                     nexts.append(with_(wpcs=adv))
             elif kind == "zero_v":
                 nexts.append(with_(wpcs=adv, zeroed=zeroed | {w}))
             elif kind == "arrive_p":
                 nb = clone_bars(bars)
-                nb["p%d" % (j & 1)].arrive()
+                nb["p%d" % (j % s_bufs)].arrive()
                 nexts.append(with_(wpcs=adv, bars=nb))
             elif kind == "wait_final":
                 if bars["drain"].passed(0):
@@ -433,6 +442,18 @@ def explore_with_loads(n_tiles, split_producers, warps=2, mistake=None, k_stages
 def test_k_and_v_rings_are_safe_with_one_or_two_producers(n_tiles, split):
     # K and V from separate producer threads, or (the earlier form) from one
     assert explore_with_loads(n_tiles, split_producers=split) == set()
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 4])
+def test_single_s_buffer_with_one_stage_rings_is_safe(n_tiles):
+    # 128-key tiles: one S buffer (S(j+1) after P V(j)), one K and one V stage
+    assert explore_with_loads(n_tiles, split_producers=True, k_stages=1, v_stages=1, s_bufs=1) == set()
+
+
+def test_single_s_buffer_needs_s_after_p_v():
+    # issuing S(j+1) ahead of P V(j) into the only buffer would overwrite P(j)
+    v = explore_with_loads(3, split_producers=True, k_stages=2, v_stages=1, s_bufs=1, mistake="s_ahead")
+    assert "S overwrites a P that P V has not read" in v or "P overwrites a P not yet read" in v
 
 
 @pytest.mark.parametrize("n_tiles", [2, 4])
