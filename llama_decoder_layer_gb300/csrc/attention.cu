@@ -347,12 +347,21 @@ __global__ void __launch_bounds__(kDecWarps * 32)
 }
 
 // Merges the split-KV partials of every multi-chunk decode sequence: one CTA
-// per (q head, sequence), one thread per output column, chunks in order.
+// per (sequence, kCombineThreads * 4 / D q heads), a thread per 4 output
+// columns of one head, chunks in order.  (One CTA per head and a thread per
+// column gave thousands of short CTAs whose launch and load latency, not the
+// bytes, set the time.)
+constexpr int kCombineThreads = 256;
+
 template <int D>
-__global__ void k_attn_combine(AttnParams p) {
+__global__ void __launch_bounds__(kCombineThreads) k_attn_combine(AttnParams p) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.y, h = blockIdx.x, col = threadIdx.x;
+  constexpr int kThreadsPerHead = D / 4;
+  const int b = blockIdx.y;
+  const int h = blockIdx.x * (kCombineThreads / kThreadsPerHead) + threadIdx.x / kThreadsPerHead;
+  const int col = (threadIdx.x % kThreadsPerHead) * 4;
+  if (h >= p.nq) return;
   const int t0 = p.qsl[b];
   if (p.qsl[b + 1] - t0 != 1) return;
   const int pos = p.positions[t0];
@@ -363,17 +372,25 @@ __global__ void k_attn_combine(AttnParams p) {
   const size_t base = static_cast<size_t>(b) * p.max_chunks * p.nq + h;
   float M = -INFINITY;
   for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(c) * p.nq].x);
-  float L = 0.f, O = 0.f;
+  float L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
     for (int c = 0; c < nch; ++c) {
       const size_t pi = base + static_cast<size_t>(c) * p.nq;
       const float2 ml = p.part_ml[pi];
+      const float4 o = *reinterpret_cast<const float4*>(p.part_o + pi * D + col);
       const float f = exp2f(ml.x - M);
       L += ml.y * f;
-      O += p.part_o[pi * D + col] * f;
+      O.x += o.x * f;
+      O.y += o.y * f;
+      O.z += o.z * f;
+      O.w += o.w * f;
     }
   }
-  p.out[static_cast<size_t>(t0) * p.nq * D + h * D + col] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+  uint2 u;
+  u.x = pack_bf16x2(L > 0.f ? O.x / L : 0.f, L > 0.f ? O.y / L : 0.f);
+  u.y = pack_bf16x2(L > 0.f ? O.z / L : 0.f, L > 0.f ? O.w / L : 0.f);
+  *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(t0) * p.nq * D + h * D + col) = u;
 }
 
 // ---------------------------------------------------------------------------
@@ -1279,8 +1296,11 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
   if (e == cudaSuccess) {
     dim3 gd(p.max_chunks, a.nkv, a.B);
     e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), sd, pdl_d, tk, tv, p);
-    if (e == cudaSuccess && p.max_chunks > 1)
-      e = launch_kernel(k_attn_combine<D>, dim3(a.nq, a.B), dim3(D), 0, sd, true, p);
+    if (e == cudaSuccess && p.max_chunks > 1) {
+      constexpr int heads_per_cta = kCombineThreads / (D / 4);
+      e = launch_kernel(k_attn_combine<D>, dim3((a.nq + heads_per_cta - 1) / heads_per_cta, a.B),
+                        dim3(kCombineThreads), 0, sd, true, p);
+    }
     if (!forked) pdl_s = true;
   }
   if (e == cudaSuccess && a.max_query_len >= 2)

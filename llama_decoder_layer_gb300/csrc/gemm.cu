@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // a split tile: this CTA's partial goes to the workspace
         float4* dst = partial_slot(p.partials, blockIdx.x, nseg == 0 ? 0 : 1) + row_in_tile;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < BN && tm * BM + quad * 32 < tc.m_limit; c += 32) {  // rows past M are never read
           float v[32];
           tmem_ld32(taddr + c, v);
           if (valid) {
@@ -1012,26 +1012,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 // Split-K over a thread-block cluster, for problems with at most half as many
 // tiles as SMs (decode-sized M).  The S CTAs of a cluster compute one tile,
-// CTA rank r over k-blocks [r*kb/S, (r+1)*kb/S), and each leaves its fp32
-// accumulator in its own shared memory ([BN/4][BM] float4 in the operand
-// ring, which is idle by then).  After a cluster barrier CTA r finishes the
-// column units u with u % S == r of every row, summing the S slices in rank
-// order through distributed shared memory; a second barrier keeps every
-// slice alive until all reads are done.  No partial tile leaves the chip and
-// no second kernel runs.
+// CTA rank r over k-blocks [r*kb/S, (r+1)*kb/S).  CTA r finishes the column
+// units u with u % S == r of every row.  Once every CTA's MMAs are done (a
+// cluster barrier), each CTA writes the 32-column chunks of its accumulator
+// straight into the shared memory of the CTA that finishes them (remote
+// stores into the operand ring, idle by then), a second barrier makes them
+// visible, and each CTA sums the S slices of its own chunks in rank order from
+// its own shared memory.  Stores to another CTA need no round trip, unlike
+// loads from it, so the reduction is not bound by distributed-shared-memory
+// latency.  No partial tile leaves the chip and no second kernel runs.
 // ---------------------------------------------------------------------------
-struct ClusterLoader {
-  uint32_t slice;  // shared::cta address of this CTA's fp32 slice
-  int S, row;
+
+// The unit that reads accumulator chunk c (columns 32c..32c+31) in
+// epilogue_unit and which of the unit's chunks it is; every unit reads
+// kChunksPerUnit chunks.
+template <int EPI>
+struct ChunkMap {
+  static constexpr int kChunksPerUnit = (EPI == kEpiBf16 || EPI == kEpiF32) ? 1 : 2;
+  __device__ __forceinline__ static void of(const GemmParams& p, int c, int& unit, int& which) {
+    if constexpr (EPI == kEpiBf16 || EPI == kEpiF32) {
+      unit = c;
+      which = 0;
+    } else if constexpr (EPI == kEpiSwiGlu) {  // gate columns 32u.., up columns BN/2 + 32u..
+      unit = c % (BN / 64);
+      which = c / (BN / 64);
+    } else {  // qkv: per head, lo chunks j then hi chunks half + j
+      const int per_head = p.qkv.head_dim / 64;
+      const int head = c / (2 * per_head), within = c % (2 * per_head);
+      unit = head * per_head + within % per_head;
+      which = within / per_head;
+    }
+  }
+};
+
+// Chunks CTA r receives: those of units r, r + S, ...; slot of chunk (unit, which).
+template <int EPI>
+__host__ __device__ constexpr int cluster_local_chunks(int S) {
+  return (EpiUnits<EPI>::kUnits + S - 1) / S * ChunkMap<EPI>::kChunksPerUnit;
+}
+
+// Receive buffer of CTA r: [source rank s][local chunk][8 float4 columns][BM rows],
+// so a warp's 32 rows write and read 512 contiguous bytes.
+__device__ __forceinline__ uint32_t recv_offset(int s, int nloc, int li, int q, int row) {
+  return static_cast<uint32_t>((((s * nloc + li) * 8 + q) * BM + row) * 16);
+}
+
+template <int EPI>
+struct PushLoader {
+  const GemmParams& p;
+  const uint8_t* recv;  // this CTA's receive buffer
+  int S, nloc, row;
   __device__ __forceinline__ void operator()(int col, float (&v)[32]) const {
+    int unit, which;
+    ChunkMap<EPI>::of(p, col / 32, unit, which);
+    const int li = unit / S * ChunkMap<EPI>::kChunksPerUnit + which;
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] = 0.f;
-    const uint32_t off = slice + static_cast<uint32_t>(((col / 4) * BM + row) * 16);
-    for (int c = 0; c < S; ++c) {
-      const uint32_t a = mapa_shared(off, static_cast<uint32_t>(c));
+    for (int s = 0; s < S; ++s) {
       float4 t[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) t[q] = ld_cluster_f4(a + q * BM * 16);
+      for (int q = 0; q < 8; ++q) t[q] = *reinterpret_cast<const float4*>(recv + recv_offset(s, nloc, li, q, row));
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         v[4 * q] += t[q].x;
@@ -1192,48 +1232,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
     if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain_bar, 0, nullptr);
   } else {
-    // ---------------- epilogue warps: accumulator -> this CTA's slice ----------------
+    // ---------------- epilogue warps: wait for the accumulator ----------------
     pdl_wait();
-    const int quad = warp & 3;
-    const int row_in_tile = quad * 32 + lane;
-    if (mbar_wait(tfull_bar, 0, abort_flag)) {
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-      float4* dst = reinterpret_cast<float4*>(smem) + row_in_tile;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(taddr + c, v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[(c / 4 + q) * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      }
-    } else {
+    if (!mbar_wait(tfull_bar, 0, abort_flag)) {
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmEpilogue);
       *abort_flag = 1;
     }
   }
 
+  constexpr int kUnits = EpiUnits<EPI>::kUnits;
+  const int nloc = cluster_local_chunks<EPI>(S);
+  if (S * nloc * BM * 128 > STAGES * STAGE_BYTES) {  // the host never picks such an S
+    if (threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereGemmEpilogue);
+    *abort_flag = 1;
+  }
   tc_fence_before();
   __syncwarp();
-  cluster_sync();  // every slice of the cluster is in shared memory
+  cluster_sync();  // every MMA of the cluster is done: the operand rings may be written
+  tc_fence_after();
+  const int quad = warp & 3;
+  if (warp >= 2 && !*abort_flag && tm * BM + quad * 32 < p.M) {  // rows past M are never read
+    // this warp's 32 accumulator rows, chunk by chunk, into the ring of the CTA that finishes the chunk
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      int unit, which;
+      ChunkMap<EPI>::of(p, c, unit, which);
+      const int li = unit / S * ChunkMap<EPI>::kChunksPerUnit + which;
+      const uint32_t dst = mapa_shared(sbase + recv_offset(rank, nloc, li, 0, row_in_tile),
+                                       static_cast<uint32_t>(unit % S));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_cluster_f4(dst + q * BM * 16, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();  // every chunk has arrived; no CTA touches another's shared memory after this
+  tc_fence_after();
   if (warp >= 2 && !*abort_flag) {
-    constexpr int kUnits = EpiUnits<EPI>::kUnits;
+    // the units of this CTA, row group by row group, spread over the four warps
     const int e = warp - 2;
     int item = 0;
     for (int u = rank; u < kUnits; u += S) {
-      for (int g = 0; g < BM / 32; ++g, ++item) {
-        if ((item & 3) != e || tm * BM + g * 32 >= p.M) continue;
+      for (int g = 0; g < BM / 32; ++g) {
+        if (tm * BM + g * 32 >= p.M) break;
+        if ((item++ & 3) != e) continue;
         const int row_in_tile = g * 32 + lane;
-        ClusterLoader cl{sbase, S, row_in_tile};
-        ScaledLoader<ClusterLoader> ld{cl, row_scale_of(p, tm * BM + row_in_tile, p.M)};
+        PushLoader<EPI> pl{p, smem, S, nloc, row_in_tile};
+        ScaledLoader<PushLoader<EPI>> ld{pl, row_scale_of(p, tm * BM + row_in_tile, p.M)};
         epilogue_unit<EPI>(p, tm, tn, row_in_tile, u, ld, rope_tab);
       }
     }
   }
-  __syncwarp();
-  cluster_sync();  // no slice is released while another CTA may still read it
-  tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, BN);
 }
 
@@ -1414,6 +1468,28 @@ int max_active_clusters_of(int epi, int S) {
   }
 }
 
+// The chunks a CTA of an S-CTA cluster receives fit its operand ring.
+bool cluster_chunks_fit(int epi, int S) {
+  int n = 0;
+  switch (epi) {
+    case kEpiBf16:
+      n = cluster_local_chunks<kEpiBf16>(S);
+      break;
+    case kEpiQkv:
+      n = cluster_local_chunks<kEpiQkv>(S);
+      break;
+    case kEpiSwiGlu:
+      n = cluster_local_chunks<kEpiSwiGlu>(S);
+      break;
+    case kEpiF32:
+      n = cluster_local_chunks<kEpiF32>(S);
+      break;
+    default:
+      return false;
+  }
+  return S * n * BM * 128 <= STAGES * STAGE_BYTES;
+}
+
 template <int EPI>
 int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pair, bool pdl,
                  cudaStream_t s) {
@@ -1491,7 +1567,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   int cluster = 0;
   if (!grouped && (mode == -1 || mode == 2) && p.tiles * 2 <= sms) {
     for (int S = sms / p.tiles < 8 ? sms / p.tiles : 8; S >= 2; --S) {
-      if (p.kb < 2 * S || max_active_clusters_of(a.epi, S) < p.tiles) continue;
+      if (p.kb < 2 * S || !cluster_chunks_fit(a.epi, S) || max_active_clusters_of(a.epi, S) < p.tiles) continue;
       cluster = S;
       break;
     }
@@ -1501,9 +1577,6 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   // (the 70B decode gate_up, 224 tiles: 162.9 us against 168.3 for stream-K
   // and its fixup)
   bool sk = cluster == 0 && p.tiles < sms;
-  if (mode == 0 || mode == 3) sk = false;
-  if (mode == 1) sk = true;
-  if (grouped) sk = false;
   // SM pairs (k_gemm_pair) only when asked for (schedule 3).  On the 70B
   // gate_up GEMM (4128 and 32768 rows) the pair kernel keeps the tensor pipe
   // 89-90% busy against 78% for single-SM tiles, but the part is then held by
