@@ -56,6 +56,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;  // accumulator columns per tile
+constexpr int kNarrowBN = 192;  // SwiGLU tiles of decode-sized M (96 gate + 96 up columns)
 constexpr int BK = 64;   // one 128-byte swizzle row of bf16
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
@@ -393,9 +394,10 @@ __device__ __forceinline__ void epilogue_unit(const GemmParams& p, int tm, int t
 // The whole tile for one row (one thread per row, the GEMM kernel's epilogue
 // warps).  For qkv the j-chunks are the outer loop so sin/cos are shared by
 // the heads of the tile.
-template <int EPI, class Loader>
+template <int EPI, int NB = BN, class Loader>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int tn, int row_in_tile, Loader& ld,
                                               const float2* rope_tab, int m_limit) {
+  static_assert(NB == BN || EPI == kEpiSwiGlu, "narrow tiles are SwiGLU tiles");
   const int row = tm * BM + row_in_tile;
   const bool valid = row < m_limit;
   if constexpr (EPI == kEpiBf16 || EPI == kEpiF32) {
@@ -408,13 +410,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int tm, int t
       if (valid) store_chunk(p, row, n_base + c, v, EPI == kEpiF32);
     }
   } else if constexpr (EPI == kEpiSwiGlu) {
-    const int n_base = tn * (BN / 2);
+    const int n_base = tn * (NB / 2);
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = 0; c < NB / 2; c += 32) {
       if (n_base + c >= p.n_out) break;
       float g[32], u[32];
       ld(c, g);
-      ld(BN / 2 + c, u);
+      ld(NB / 2 + c, u);
       if (!valid) continue;
       swiglu32(g, u);
       store_chunk(p, row, n_base + c, g, false);
@@ -514,7 +516,9 @@ struct PartialLoader {
   }
 };
 
-template <int EPI>
+// NB: the tile width (BN, or 192 for the narrow SwiGLU tiles of decode-sized
+// M: 96 gate and 96 up rows of B, in the first 24 KB of each stage's B slot).
+template <int EPI, int NB = BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ GemmParams p) {
@@ -524,6 +528,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;
 
+  static_assert(NB == BN || (EPI == kEpiSwiGlu && NB % 64 == 0 && NB < BN), "tile width");
+  constexpr int kStageTx = A_BYTES + NB * BK * 2;  // bytes a stage's loads deliver
   uint8_t* meta = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * STAGES + 5));
@@ -616,10 +622,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+          mbar_arrive_expect_tx(full_bar(stage), kStageTx);
           if (waited) tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
           tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
-          tma_load_2d(sb + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow1, pol_b);
+          tma_load_2d(sb + NB * BK, &tmB, full_bar(stage), kb * BK, brow1, pol_b);  // second NB / 2 rows
         }
         __syncwarp();
         if (!waited) {  // stage == n_pre here
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- MMA issuer ----------------
     // its bounded waits start only once the previous kernel has completed
     pdl_wait();
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, NB);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -727,7 +733,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (w.kb0 == 0 && w.kb1 == p.kb) {
         TmemLoader tl{taddr};
         ScaledLoader<TmemLoader> ld{tl, row_scale_of(p, tm * BM + row_in_tile, tc.m_limit)};
-        epilogue_tile<EPI>(p, tm, tn, row_in_tile, ld, rope_tab, tc.m_limit);
+        epilogue_tile<EPI, NB>(p, tm, tn, row_in_tile, ld, rope_tab, tc.m_limit);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -735,7 +741,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // a split tile: this CTA's partial goes to the workspace
         float4* dst = partial_slot(p.partials, blockIdx.x, nseg == 0 ? 0 : 1) + row_in_tile;
 #pragma unroll 1
-        for (int c = 0; c < BN && tm * BM + quad * 32 < tc.m_limit; c += 32) {  // rows past M are never read
+        for (int c = 0; c < NB && tm * BM + quad * 32 < tc.m_limit; c += 32) {  // rows past M are never read
           float v[32];
           tmem_ld32(taddr + c, v);
           if (valid) {
@@ -1364,6 +1370,10 @@ cudaError_t set_smem_attrs() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if constexpr (EPI == kEpiSwiGlu)
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(k_gemm_tc<EPI, kNarrowBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   SMEM_BYTES);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_gemm_cluster<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err == cudaSuccess)
@@ -1491,8 +1501,8 @@ bool cluster_chunks_fit(int epi, int S) {
 }
 
 template <int EPI>
-int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pair, bool pdl,
-                 cudaStream_t s) {
+int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pair,
+                 bool narrow, bool pdl, cudaStream_t s) {
   const cudaError_t attr_err = set_smem_attrs<EPI>();
   if (attr_err != cudaSuccess) return attr_err;
   if (pair)
@@ -1501,6 +1511,10 @@ int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams&
   if (cluster > 1)
     return launch_kernel_cluster(k_gemm_cluster<EPI>, dim3(p.tiles * cluster), dim3(NUM_THREADS), SMEM_BYTES, s, pdl,
                                  cluster, ta, tb, p);
+  if constexpr (EPI == kEpiSwiGlu) {
+    if (narrow)
+      return launch_kernel(k_gemm_tc<EPI, kNarrowBN>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
+  }
   cudaError_t e = launch_kernel(k_gemm_tc<EPI>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
   if (e != cudaSuccess || !p.sk) return e;
   return launch_kernel(k_gemm_fixup<EPI>, dim3(p.tiles, BM / kFixRows), dim3(EpiUnits<EPI>::kUnits * 32), 0, s,
@@ -1577,6 +1591,26 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   // (the 70B decode gate_up, 224 tiles: 162.9 us against 168.3 for stream-K
   // and its fixup)
   bool sk = cluster == 0 && p.tiles < sms;
+  // Narrow SwiGLU tiles for one row block (decode): 192 columns instead of 256
+  // when they fill the SMs' waves better, as whole tiles without a fixup (the
+  // 8B decode gate_up: 150 tiles in one wave instead of 112 tiles of stream-K;
+  // the 70B one: 299 tiles in two waves instead of 224).
+  bool narrow = false;
+  if (a.epi == kEpiSwiGlu && !grouped && mode == -1 && cluster == 0 && p.tiles_m == 1) {
+    const int I = a.N / 2;
+    const long long t_narrow = (I + kNarrowBN / 2 - 1) / (kNarrowBN / 2);
+    const long long waves_narrow = (t_narrow + sms - 1) / sms, waves_wide = (p.tiles + sms - 1) / sms;
+    if (waves_narrow * kNarrowBN < waves_wide * BN) {
+      narrow = true;
+      sk = false;
+      p.tiles_n = static_cast<int>(t_narrow);
+      p.b_tile_rows = kNarrowBN / 2;
+      p.tiles = p.tiles_m * p.tiles_n;
+    }
+  }
+  if (mode == 0 || mode == 3) sk = false;
+  if (mode == 1) sk = true;
+  if (grouped) sk = false;
   // SM pairs (k_gemm_pair) only when asked for (schedule 3).  On the 70B
   // gate_up GEMM (4128 and 32768 rows) the pair kernel keeps the tensor pipe
   // 89-90% busy against 78% for single-SM tiles, but the part is then held by
@@ -1608,16 +1642,17 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
 
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a.A, a.M, a.K, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, a.B, a.b_rows > 0 ? a.b_rows : a.N, a.K, BN / 2)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, a.B, a.b_rows > 0 ? a.b_rows : a.N, a.K, (narrow ? kNarrowBN : BN) / 2))
+    return cudaErrorInvalidValue;
   switch (a.epi) {
     case kEpiBf16:
-      return launch_typed<kEpiBf16>(ta, tb, p, cluster, pair, a.pdl != 0, s);
+      return launch_typed<kEpiBf16>(ta, tb, p, cluster, pair, narrow, a.pdl != 0, s);
     case kEpiQkv:
-      return launch_typed<kEpiQkv>(ta, tb, p, cluster, pair, a.pdl != 0, s);
+      return launch_typed<kEpiQkv>(ta, tb, p, cluster, pair, narrow, a.pdl != 0, s);
     case kEpiSwiGlu:
-      return launch_typed<kEpiSwiGlu>(ta, tb, p, cluster, pair, a.pdl != 0, s);
+      return launch_typed<kEpiSwiGlu>(ta, tb, p, cluster, pair, narrow, a.pdl != 0, s);
     case kEpiF32:
-      return launch_typed<kEpiF32>(ta, tb, p, cluster, pair, a.pdl != 0, s);
+      return launch_typed<kEpiF32>(ta, tb, p, cluster, pair, narrow, a.pdl != 0, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -178,3 +178,29 @@ def test_gate_up_timer_counts_the_layer_launches():
     assert n1 == 1 and ms1 > 0
     torch.cuda.synchronize()
     assert lb.get_device_error()[0] == lb.LLAMA_OK
+
+
+@pytest.mark.parametrize("M,I_,K", [
+    (64, 14336, 256),   # the 8B decode gate_up's tile grid: 150 narrow tiles in one wave
+    (128, 28672, 128),  # the 70B decode gate_up's: 299 narrow tiles in two waves
+    (37, 10000, 192),   # ragged M and a last tile with 16 of its 96 columns valid
+])
+def test_narrow_swiglu_tiles_for_one_row_block(M, I_, K):
+    """SwiGLU at decode-sized M with more than sms / 2 wide tiles runs on
+    192-column tiles (96 gate + 96 up rows of B); compared with the oracle
+    and with 256-column tiles (forced single-SM schedule)."""
+    x = I.normal_bf16((M, K), 1.0, 0.0, 51 + M, DEV)
+    w = I.normal_bf16((2 * I_, K), 0.02, 0.0, 52 + K, DEV)
+    outs = {}
+    for schedule in (-1, SINGLE):
+        lb.set_gemm_schedule(schedule)
+        a = torch.full((M, I_), float("nan"), dtype=torch.bfloat16, device=DEV)
+        lb.gate_up_silu(x, w, a, _ws())
+        torch.cuda.synchronize()
+        assert lb.get_device_error()[0] == lb.LLAMA_OK
+        outs[schedule] = a
+    gu = O.store(O.linear(f32(x), f32(w)), True)
+    ref = O.store(O.silu_and_mul(gu), True)
+    assert_close(f32(outs[-1]), ref, f"narrow SwiGLU {M}x{2 * I_}x{K}")
+    assert_close(f32(outs[SINGLE]), ref, f"wide SwiGLU {M}x{2 * I_}x{K}")
+    print(f"narrow vs wide tiles bit-identical: {torch.equal(outs[-1], outs[SINGLE])}")
