@@ -58,13 +58,15 @@ constexpr int BM = 128;
 constexpr int BN = 256;  // accumulator columns per tile
 constexpr int kNarrowBN = 192;  // SwiGLU tiles of decode-sized M (96 gate + 96 up columns)
 constexpr int BK = 64;   // one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int kMaxStages = 8;  // operand stages: as many as fit (4 of 48 KB for 256-column tiles and 128-row A boxes)
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// k_gemm_cluster: warp 0 TMA, warp 1 MMA, warps 2-7 wait for the accumulator;
+// then all eight move it, two warps per tensor-memory lane quarter
+constexpr int kClusterThreads = 256;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2048;  // + barriers, rope table, alignment slack
+constexpr int kMaxSmemBytes = 232448;              // the opt-in limit per CTA (227 KB)
+constexpr int kRingBudget = kMaxSmemBytes - 2048;  // the ring; the rest: barriers, rope table, alignment slack
 
 struct GemmParams {
   int M, N, K;
@@ -74,6 +76,10 @@ struct GemmParams {
   int b_row_step;    // row offset of the second 128-row B box (128, or I for SwiGLU)
   int b_tile_rows;   // B rows advanced per output tile (256, or 128 for SwiGLU)
   int b_evict_first;
+  // operand ring: stages of stage_bytes, the A box (a_rows rows: 128, or 64
+  // when M <= 64, the MMA then reading B bytes as rows 64-127 of A, whose
+  // accumulator rows are never stored) first in each stage
+  int stages, stage_bytes, a_rows;
   void* out;
   int ldo, n_out;
   float* partials;
@@ -529,25 +535,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sbase = raw_addr + pad;
 
   static_assert(NB == BN || (EPI == kEpiSwiGlu && NB % 64 == 0 && NB < BN), "tile width");
-  constexpr int kStageTx = A_BYTES + NB * BK * 2;  // bytes a stage's loads deliver
-  uint8_t* meta = smem + STAGES * STAGE_BYTES;
+  const int nst = p.stages, stage_bytes = p.stage_bytes, a_bytes = p.a_rows * BK * 2;
+  const int stage_tx = a_bytes + NB * BK * 2;  // bytes a stage's loads deliver
+  uint8_t* meta = smem + nst * stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * STAGES + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * nst + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* rope_tab = reinterpret_cast<float2*>(meta + 512);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (nst + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * nst + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * nst + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * nst + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -584,24 +591,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    // The weight tiles of the first STAGES k-blocks are requested before
+    // The weight tiles of the first nst k-blocks are requested before
     // waiting for the previous kernel (no kernel of the chain writes weights);
     // their activation tiles follow once it has completed.
     const uint64_t pol_a = policy_evict_last();
     const uint64_t pol_b = p.b_evict_first ? policy_evict_first() : policy_evict_normal();
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t uses[STAGES];
+    uint32_t uses[kMaxStages];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+    for (int s = 0; s < kMaxStages; ++s) uses[s] = 0;
     bool waited = false;
     int n_pre = 0;
-    int pre_kb[STAGES], pre_row[STAGES];
+    int pre_kb[kMaxStages], pre_row[kMaxStages];
     auto finish_wait = [&]() {
       pdl_wait();
       if (lane == 0)
         for (int i = 0; i < n_pre; ++i)
-          tma_load_2d(sbase + i * STAGE_BYTES, &tmA, full_bar(i), pre_kb[i] * BK, pre_row[i], pol_a);
+          tma_load_2d(sbase + i * stage_bytes, &tmA, full_bar(i), pre_kb[i] * BK, pre_row[i], pol_a);
       __syncwarp();
       waited = true;
     };
@@ -620,9 +627,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         if (lane == 0) {
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full_bar(stage), kStageTx);
+          const uint32_t sa = sbase + stage * stage_bytes;
+          const uint32_t sb = sa + a_bytes;
+          mbar_arrive_expect_tx(full_bar(stage), stage_tx);
           if (waited) tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
           tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
           tma_load_2d(sb + NB * BK, &tmB, full_bar(stage), kb * BK, brow1, pol_b);  // second NB / 2 rows
@@ -634,11 +641,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++n_pre;
         }
         uses[stage]++;
-        if (++stage == STAGES) {
+        if (++stage == nst) {
           stage = 0;
           phase ^= 1u;
         }
-        if (!waited && n_pre == STAGES) finish_wait();
+        if (!waited && n_pre == nst) finish_wait();
       }
     }
     if (!waited) finish_wait();
@@ -651,7 +658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       *abort_flag = 1;
     }
     // wait for every load this warp issued to land before the CTA can exit
-    for (int s = 0; s < STAGES; ++s)
+    for (int s = 0; s < nst; ++s)
       if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -679,8 +686,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa = sbase + stage * stage_bytes;
+          const uint32_t sb = sa + a_bytes;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k), idesc,
@@ -690,7 +697,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           issued = true;
         }
         __syncwarp();
-        if (++stage == STAGES) {
+        if (++stage == nst) {
           stage = 0;
           phase ^= 1u;
         }
@@ -1090,7 +1097,7 @@ struct PushLoader {
 };
 
 template <int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(kClusterThreads, 1)
     k_gemm_cluster(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1099,17 +1106,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;
 
-  uint8_t* meta = smem + STAGES * STAGE_BYTES;
+  const int nst = p.stages, stage_bytes = p.stage_bytes, a_bytes = p.a_rows * BK * 2;
+  uint8_t* meta = smem + nst * stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(meta);  // full[S], empty[S], tfull, drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * STAGES + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(meta + 8 * (2 * nst + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* rope_tab = reinterpret_cast<float2*>(meta + 512);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  const uint32_t tfull_bar = bar0 + 8u * (2 * STAGES);
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 1);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (nst + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * nst);
+  const uint32_t drain_bar = bar0 + 8u * (2 * nst + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1122,7 +1130,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tile_coords(p, tile, tm, tn);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -1138,7 +1146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   if constexpr (EPI == kEpiQkv) {
-    if (warp >= 2) copy_rope_table(p, rope_tab, threadIdx.x - 64, NUM_THREADS - 64);
+    if (warp >= 2) copy_rope_table(p, rope_tab, threadIdx.x - 64, kClusterThreads - 64);
   }
   tc_fence_before();
   __syncthreads();
@@ -1153,19 +1161,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int arow = tm * BM;
     const int brow0 = tn * p.b_tile_rows;
     const int brow1 = brow0 + p.b_row_step;
-    uint32_t uses[STAGES];
+    uint32_t uses[kMaxStages];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+    for (int s = 0; s < kMaxStages; ++s) uses[s] = 0;
     int stage = 0;
     uint32_t phase = 0;
     bool waited = false, ok = true;
     int n_pre = 0;
-    int pre_kb[STAGES];
+    int pre_kb[kMaxStages];
     auto finish_wait = [&]() {
       pdl_wait();
       if (lane == 0)
         for (int i = 0; i < n_pre; ++i)
-          tma_load_2d(sbase + i * STAGE_BYTES, &tmA, full_bar(i), pre_kb[i] * BK, arow, pol_a);
+          tma_load_2d(sbase + i * stage_bytes, &tmA, full_bar(i), pre_kb[i] * BK, arow, pol_a);
       __syncwarp();
       waited = true;
     };
@@ -1175,9 +1183,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       if (lane == 0) {
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+        const uint32_t sa = sbase + stage * stage_bytes;
+        const uint32_t sb = sa + a_bytes;
+        mbar_arrive_expect_tx(full_bar(stage), a_bytes + B_BYTES);
         if (waited) tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, arow, pol_a);
         tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, brow0, pol_b);
         tma_load_2d(sb + B_BYTES / 2, &tmB, full_bar(stage), kb * BK, brow1, pol_b);
@@ -1185,11 +1193,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (!waited) pre_kb[n_pre++] = kb;
       uses[stage]++;
-      if (++stage == STAGES) {
+      if (++stage == nst) {
         stage = 0;
         phase ^= 1u;
       }
-      if (!waited && n_pre == STAGES) finish_wait();
+      if (!waited && n_pre == nst) finish_wait();
     }
     if (!waited) finish_wait();
     if (lane == 0) pdl_trigger();
@@ -1197,7 +1205,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereGemmProducer);
       *abort_flag = 1;
     }
-    for (int s = 0; s < STAGES; ++s)
+    for (int s = 0; s < nst; ++s)
       if (uses[s] > 0) mbar_wait(full_bar(s), (uses[s] - 1) & 1u, nullptr);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -1213,8 +1221,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t sa = sbase + stage * stage_bytes;
+        const uint32_t sb = sa + a_bytes;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
           tc_mma_f16(tmem_base, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k), idesc,
@@ -1223,7 +1231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issued = true;
       }
       __syncwarp();
-      if (++stage == STAGES) {
+      if (++stage == nst) {
         stage = 0;
         phase ^= 1u;
       }
@@ -1248,7 +1256,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   constexpr int kUnits = EpiUnits<EPI>::kUnits;
   const int nloc = cluster_local_chunks<EPI>(S);
-  if (S * nloc * BM * 128 > STAGES * STAGE_BYTES) {  // the host never picks such an S
+  if (S * nloc * BM * 128 > nst * stage_bytes) {  // the host never picks such an S
     if (threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereGemmEpilogue);
     *abort_flag = 1;
   }
@@ -1257,14 +1265,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // every MMA of the cluster is done: the operand rings may be written
   tc_fence_after();
   const int quad = warp & 3;
-  if (warp >= 2 && !*abort_flag && tm * BM + quad * 32 < p.M) {  // rows past M are never read
-    // this warp's 32 accumulator rows, chunk by chunk, into the ring of the CTA that finishes the chunk
+  if (!*abort_flag && tm * BM + quad * 32 < p.M) {  // rows past M are never read
+    // this warp's 32 accumulator rows, half of the chunks (warps q and q + 4
+    // share lane quarter q), into the ring of the CTA that finishes each
+    // chunk; the next chunk is loaded while this one is stored
+    constexpr int kPerWarp = BN / 32 / 2;
     const int row_in_tile = quad * 32 + lane;
+    const int c0 = (warp >> 2) * kPerWarp;
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+    auto push = [&](int c, const uint32_t (&r)[32]) {
       int unit, which;
       ChunkMap<EPI>::of(p, c, unit, which);
       const int li = unit / S * ChunkMap<EPI>::kChunksPerUnit + which;
@@ -1272,21 +1281,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        static_cast<uint32_t>(unit % S));
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        st_cluster_f4(dst + q * BM * 16, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        st_cluster_f4(dst + q * BM * 16, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+    };
+    uint32_t r0[32], r1[32];
+    tmem_ld32_async(taddr + c0 * 32, r0);
+    tmem_ld_wait(r0);
+#pragma unroll
+    for (int i = 0; i < kPerWarp; i += 2) {
+      tmem_ld32_async(taddr + (c0 + i + 1) * 32, r1);
+      push(c0 + i, r0);
+      tmem_ld_wait(r1);
+      if (i + 2 < kPerWarp) tmem_ld32_async(taddr + (c0 + i + 2) * 32, r0);
+      push(c0 + i + 1, r1);
+      if (i + 2 < kPerWarp) tmem_ld_wait(r0);
     }
   }
   tc_fence_before();
   __syncwarp();
   cluster_sync();  // every chunk has arrived; no CTA touches another's shared memory after this
   tc_fence_after();
-  if (warp >= 2 && !*abort_flag) {
-    // the units of this CTA, row group by row group, spread over the four warps
-    const int e = warp - 2;
+  if (!*abort_flag) {
+    // the units of this CTA, row group by row group, spread over the eight warps
     int item = 0;
     for (int u = rank; u < kUnits; u += S) {
       for (int g = 0; g < BM / 32; ++g) {
         if (tm * BM + g * 32 >= p.M) break;
-        if ((item++ & 3) != e) continue;
+        if ((item++ & 7) != warp) continue;
         const int row_in_tile = g * 32 + lane;
         PushLoader<EPI> pl{p, smem, S, nloc, row_in_tile};
         ScaledLoader<PushLoader<EPI>> ld{pl, row_scale_of(p, tm * BM + row_in_tile, p.M)};
@@ -1369,13 +1390,13 @@ cudaError_t set_smem_attrs() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemBytes);
     if constexpr (EPI == kEpiSwiGlu)
       if (err == cudaSuccess)
         err = cudaFuncSetAttribute(k_gemm_tc<EPI, kNarrowBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   SMEM_BYTES);
+                                   kMaxSmemBytes);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(k_gemm_cluster<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      err = cudaFuncSetAttribute(k_gemm_cluster<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemBytes);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_gemm_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
   });
@@ -1445,8 +1466,8 @@ int max_active_clusters(int S) {
     if (set_smem_attrs<EPI>() == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
       cfg.gridDim = dim3(S * 64);
-      cfg.blockDim = dim3(NUM_THREADS);
-      cfg.dynamicSmemBytes = SMEM_BYTES;
+      cfg.blockDim = dim3(kClusterThreads);
+      cfg.dynamicSmemBytes = kMaxSmemBytes;  // one CTA per SM whatever the ring
       cudaLaunchAttribute attr;
       attr.id = cudaLaunchAttributeClusterDimension;
       attr.val.clusterDim.x = static_cast<unsigned>(S);
@@ -1478,8 +1499,14 @@ int max_active_clusters_of(int epi, int S) {
   }
 }
 
+// Stages of stage_bytes that fit the ring budget.
+int ring_stages(int stage_bytes) {
+  const int n = kRingBudget / stage_bytes;
+  return n < kMaxStages ? n : kMaxStages;
+}
+
 // The chunks a CTA of an S-CTA cluster receives fit its operand ring.
-bool cluster_chunks_fit(int epi, int S) {
+bool cluster_chunks_fit(int epi, int S, int ring_bytes) {
   int n = 0;
   switch (epi) {
     case kEpiBf16:
@@ -1497,25 +1524,26 @@ bool cluster_chunks_fit(int epi, int S) {
     default:
       return false;
   }
-  return S * n * BM * 128 <= STAGES * STAGE_BYTES;
+  return S * n * BM * 128 <= ring_bytes;
 }
 
 template <int EPI>
 int launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int cluster, bool pair,
                  bool narrow, bool pdl, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2048;
   const cudaError_t attr_err = set_smem_attrs<EPI>();
   if (attr_err != cudaSuccess) return attr_err;
   if (pair)
     return launch_kernel_cluster(k_gemm_pair<EPI>, dim3(p.grid), dim3(NUM_THREADS), PAIR_SMEM_BYTES, s, pdl, 2, ta,
                                  tb, p);
   if (cluster > 1)
-    return launch_kernel_cluster(k_gemm_cluster<EPI>, dim3(p.tiles * cluster), dim3(NUM_THREADS), SMEM_BYTES, s, pdl,
+    return launch_kernel_cluster(k_gemm_cluster<EPI>, dim3(p.tiles * cluster), dim3(kClusterThreads), smem, s, pdl,
                                  cluster, ta, tb, p);
   if constexpr (EPI == kEpiSwiGlu) {
     if (narrow)
-      return launch_kernel(k_gemm_tc<EPI, kNarrowBN>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
+      return launch_kernel(k_gemm_tc<EPI, kNarrowBN>, dim3(p.grid), dim3(NUM_THREADS), smem, s, pdl, ta, tb, p);
   }
-  cudaError_t e = launch_kernel(k_gemm_tc<EPI>, dim3(p.grid), dim3(NUM_THREADS), SMEM_BYTES, s, pdl, ta, tb, p);
+  cudaError_t e = launch_kernel(k_gemm_tc<EPI>, dim3(p.grid), dim3(NUM_THREADS), smem, s, pdl, ta, tb, p);
   if (e != cudaSuccess || !p.sk) return e;
   return launch_kernel(k_gemm_fixup<EPI>, dim3(p.tiles, BM / kFixRows), dim3(EpiUnits<EPI>::kUnits * 32), 0, s,
                        true, p);
@@ -1575,13 +1603,19 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.b_evict_first = grouped ? 0 : 1;
   p.group_m = p.tiles_m < 24 ? p.tiles_m : 24;
   const int sms = num_sms();
+  // A box of 64 rows when M <= 64 (not for SM pairs or expert tiles): every
+  // stage is 8 KB smaller, so the ring holds more stages of weights in flight.
+  p.a_rows = (a.M <= 64 && !grouped && mode != 3) ? 64 : BM;
+  const int wide_stage = p.a_rows * BK * 2 + B_BYTES;
   // At most sms / 2 tiles: split K over clusters of S CTAs (S as large as the
   // SMs allow, at least two k-blocks per CTA, all clusters resident at once).
   if (grouped && a.group_count == nullptr) return cudaErrorInvalidValue;
   int cluster = 0;
   if (!grouped && (mode == -1 || mode == 2) && p.tiles * 2 <= sms) {
     for (int S = sms / p.tiles < 8 ? sms / p.tiles : 8; S >= 2; --S) {
-      if (p.kb < 2 * S || !cluster_chunks_fit(a.epi, S) || max_active_clusters_of(a.epi, S) < p.tiles) continue;
+      if (p.kb < 2 * S || !cluster_chunks_fit(a.epi, S, ring_stages(wide_stage) * wide_stage) ||
+          max_active_clusters_of(a.epi, S) < p.tiles)
+        continue;
       cluster = S;
       break;
     }
@@ -1627,6 +1661,8 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
     p.tiles = p.tiles_m * p.tiles_n;
     p.group_m = p.tiles_m < 12 ? p.tiles_m : 12;  // 3072 activation rows per raster group, as above
   }
+  p.stage_bytes = p.a_rows * BK * 2 + (narrow ? kNarrowBN : BN) * BK * 2;
+  p.stages = ring_stages(p.stage_bytes);
   p.units = static_cast<long long>(p.tiles) * p.kb;
   if (sk) {
     long long g = p.units < sms ? p.units : sms;
@@ -1641,7 +1677,7 @@ int gemm_launch(const GemmArgs& a, cudaStream_t s) {
   p.sk = sk ? 1 : 0;
 
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, a.A, a.M, a.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&ta, a.A, a.M, a.K, p.a_rows)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.B, a.b_rows > 0 ? a.b_rows : a.N, a.K, (narrow ? kNarrowBN : BN) / 2))
     return cudaErrorInvalidValue;
   switch (a.epi) {
