@@ -422,6 +422,34 @@ def run_ours(args, world, rank, local):
         return run_single_layer(args, world, rank, local, lb, I, dev, peaks, peak_src, seed)
     W = setup_stack(lb, I, seed, dev, fold=args.fold_norms)
 
+    extra = {}
+    if not args.no_extra:
+        # Single-layer configurations, each timed as a workload of its own
+        # before the stack: the 70B decode and prefill layers (weights of the
+        # stack's layer 0, their own batches and caches) and the 8B decode
+        # layer.  The decode layers go first: after a power-capped prefill
+        # run the SM clock takes a while to come back, and the small decode
+        # GEMMs are latency-bound.  Clocks are sampled over each timed region.
+        for name in ("decode_70b", "decode_8b", "prefill_70b"):
+            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0] if name != "decode_8b" else None,
+                            fold=args.fold_norms)
+            steps = max(args.steps, 30) if name.startswith("decode") else args.steps
+            lms, lclocks = time_steps(L.step, steps, args.warmup, world, ClockSampler(local))
+            alg = layer_algorithmic(L.spec, L.bl)
+            tps = L.tokens_per_step * world / (lms / 1e3)
+            extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
+                           "roofline": layer_roofline(name, alg, lms, peaks, peak_src), "clocks": lclocks}
+            if name.startswith("decode"):
+                gms = time_graph(L.step, steps, args.warmup, world)
+                extra[name]["cuda_graph"] = {"layer_ms": round(gms, 4),
+                                             "tokens_per_s": round(L.tokens_per_step * world / (gms / 1e3), 1),
+                                             "roofline": layer_roofline(name, alg, gms, peaks, peak_src)}
+            st, detail = lb.get_device_error()
+            if st != lb.LLAMA_OK:
+                raise RuntimeError(f"device error in {name}: {lb.status_string(st)}")
+            del L
+            torch.cuda.empty_cache()
+
     # main line: the stack step
     sampler = ClockSampler(local)
     ms, clocks = time_steps(W.step, args.steps, args.warmup, world, sampler, counter=lb.launch_count)
@@ -470,29 +498,6 @@ def run_ours(args, world, rank, local):
     e2e_ms, h2d, d2h = time_e2e(lb, W, args.steps, args.warmup, world, dev)
     e2e_value = tok_layers * world / (e2e_ms / 1e3)
 
-    extra = {}
-    if not args.no_extra:
-        # single-layer 70B decode and prefill (weights of the stack's layer 0; their own batches/caches)
-        for name in ("decode_70b", "prefill_70b", "decode_8b"):
-            L = setup_layer(lb, I, name, seed, dev, weights=W.layers[0] if name != "decode_8b" else None,
-                            fold=args.fold_norms)
-            steps = max(args.steps, 30) if name.startswith("decode") else args.steps
-            lms, _ = time_steps(L.step, steps, args.warmup, world)
-            alg = layer_algorithmic(L.spec, L.bl)
-            tps = L.tokens_per_step * world / (lms / 1e3)
-            extra[name] = {"tokens_per_s": round(tps, 1), "layer_ms": round(lms, 4),
-                           "roofline": layer_roofline(name, alg, lms, peaks, peak_src)}
-            if name.startswith("decode"):
-                gms = time_graph(L.step, steps, args.warmup, world)
-                extra[name]["cuda_graph"] = {"layer_ms": round(gms, 4),
-                                             "tokens_per_s": round(L.tokens_per_step * world / (gms / 1e3), 1),
-                                             "roofline": layer_roofline(name, alg, gms, peaks, peak_src)}
-            st, detail = lb.get_device_error()
-            if st != lb.LLAMA_OK:
-                raise RuntimeError(f"device error in {name}: {lb.status_string(st)}")
-            del L
-            torch.cuda.empty_cache()
-
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         osmp = OracleSample(W, n_seqs=2)
@@ -518,6 +523,7 @@ def run_ours(args, world, rank, local):
         extra["decode_70b_80l"] = {
             "tokens_per_s_per_layer": round(B * L * world / (r["ms"] / 1e3), 1), "step_ms": round(r["ms"], 4),
             "roofline": r["roofline"],
+            "clocks": r["clocks"],
             "cuda_graph": {"step_ms": round(r["graph_ms"], 4),
                            "tokens_per_s_per_layer": round(B * L * world / (r["graph_ms"] / 1e3), 1),
                            "roofline": r["graph_roofline"]},
