@@ -153,7 +153,11 @@ int llama_fold_norm_weights(const void* norm_weight, const void* w, int rows, in
  * A token at position p attends to cache positions 0..p of its sequence
  * (this step's tokens are written first, so it sees itself).  A sequence with
  * one new token takes the split-KV decode path, one with two or more the
- * prefill path; both may appear in one batch.
+ * prefill path; both may appear in one batch.  The cache slots this step
+ * writes lie only in blocks of their own sequence that no other sequence of
+ * the batch reads (blocks shared between sequences hold only earlier
+ * tokens): the decode path requests a sequence's blocks before its last one
+ * while the qkv projection of the same call is still writing.
  * Device arrays (int32): positions [num_tokens], query_start_loc
  * [num_seqs+1], seq_lens [num_seqs], block_table [num_seqs,
  * max_blocks_per_seq], slot_mapping [num_tokens] or NULL (then slot =

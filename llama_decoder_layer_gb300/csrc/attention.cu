@@ -142,27 +142,85 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   uint8_t* qtile = smem + kDecWarps * kDecStages * 2 * TB;           // [16][D + 8] bf16
   uint64_t* bars = reinterpret_cast<uint64_t*>(qtile + 16 * QS);     // [warp][stage]
 
-  pdl_wait();
-  pdl_trigger();
+  // The batch metadata, the block table and every cache block but the one
+  // holding the sequence's new token are inputs of the call: no kernel of the
+  // chain writes them (the new token's K/V slot, in the last block, is
+  // written by the qkv epilogue).  They are read, and the chunk's first
+  // blocks requested, before waiting for the previous kernel; the q rows and
+  // the last block after it, and so is every global write.
   const int b = blockIdx.z, kvh = blockIdx.y, chunk = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = p.qsl[b];
-  if (p.qsl[b + 1] - t0 != 1) return;
-  const int pos = p.positions[t0];
+  int err_where = -1;  // reported once the previous kernel has completed
+  bool work = p.qsl[b + 1] - t0 == 1;
+  const int pos = work ? p.positions[t0] : 0;
   const int n_keys = pos + 1;
-  if (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks) {
-    if (chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
-    return;
+  if (work && (pos < 0 || n_keys > p.seq_lens[b] || (n_keys + kBS - 1) / kBS > p.max_blocks)) {
+    err_where = kWhereQueryLen;
+    work = false;
   }
   const int nblk = (n_keys + kBS - 1) / kBS;
-  const int nch = num_chunks(nblk);
-  if (nch > p.max_chunks) {  // context longer than the launch's max_seq_len
-    if (chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, kWhereQueryLen);
+  const int nch = work ? num_chunks(nblk) : 0;
+  if (work && nch > p.max_chunks) {  // context longer than the launch's max_seq_len
+    err_where = kWhereQueryLen;
+    work = false;
+  }
+  if (!work || chunk >= nch) {
+    pdl_wait();
+    pdl_trigger();
+    if (err_where >= 0 && chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, err_where);
     return;
   }
-  if (chunk >= nch) return;
   const int blk0 = chunk * nblk / nch, blk1 = (chunk + 1) * nblk / nch;
   const int G = p.group;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(smem_u32(bars + i), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int nb_w = blk0 + warp < blk1 ? (blk1 - blk0 - warp + kDecWarps - 1) / kDecWarps : 0;
+  const uint32_t wring = ring + warp * kDecStages * 2 * TB;
+  const uint32_t wbar = smem_u32(bars + warp * kDecStages);
+  const uint64_t pol = policy_evict_first();
+  const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+
+  auto issue_blk = [&](int i, int blk) {
+    const int row = (blk * p.nkv + kvh) * kBS;
+    const int st = i % kDecStages;
+    const uint32_t dst = wring + st * 2 * TB;
+    const uint32_t bar = wbar + 8 * st;
+    mbar_arrive_expect_tx(bar, 2 * TB);
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx) {
+      tma_load_2d(dst + bx * 2048, &tmK, bar, bx * 64, row, pol);
+      tma_load_2d(dst + TB + bx * 2048, &tmV, bar, bx * 64, row, pol);
+    }
+  };
+  auto issue = [&](int i) {  // after the wait: reports a bad block table entry
+    int blk = bt[blk0 + warp + kDecWarps * i];
+    if (blk < 0 || blk >= p.num_blocks) {
+      report_error(p.err, kErrGuard, kWhereBlockTable);
+      blk = 0;
+    }
+    issue_blk(i, blk);
+  };
+
+  // first stages before the wait: blocks other than the last, with valid entries
+  int n_early = 0;
+  if (lane == 0) {
+    for (; n_early < kDecStages && n_early < nb_w; ++n_early) {
+      const int jb = blk0 + warp + kDecWarps * n_early;
+      const int blk = bt[jb];
+      if (jb == nblk - 1 || blk < 0 || blk >= p.num_blocks) break;
+      issue_blk(n_early, blk);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (lane == 0)
+    for (int i = n_early; i < kDecStages && i < nb_w; ++i) issue(i);
+  __syncwarp();
 
   // q rows of the group (rows >= G are zero padding)
   for (int i = threadIdx.x; i < 16 * (D / 8); i += blockDim.x) {
@@ -170,10 +228,6 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < G) v = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(t0) * p.nq + kvh * G + r) * D)[c];
     *reinterpret_cast<uint4*>(qtile + r * QS + c * 16) = v;
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(smem_u32(bars + i), 1);
-    fence_mbar_init();
   }
   __syncthreads();
 
@@ -186,35 +240,6 @@ __global__ void __launch_bounds__(kDecWarps * 32)
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) ldsm_x4(base + kk * 32, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
   }
-
-  const int nb_w = blk0 + warp < blk1 ? (blk1 - blk0 - warp + kDecWarps - 1) / kDecWarps : 0;
-  const uint32_t wring = ring + warp * kDecStages * 2 * TB;
-  const uint32_t wbar = smem_u32(bars + warp * kDecStages);
-  const uint64_t pol = policy_evict_first();
-  const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-
-  auto issue = [&](int i) {
-    const int jb = blk0 + warp + kDecWarps * i;
-    int blk = bt[jb];
-    if (blk < 0 || blk >= p.num_blocks) {
-      report_error(p.err, kErrGuard, kWhereBlockTable);
-      blk = 0;
-    }
-    const int row = (blk * p.nkv + kvh) * kBS;
-    const int st = i % kDecStages;
-    const uint32_t dst = wring + st * 2 * TB;
-    const uint32_t bar = wbar + 8 * st;
-    mbar_arrive_expect_tx(bar, 2 * TB);
-#pragma unroll
-    for (int bx = 0; bx < D / 64; ++bx) {
-      tma_load_2d(dst + bx * 2048, &tmK, bar, bx * 64, row, pol);
-      tma_load_2d(dst + TB + bx * 2048, &tmV, bar, bx * 64, row, pol);
-    }
-  };
-
-  if (lane == 0)
-    for (int i = 0; i < kDecStages && i < nb_w; ++i) issue(i);
-  __syncwarp();
 
   float o[D / 8][4];
 #pragma unroll
