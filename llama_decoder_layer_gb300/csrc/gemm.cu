@@ -1,6 +1,6 @@
 // Tensor-core GEMM y = x * W^T for the four projections (and lm_head), on the
 // 5th-generation tensor cores: TMA loads 128-byte-swizzled K-major tiles into
-// a shared-memory ring, one thread issues tcgen05.mma (M=128, N=256, K=16)
+// a shared-memory ring, one thread issues tcgen05.mma (M=128, N=256 or 192, K=16)
 // into an fp32 accumulator in tensor memory, and four epilogue warps drain it
 // with tcgen05.ld and apply the fused epilogue:
 //   * plain bf16 store                         (o_proj, down_proj)
@@ -15,17 +15,21 @@
 // before SiluAndMul, exactly where the unfused modules would store it.
 //
 // Three schedules, by the number of output tiles against the SM count:
-//   * at least one wave of tiles (prefill, the 70B decode gate_up): k_gemm_tc,
-//     persistent (one CTA per SM), whole
-//     tiles in a grouped raster for L2 reuse, the accumulator double-buffered
-//     so the epilogue of one tile overlaps the MMAs of the next;
+//   * at least one wave of tiles (prefill): k_gemm_tc, persistent (one CTA
+//     per SM), whole tiles in a grouped raster for L2 reuse, the accumulator
+//     double-buffered so the epilogue of one tile overlaps the MMAs of the
+//     next;
 //   * at most half as many tiles as SMs (decode qkv, o_proj, down_proj):
-//     k_gemm_cluster, split-K over a thread-block cluster whose CTAs sum their
-//     fp32 slices through distributed shared memory;
-//   * in between, below one wave of tiles (the 8B decode gate_up): k_gemm_tc
-//     stream-K, every CTA an equal share of (tile, k-block) units, partial
-//     tiles in a workspace, and k_gemm_fixup summing them in CTA order
-//     (deterministic) spread over many CTAs.
+//     k_gemm_cluster, split-K over a thread-block cluster whose CTAs hand
+//     their fp32 slices to each other through distributed shared memory;
+//   * in between, below one wave of tiles: k_gemm_tc stream-K, every CTA an
+//     equal share of (tile, k-block) units, partial tiles in a workspace, and
+//     k_gemm_fixup summing them in CTA order (deterministic) spread over many
+//     CTAs.
+// SwiGLU over one row block (the decode gate_up) uses 192-column tiles when
+// they fill the waves better than 256-column ones (k_gemm_tc<SwiGLU, 192>).
+// The operand ring holds as many stages as fit: a 64-row A box when M <= 64
+// and narrow tiles make each stage smaller and the ring deeper.
 // Grouped mode (the experts of an MoE block): k_gemm_tc walks a tile list
 // built on the device, each entry naming its A rows, its expert's B rows and
 // how many of its rows are valid.  A row scale (an RMSNorm's rsqrt, its
