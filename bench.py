@@ -39,10 +39,10 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the gate_up
 # GEMM at the stack's shape (4128 x 57344 x 8192) from an ncu capture of the
-# current kernel (2.594 GB read + 0.183 GB written, one launch of
-# `bench.py --workload gemm_gate_up`, tensor pipe 78.3% active at 1837 MHz),
+# current kernel (2.415 GB read + 0.183 GB written, one launch of
+# `bench.py --workload gemm_gate_up`, tensor pipe 76.8% active at 1844 MHz),
 # or None when the kernel has changed since that capture.
-GATE_UP_DRAM_BYTES_PER_LAUNCH = 2594396160 + 183139840
+GATE_UP_DRAM_BYTES_PER_LAUNCH = 2414840576 + 183184640
 
 
 def load_peaks():

@@ -45,8 +45,8 @@ namespace {
 constexpr int kBS = 16;             // tokens per cache block
 constexpr int kDecWarps = 4;
 constexpr int kDecStages = 3;
-constexpr int kChunkBlocks = 96;    // at most 1536 keys per split-KV chunk (sweep: 512 -> 1536 keys took
-                                    // the 70B decode batch from 0.372 to 0.329 ms)
+constexpr int kChunkBlocks = 96;    // a sequence splits into ceil(keys / 1536) split-KV chunks (sweep:
+                                    // 512 -> 1536 keys took the 70B decode batch from 0.372 to 0.329 ms)
 constexpr int kPreStages = 2;
 constexpr int kPreKeys = 64;        // keys per prefill K/V tile (4 blocks)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kDecWarps * 32)
   // written by the qkv epilogue).  They are read, and the chunk's first
   // blocks requested, before waiting for the previous kernel; the q rows and
   // the last block after it, and so is every global write.
-  const int b = blockIdx.z, kvh = blockIdx.y, chunk = blockIdx.x;
+  const int b = blockIdx.x / p.nkv, kvh = blockIdx.x % p.nkv, chunk = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = p.qsl[b];
   int err_where = -1;  // reported once the previous kernel has completed
@@ -171,7 +171,14 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     if (err_where >= 0 && chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, err_where);
     return;
   }
-  const int blk0 = chunk * nblk / nch, blk1 = (chunk + 1) * nblk / nch;
+  // Chunk c of nch covers weight nch + 1 - c of the sequence's blocks, so
+  // earlier chunks are longer; the grid dispatches every sequence's chunk 0
+  // first, then every chunk 1, ..., so the last CTAs of the launch are the
+  // shortest and fill the last wave more evenly.
+  const int wsum = nch * (nch + 3) / 2;
+  const int wpre = chunk * (2 * nch + 3 - chunk) / 2;  // weights of chunks 0 .. chunk-1
+  const int blk0 = static_cast<int>(static_cast<long long>(nblk) * wpre / wsum);
+  const int blk1 = static_cast<int>(static_cast<long long>(nblk) * (wpre + nch + 1 - chunk) / wsum);
   const int G = p.group;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(smem_u32(bars + i), 1);
@@ -1319,7 +1326,7 @@ int launch_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, At
     if (!forked) pdl_d = true;
   }
   if (e == cudaSuccess) {
-    dim3 gd(p.max_chunks, a.nkv, a.B);
+    dim3 gd(a.B * a.nkv, p.max_chunks, 1);  // chunk-major: every sequence's first chunk first
     e = launch_kernel(k_attn_decode<D>, gd, dim3(kDecWarps * 32), decode_smem<D>(), sd, pdl_d, tk, tv, p);
     if (e == cudaSuccess && p.max_chunks > 1) {
       constexpr int heads_per_cta = kCombineThreads / (D / 4);

@@ -149,8 +149,8 @@ def _attn_case(nq, nkv, d, groups, seed):
 
 @pytest.mark.parametrize("nq,nkv,d", [(8, 2, 64), (16, 2, 128), (64, 8, 128)])
 def test_attention_decode(nq, nkv, d):
-    # contexts 0 (one visible key), 15, 16 (block edges), 1535/1536 (chunk edges: 1536 keys per
-    # split-KV chunk), up to 5000 (4 chunks)
+    # contexts 0 (one visible key), 15, 16 (block edges), 1535/1536 (where a sequence goes from one
+    # split-KV chunk to two), up to 5000 (4 chunks of decreasing length)
     groups = (("decode", 1, 1, 0, 0), ("decode", 1, 1, 15, 15), ("decode", 1, 1, 16, 16),
               ("decode", 1, 1, 1535, 1535), ("decode", 1, 1, 1536, 1536), ("decode", 5, 1, 1, 5000))
     g, r = _attn_case(nq, nkv, d, groups, 21)
