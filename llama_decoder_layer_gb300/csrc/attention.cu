@@ -171,14 +171,19 @@ __global__ void __launch_bounds__(kDecWarps * 32)
     if (err_where >= 0 && chunk == 0 && kvh == 0 && threadIdx.x == 0) report_error(p.err, kErrGuard, err_where);
     return;
   }
-  // Chunk c of nch covers weight nch + 1 - c of the sequence's blocks, so
-  // earlier chunks are longer; the grid dispatches every sequence's chunk 0
-  // first, then every chunk 1, ..., so the last CTAs of the launch are the
-  // shortest and fill the last wave more evenly.
-  const int wsum = nch * (nch + 3) / 2;
-  const int wpre = chunk * (2 * nch + 3 - chunk) / 2;  // weights of chunks 0 .. chunk-1
+  // Chunk c of nch covers a share of the sequence's blocks that falls with c
+  // (8:1 for two chunks, nch + 1 - c for more), and the grid dispatches every
+  // sequence's chunk 0 first, then every chunk 1, ..., so the last CTAs of
+  // the launch are the shortest and fill the last wave more evenly.
+  int wsum = 0, wpre = 0, wcur = 0;
+  for (int c = 0; c < nch; ++c) {
+    const int w = nch <= 2 ? (nch - c) * (nch - c) * (nch - c) : nch + 1 - c;
+    if (c < chunk) wpre += w;
+    if (c == chunk) wcur = w;
+    wsum += w;
+  }
   const int blk0 = static_cast<int>(static_cast<long long>(nblk) * wpre / wsum);
-  const int blk1 = static_cast<int>(static_cast<long long>(nblk) * (wpre + nch + 1 - chunk) / wsum);
+  const int blk1 = static_cast<int>(static_cast<long long>(nblk) * (wpre + wcur) / wsum);
   const int G = p.group;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(smem_u32(bars + i), 1);
