@@ -939,6 +939,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idS = idesc_bf16_f32(128, kTcKeys);
     constexpr uint32_t idPV = idesc_bf16_f32_bmn(128, 128);
+    // Operand descriptors, built once: only the start-address field (address
+    // / 16, bits 0-13; every shared address here is below 2^18) moves from one
+    // MMA to the next, so each MMA adds a constant to a precomputed low word.
+    const uint64_t sw0 = smem_desc_sw128(0), vd0 = smem_desc_sw128_lbo_sbo(0, kTcHalf, 1024);
+    const uint32_t sw_hi = static_cast<uint32_t>(sw0 >> 32), v_hi = static_cast<uint32_t>(vd0 >> 32);
+    const uint32_t sw_lo = static_cast<uint32_t>(sw0), v_lo = static_cast<uint32_t>(vd0);
+    const uint32_t q_lo = sw_lo + (q_s >> 4);
+    const uint32_t k_lo0 = sw_lo + (k_s(0) >> 4), k_lo1 = sw_lo + (k_s(1) >> 4);
+    const uint32_t v_lo0 = v_lo + (v_s(0) >> 4), v_lo1 = v_lo + (v_s(1) >> 4);
+    auto desc = [](uint32_t lo, uint32_t hi) { return (static_cast<uint64_t>(hi) << 32) | lo; };
+    static_assert(kTcKStages == 2 && kTcVStages == 2, "the MMA warp selects between two K and two V stages");
     bool ok = mbar_wait(q_full, 0, abort_flag);
     bool issued = false;
     auto issue_s = [&](int j) -> bool {
@@ -948,11 +959,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t d = tmem + st * kTcKeys;
+        const uint32_t kb = kst ? k_lo1 : k_lo0;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
           const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-          tc_mma_f16(d, smem_desc_sw128(q_s + cq), smem_desc_sw128(k_s(kst) + ck), idS, kk > 0 ? 1u : 0u);
+          tc_mma_f16(d, desc(q_lo + (cq >> 4), sw_hi), desc(kb + (ck >> 4), sw_hi), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full0 + 8 * st);
         tc_commit(k_empty0 + 8 * kst);
@@ -977,10 +989,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       tc_fence_after();
       if (lane == 0) {
+        const uint32_t vb = vst ? v_lo1 : v_lo0;
+        const uint32_t pa = tmem + sbuf * kTcKeys;
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
-          const uint64_t bdesc = smem_desc_sw128_lbo_sbo(v_s(vst) + ks * 2048, kTcHalf, 1024);
-          tc_mma_f16_ts(tmem + kOCol, tmem + sbuf * kTcKeys + ks * 8, bdesc, idPV, (j > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem + kOCol, pa + ks * 8, desc(vb + ks * (2048 >> 4), v_hi), idPV,
+                        (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc_commit(v_empty0 + 8 * vst);
         tc_commit(o_done);
