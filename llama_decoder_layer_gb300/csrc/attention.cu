@@ -759,20 +759,23 @@ __global__ void __launch_bounds__((kPreMaxHeads + 1) * 32)
 // every K/V tile is read once per group.  Warp 0 streams Q (one 3-D TMA box per
 // 64 columns) and the 64-key K tiles, warp 6 the 64-key V tiles (a 2-stage
 // ring each, so the next K tile never waits behind a V stage that P V still
-// holds); one thread of warp 1 issues S = Q K^T into a double-buffered TMEM
-// accumulator and
-// O += P V into a TMEM accumulator (V is the MN-major B operand); warps 2-5
-// (one row each) read each S tile from TMEM once, write P as bf16 pairs back
-// over the first half of that S buffer (tcgen05.st), and rescale O in TMEM
-// only when a row's running max grows by more than 2^8.  P V takes its A
+// holds); each reads a tile's block numbers before it waits for a free stage.
+// One thread of warp 1 issues S = Q K^T into a double-buffered TMEM
+// accumulator, one thread of warp 7 O += P V into a TMEM accumulator (V is the
+// MN-major B operand): split over two threads, the next S is issued while the
+// other thread waits for P, and neither waits behind the other's MMAs.  Warps
+// 2-5 (one row each) read each S tile from TMEM once, write P as bf16 pairs
+// back over the first half of that S buffer (tcgen05.st), and rescale O in
+// TMEM only when a row's running max grows by more than 2^8.  P V takes its A
 // operand from tensor memory, so the softmax of tile j+1 runs while P V of
-// tile j is in the tensor pipe: S buffer j%2 is next written by S of tile
-// j+2, which the MMA warp issues after P V of tile j.  Each S buffer has its
-// own P-ready barrier, and O is read after the once-only drain barrier: the
-// softmax warps may drift a tile apart, and a single P-ready barrier or a
-// parity wait on the per-tile P V barrier would then mix up tiles.
+// tile j is in the tensor pipe.  S buffer j%2 is next written by S of tile
+// j+2, which waits for the buffer's P V-done barrier (committed after P V of
+// tile j by the other thread).  Each S buffer has its own P-ready barrier, and
+// O is read after the once-only drain barrier: the softmax warps may drift a
+// tile apart, and a single P-ready barrier or a parity wait on the per-tile
+// P V barrier would then mix up tiles.
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 224;  // warp 0 Q + K loads, warp 1 MMA, warps 2-5 softmax, warp 6 V loads
+constexpr int kTcThreads = 256;  // warp 0 Q + K loads, 1 S MMAs, 2-5 softmax, 6 V loads, 7 P V MMAs
 constexpr int kTcKeys = 64;                        // keys per K/V tile (64 or 128; 128-key tiles with one S
                                                    // buffer and one-stage rings measured 2.23 vs 1.88 ms)
 constexpr int kTcSBufs = 2;                        // S buffers in tensor memory (2, or 1 with 128-key tiles)
@@ -780,7 +783,7 @@ constexpr int kTcTileBytes = kTcKeys * 128 * 2;    // K or V tile: two 64-column
 constexpr int kTcHalf = kTcKeys * 128;             // bytes of one 64-column half of K or V
 constexpr int kTcQHalf = 128 * 128;                // bytes of one 64-column half of Q (16 KB)
 constexpr int kTcSlack = 256;                      // alignment slack kept small so two CTAs share an SM
-constexpr int kTcKStages = 2;                     // K ring (three stages measured slower: 1.98 vs 1.87 ms)
+constexpr int kTcKStages = 2;                     // K ring (three stages measured slower: 1.796 vs 1.727 ms)
 constexpr int kTcVStages = 2;                     // V ring
 static_assert(kTcSBufs * kTcKeys + 128 <= 256, "S buffers and O must fit 256 tensor-memory columns");
 static_assert(kTcKeys == 64 || kTcKeys == 128, "the softmax handles 64- or 128-key tiles");
@@ -818,9 +821,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = k_full0 + 8 * kTcKStages,
                  v_full0 = k_empty0 + 8 * kTcKStages, v_empty0 = v_full0 + 8 * kTcVStages,
                  s_full0 = v_empty0 + 8 * kTcVStages, p_full0 = s_full0 + 8 * kTcSBufs,
-                 o_done = p_full0 + 8 * kTcSBufs, drain = o_done + 8;
+                 o_done = p_full0 + 8 * kTcSBufs, drain = o_done + 8, pv_done0 = drain + 8,
+                 s_drain = pv_done0 + 8 * kTcSBufs;
   uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcKStages + 2 * kTcVStages + 2 * kTcSBufs + 2);
+      reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcKStages + 2 * kTcVStages + 3 * kTcSBufs + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* p_hi_s = reinterpret_cast<int*>(tmem_slot + 2);
   int* p_lo_s = reinterpret_cast<int*>(tmem_slot + 3);
@@ -871,8 +875,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(s_full0 + 8 * i, 1);
       mbar_init(p_full0 + 8 * i, 4);
     }
+    for (int i = 0; i < kTcSBufs; ++i) mbar_init(pv_done0 + 8 * i, 1);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(s_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -904,6 +910,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const uint32_t full0 = is_k ? k_full0 : v_full0, empty0 = is_k ? k_empty0 : v_empty0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % nst;
+        // the tile's block numbers are read before the wait for a free stage
+        // (blocks past the context load the first block again: finite data the
+        // mask removes)
+        int blks[kTcKeys / kBS];
+#pragma unroll
+        for (int i = 0; i < kTcKeys / kBS; ++i) {
+          const int jb = j * (kTcKeys / kBS) + i;
+          blks[i] = bt[jb < nblk ? jb : 0];
+        }
         if (!mbar_wait(empty0 + 8 * st, ((j / nst) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -911,10 +926,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const uint32_t dst = is_k ? k_s(st) : v_s(st);
         const uint32_t bar = full0 + 8 * st;
         mbar_arrive_expect_tx(bar, kTcTileBytes);
+#pragma unroll
         for (int i = 0; i < kTcKeys / kBS; ++i) {
-          const int jb = j * (kTcKeys / kBS) + i;
-          // blocks past the context load the first block again: finite data the mask removes
-          int blk = bt[jb < nblk ? jb : 0];
+          int blk = blks[i];
           if (blk < 0 || blk >= p.num_blocks) {
             report_error(p.err, kErrGuard, kWhereBlockTable);
             blk = 0;
@@ -935,8 +949,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (uses[st] > 0) mbar_wait(full0 + 8 * st, (uses[st] - 1) & 1u, nullptr);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 || warp == 7) {
+    // ---------------- MMA issuers: S = Q K^T (warp 1), O += P V (warp 7) ----------------
     constexpr uint32_t idS = idesc_bf16_f32(128, kTcKeys);
     constexpr uint32_t idPV = idesc_bf16_f32_bmn(128, 128);
     // Operand descriptors, built once: only the start-address field (address
@@ -945,73 +959,73 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const uint64_t sw0 = smem_desc_sw128(0), vd0 = smem_desc_sw128_lbo_sbo(0, kTcHalf, 1024);
     const uint32_t sw_hi = static_cast<uint32_t>(sw0 >> 32), v_hi = static_cast<uint32_t>(vd0 >> 32);
     const uint32_t sw_lo = static_cast<uint32_t>(sw0), v_lo = static_cast<uint32_t>(vd0);
-    const uint32_t q_lo = sw_lo + (q_s >> 4);
-    const uint32_t k_lo0 = sw_lo + (k_s(0) >> 4), k_lo1 = sw_lo + (k_s(1) >> 4);
-    const uint32_t v_lo0 = v_lo + (v_s(0) >> 4), v_lo1 = v_lo + (v_s(1) >> 4);
     auto desc = [](uint32_t lo, uint32_t hi) { return (static_cast<uint64_t>(hi) << 32) | lo; };
-    static_assert(kTcKStages == 2 && kTcVStages == 2, "the MMA warp selects between two K and two V stages");
-    bool ok = mbar_wait(q_full, 0, abort_flag);
-    bool issued = false;
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % kTcSBufs;      // S buffer
-      const int kst = j % kTcKStages;   // K stage
-      if (!mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t d = tmem + st * kTcKeys;
-        const uint32_t kb = kst ? k_lo1 : k_lo0;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
-          const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-          tc_mma_f16(d, desc(q_lo + (cq >> 4), sw_hi), desc(kb + (ck >> 4), sw_hi), idS, kk > 0 ? 1u : 0u);
+    bool ok = true, issued = false;
+    if (warp == 1) {
+      // S(j) overwrites the buffer P(j - 2) was written to: it waits until
+      // P V(j - 2), issued by the other warp, has completed
+      const uint32_t q_lo = sw_lo + (q_s >> 4);
+      const uint32_t k_lo0 = sw_lo + (k_s(0) >> 4);  // stage st lies st * kTcTileBytes further on
+      ok = mbar_wait(q_full, 0, abort_flag);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j % kTcSBufs, kst = j % kTcKStages;
+        if ((j >= kTcSBufs && !mbar_wait(pv_done0 + 8 * st, ((j - kTcSBufs) / kTcSBufs) & 1, abort_flag)) ||
+            !mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        tc_commit(s_full0 + 8 * st);
-        tc_commit(k_empty0 + 8 * kst);
-        issued = true;
-      }
-      __syncwarp();
-      return true;
-    };
-    if (ok) ok = issue_s(0);
-    for (int j = 0; j < ntiles && ok; ++j) {
-      // with two S buffers S(j+1) goes ahead of P V(j); with one it must follow
-      // P V(j), which reads P(j) out of the same buffer
-      if (kTcSBufs > 1 && j + 1 < ntiles && !issue_s(j + 1)) {
-        ok = false;
-        break;
-      }
-      const int sbuf = j % kTcSBufs, vst = j % kTcVStages;
-      if (!mbar_wait(p_full0 + 8 * sbuf, (j / kTcSBufs) & 1, abort_flag) ||
-          !mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t vb = vst ? v_lo1 : v_lo0;
-        const uint32_t pa = tmem + sbuf * kTcKeys;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + st * kTcKeys;
+          const uint32_t kb = k_lo0 + kst * (kTcTileBytes >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
-          tc_mma_f16_ts(tmem + kOCol, pa + ks * 8, desc(vb + ks * (2048 >> 4), v_hi), idPV,
-                        (j > 0 || ks > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t cq = (kk >> 2) * kTcQHalf + (kk & 3) * 32;
+            const uint32_t ck = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+            tc_mma_f16(d, desc(q_lo + (cq >> 4), sw_hi), desc(kb + (ck >> 4), sw_hi), idS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(s_full0 + 8 * st);
+          tc_commit(k_empty0 + 8 * kst);
+          issued = true;
         }
-        tc_commit(v_empty0 + 8 * vst);
-        tc_commit(o_done);
+        __syncwarp();
       }
-      __syncwarp();
-      if (kTcSBufs == 1 && j + 1 < ntiles && !issue_s(j + 1)) {
-        ok = false;
-        break;
+    } else {
+      const uint32_t v_lo0 = v_lo + (v_s(0) >> 4);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int sbuf = j % kTcSBufs, vst = j % kTcVStages;
+        if (!mbar_wait(p_full0 + 8 * sbuf, (j / kTcSBufs) & 1, abort_flag) ||
+            !mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vb = v_lo0 + vst * (kTcTileBytes >> 4);
+          const uint32_t pa = tmem + sbuf * kTcKeys;
+#pragma unroll
+          for (int ks = 0; ks < kTcKeys / 16; ++ks) {  // P: 16 keys = 8 packed columns per step
+            tc_mma_f16_ts(tmem + kOCol, pa + ks * 8, desc(vb + ks * (2048 >> 4), v_hi), idPV,
+                          (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(v_empty0 + 8 * vst);
+          tc_commit(o_done);
+          tc_commit(pv_done0 + 8 * sbuf);
+          issued = true;
+        }
+        __syncwarp();
       }
     }
     if (!ok) {
       if (lane == 0) report_error(p.err, kErrTimeout, kWhereAttnPrefill);
       *abort_flag = 1;
     }
-    if (lane == 0 && issued) tc_commit(drain);
+    // each issuer waits for its own MMAs before the CTA frees tensor memory;
+    // the P V issuer's drain also tells the softmax warps that O is final
+    const uint32_t fin = warp == 1 ? s_drain : drain;
+    if (lane == 0 && issued) tc_commit(fin);
     __syncwarp();
-    if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(drain, 0, nullptr);
+    if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) mbar_wait(fin, 0, nullptr);
   } else {
     // ---------------- softmax warps (2-5): one row each ----------------
     const int quad = warp & 3;

@@ -30,6 +30,13 @@ A second model adds the K and V shared-memory rings and their TMA producers
 any order: no stage is overwritten before the MMA that reads it completes, S
 and P V read the tiles they expect, and the V rows past the context are zeroed
 after V lands and before P V reads them.
+
+A third model has the MMAs issued by two threads, as the kernel does: S from
+one, P V from the other, each thread's MMAs and commits in its own in-order
+queue with no order assumed between the queues.  S(j) then waits for a
+per-buffer P V-done barrier (P V(j-2) has completed) before it overwrites the
+buffer P(j-2) was written to; without that wait, or with the commit queued
+ahead of P V, the model finds S overwriting a P that P V has not read.
 """
 
 from collections import deque
@@ -481,3 +488,245 @@ def test_planted_ring_mistakes_are_caught(mistake, expected):
 
 def test_freeing_k_late_is_only_slower():
     assert explore_with_loads(3, split_producers=True, mistake="k_freed_late") == set()
+
+
+# ---------------------------------------------------------------------------
+# Two MMA issuers: S = Q K^T from one warp, P V from another
+# ---------------------------------------------------------------------------
+
+
+def explore_two_issuers(n_tiles, warps=2, s_bufs=2, mistake=None):
+    """Every interleaving of the protocol with the MMAs issued by two threads.
+
+    The S thread issues S(j) into buffer j % s_bufs once P V(j - s_bufs), which
+    read P out of that buffer, has completed (its per-buffer P V-done barrier,
+    committed by the P V thread) and K(j) has landed; it frees the K stage by a
+    commit.  The P V thread waits for P(j) and V(j), issues P V(j) and commits
+    the V stage's empty barrier, o_done, the buffer's P V-done barrier and, after
+    the last tile, the drain barrier.  Each thread's MMAs and commits run in its
+    own in-order queue, and the two queues progress independently (no order
+    between the threads' MMAs is assumed).  K and V come from their own
+    producers through two-stage rings, loads landing in any order.
+
+    mistake: plant one error to show the model catches it:
+      "no_pv_done_wait"  S(j) issued without waiting for P V(j - s_bufs)
+      "pv_done_early"    the P V-done commit queued before P V itself
+    Returns the set of violations seen."""
+    last, k_stages, v_stages = n_tiles - 1, 2, 2
+    s_prog = []
+    for j in range(n_tiles):
+        if j >= s_bufs and mistake != "no_pv_done_wait":
+            s_prog.append(("wait_pvd", j))
+        s_prog += [("wait_k", j), ("issue_s", j)]
+    pv_prog = []
+    for j in range(n_tiles):
+        pv_prog += [("wait_p", j), ("wait_v", j), ("issue_pv", j)]
+    pv_prog.append(("commit_drain", None))
+    soft = []
+    for j in range(n_tiles):
+        soft += [("wait_s", j)]
+        if j > 0:
+            soft += [("maybe_rescale", j), ("rescale", j)]
+        soft += [("write_p", j)]
+        if j == last:
+            soft += [("wait_v_last", j), ("zero_v", j)]
+        soft += [("arrive_p", j)]
+    soft += [("wait_final", None), ("read_o", None)]
+    producers = []
+    for kv in ("K", "V"):
+        prog = []
+        for j in range(n_tiles):
+            prog += [("wait_empty", (kv, j)), ("load", (kv, j))]
+        producers.append(prog)
+
+    def fresh_barriers():
+        b = {"o_done": Barrier(1), "drain": Barrier(1)}
+        for i in range(s_bufs):
+            b["s%d" % i], b["p%d" % i], b["pvd%d" % i] = Barrier(1), Barrier(warps), Barrier(1)
+        for i in range(2):
+            b["vf%d" % i], b["ve%d" % i], b["kf%d" % i], b["ke%d" % i] = Barrier(1), Barrier(1), Barrier(1), Barrier(1)
+        return b
+
+    def clone_bars(bars):
+        out = {}
+        for k, v in bars.items():
+            c = Barrier(v.count)
+            c.pending, c.phase = v.pending, v.phase
+            out[k] = c
+        return out
+
+    # state: S pc, P V pc, warp pcs, producer pcs, S queue, P V queue, barriers,
+    # loads in flight, K stages, V stages, P written, S done, P V done, V zeroed
+    start = (0, 0, (0,) * warps, (0, 0), (), (), fresh_barriers(), frozenset(), (None,) * k_stages,
+             (None,) * v_stages, frozenset(), frozenset(), frozenset(), frozenset())
+    names = ("spc", "vpc", "wpcs", "ppcs", "qs", "qv", "bars", "flight", "kst", "vst", "written", "s_done",
+             "pv_done", "zeroed")
+
+    def key(st):
+        return tuple(tuple(sorted((k, v.key()) for k, v in x.items())) if i == 6 else x for i, x in enumerate(st))
+
+    seen, queue, violations = set(), deque([start]), set()
+    while queue:
+        st = queue.popleft()
+        k = key(st)
+        if k in seen:
+            continue
+        seen.add(k)
+        cur = dict(zip(names, st))
+        bars = cur["bars"]
+        nexts = []
+
+        def with_(**kw):
+            d = dict(cur)
+            d.update(kw)
+            return tuple(d[n] for n in names)
+
+        def arrive(name):
+            nb = clone_bars(bars)
+            nb[name].arrive()
+            return nb
+
+        # producers
+        for i, prog in enumerate(producers):
+            pc = cur["ppcs"][i]
+            if pc >= len(prog):
+                continue
+            kind, (kv, j) = prog[pc]
+            adv = cur["ppcs"][:i] + (pc + 1,) + cur["ppcs"][i + 1:]
+            e = ("ke%d" if kv == "K" else "ve%d") % (j % 2)
+            if kind == "wait_empty":
+                if bars[e].passed(((j // 2) & 1) ^ 1):
+                    nexts.append(with_(ppcs=adv))
+            else:
+                nexts.append(with_(ppcs=adv, flight=cur["flight"] | {(kv, j)}))
+        # loads land
+        for (kv, j) in cur["flight"]:
+            s = j % 2
+            if kv == "K":
+                if j >= 2 and (j - 2) not in cur["s_done"]:
+                    violations.add("K load overwrites a tile S has not read")
+                nexts.append(with_(bars=arrive("kf%d" % s), flight=cur["flight"] - {(kv, j)},
+                                   kst=cur["kst"][:s] + (j,) + cur["kst"][s + 1:]))
+            else:
+                if j >= 2 and (j - 2) not in cur["pv_done"]:
+                    violations.add("V load overwrites a tile P V has not read")
+                if j == last and cur["zeroed"]:
+                    violations.add("V load lands over the zeroed rows")
+                nexts.append(with_(bars=arrive("vf%d" % s), flight=cur["flight"] - {(kv, j)},
+                                   vst=cur["vst"][:s] + (j,) + cur["vst"][s + 1:]))
+        # the S thread
+        if cur["spc"] < len(s_prog):
+            kind, j = s_prog[cur["spc"]]
+            adv = cur["spc"] + 1
+            if kind == "wait_pvd":
+                if bars["pvd%d" % (j % s_bufs)].passed(((j - s_bufs) // s_bufs) & 1):
+                    nexts.append(with_(spc=adv))
+            elif kind == "wait_k":
+                if bars["kf%d" % (j % 2)].passed((j // 2) & 1):
+                    nexts.append(with_(spc=adv))
+            else:
+                nexts.append(with_(spc=adv, qs=cur["qs"] + (("S", j), ("commit", "s%d" % (j % s_bufs)),
+                                                            ("commit", "ke%d" % (j % 2)))))
+        # the P V thread
+        if cur["vpc"] < len(pv_prog):
+            kind, j = pv_prog[cur["vpc"]]
+            adv = cur["vpc"] + 1
+            if kind == "wait_p":
+                if bars["p%d" % (j % s_bufs)].passed((j // s_bufs) & 1):
+                    nexts.append(with_(vpc=adv))
+            elif kind == "wait_v":
+                if bars["vf%d" % (j % 2)].passed((j // 2) & 1):
+                    nexts.append(with_(vpc=adv))
+            elif kind == "issue_pv":
+                pvd = ("commit", "pvd%d" % (j % s_bufs))
+                ops = (("PV", j), ("commit", "ve%d" % (j % 2)), ("commit", "o_done"), pvd)
+                if mistake == "pv_done_early":
+                    ops = (pvd, ("PV", j), ("commit", "ve%d" % (j % 2)), ("commit", "o_done"))
+                nexts.append(with_(vpc=adv, qv=cur["qv"] + ops))
+            else:
+                nexts.append(with_(vpc=adv, qv=cur["qv"] + (("commit", "drain"),)))
+        # either queue completes its oldest operation
+        for qn in ("qs", "qv"):
+            q = cur[qn]
+            if not q:
+                continue
+            op, arg = q[0]
+            if op == "S":
+                if cur["kst"][arg % 2] != arg or ("K", arg) in cur["flight"]:
+                    violations.add("S reads a K stage that does not hold its tile")
+                if arg >= s_bufs and (arg - s_bufs) not in cur["pv_done"]:
+                    violations.add("S overwrites a P that P V has not read")
+                nexts.append(with_(**{qn: q[1:], "s_done": cur["s_done"] | {arg}}))
+            elif op == "PV":
+                if any((arg, w) not in cur["written"] for w in range(warps)):
+                    violations.add("P V reads an incomplete P")
+                if cur["vst"][arg % 2] != arg:
+                    violations.add("P V reads a V stage that does not hold its tile")
+                if arg == last and len(cur["zeroed"]) != warps:
+                    violations.add("P V reads V rows that are not zeroed")
+                nexts.append(with_(**{qn: q[1:], "pv_done": cur["pv_done"] | {arg}}))
+            else:
+                nexts.append(with_(**{qn: q[1:], "bars": arrive(arg)}))
+        # softmax warps
+        wpcs = cur["wpcs"]
+        for w in range(warps):
+            pc = wpcs[w]
+            if pc >= len(soft):
+                continue
+            kind, j = soft[pc]
+            adv = wpcs[:w] + (pc + 1,) + wpcs[w + 1:]
+            if kind == "wait_s":
+                if bars["s%d" % (j % s_bufs)].passed((j // s_bufs) & 1):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "maybe_rescale":
+                nexts.append(with_(wpcs=adv))
+                nexts.append(with_(wpcs=wpcs[:w] + (pc + 2,) + wpcs[w + 1:]))
+            elif kind == "rescale":
+                if bars["o_done"].passed((j - 1) & 1):
+                    if (j - 1) not in cur["pv_done"]:
+                        violations.add("O rescaled before P V(j-1)")
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "write_p":
+                if j >= s_bufs and (j - s_bufs) not in cur["pv_done"]:
+                    violations.add("P overwrites a P not yet read")
+                nexts.append(with_(wpcs=adv, written=cur["written"] | {(j, w)}))
+            elif kind == "wait_v_last":
+                if bars["vf%d" % (j % 2)].passed((j // 2) & 1):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "zero_v":
+                nexts.append(with_(wpcs=adv, zeroed=cur["zeroed"] | {w}))
+            elif kind == "arrive_p":
+                nexts.append(with_(wpcs=adv, bars=arrive("p%d" % (j % s_bufs))))
+            elif kind == "wait_final":
+                if bars["drain"].passed(0):
+                    nexts.append(with_(wpcs=adv))
+            elif kind == "read_o":
+                if len(cur["pv_done"]) != n_tiles:
+                    violations.add("O read before the last P V")
+                nexts.append(with_(wpcs=adv))
+        done = (cur["spc"] == len(s_prog) and cur["vpc"] == len(pv_prog) and all(pc == len(soft) for pc in wpcs)
+                and not cur["qs"] and not cur["qv"] and not cur["flight"]
+                and all(pc == len(prog) for pc, prog in zip(cur["ppcs"], producers)))
+        if not nexts and not done:
+            violations.add("deadlock")
+        queue.extend(nexts)
+    return violations
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 4])
+def test_two_mma_issuers_are_safe(n_tiles):
+    # the kernel's protocol: S and P V from separate threads, S(j) after P V(j-2) has completed
+    assert explore_two_issuers(n_tiles) == set()
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3])
+def test_two_mma_issuers_with_one_s_buffer_are_safe(n_tiles):
+    # 128-key tiles: S(j) waits for P V(j-1)
+    assert explore_two_issuers(n_tiles, s_bufs=1) == set()
+
+
+@pytest.mark.parametrize("mistake", ["no_pv_done_wait", "pv_done_early"])
+def test_two_mma_issuers_need_the_p_v_done_wait(mistake):
+    # without the wait (or with the commit ahead of P V) S(j) can overwrite P(j-2) before P V(j-2) read it
+    v = explore_two_issuers(3, mistake=mistake)
+    assert "S overwrites a P that P V has not read" in v
