@@ -963,14 +963,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     bool ok = true, issued = false;
     if (warp == 1) {
       // S(j) overwrites the buffer P(j - 2) was written to: it waits until
-      // P V(j - 2), issued by the other warp, has completed
+      // P V(j - 2), issued by the other warp, has completed.  (Each issuer
+      // first waits for its operand tile, which has usually landed long
+      // before, so the wait that ends last is the one nearest the MMAs.)
       const uint32_t q_lo = sw_lo + (q_s >> 4);
       const uint32_t k_lo0 = sw_lo + (k_s(0) >> 4);  // stage st lies st * kTcTileBytes further on
       ok = mbar_wait(q_full, 0, abort_flag);
       for (int j = 0; j < ntiles && ok; ++j) {
         const int st = j % kTcSBufs, kst = j % kTcKStages;
-        if ((j >= kTcSBufs && !mbar_wait(pv_done0 + 8 * st, ((j - kTcSBufs) / kTcSBufs) & 1, abort_flag)) ||
-            !mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag)) {
+        if (!mbar_wait(k_full0 + 8 * kst, (j / kTcKStages) & 1, abort_flag) ||
+            (j >= kTcSBufs && !mbar_wait(pv_done0 + 8 * st, ((j - kTcSBufs) / kTcSBufs) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -994,8 +996,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const uint32_t v_lo0 = v_lo + (v_s(0) >> 4);
       for (int j = 0; j < ntiles && ok; ++j) {
         const int sbuf = j % kTcSBufs, vst = j % kTcVStages;
-        if (!mbar_wait(p_full0 + 8 * sbuf, (j / kTcSBufs) & 1, abort_flag) ||
-            !mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag)) {
+        if (!mbar_wait(v_full0 + 8 * vst, (j / kTcVStages) & 1, abort_flag) ||
+            !mbar_wait(p_full0 + 8 * sbuf, (j / kTcSBufs) & 1, abort_flag)) {
           ok = false;
           break;
         }

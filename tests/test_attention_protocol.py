@@ -498,10 +498,10 @@ def test_freeing_k_late_is_only_slower():
 def explore_two_issuers(n_tiles, warps=2, s_bufs=2, mistake=None):
     """Every interleaving of the protocol with the MMAs issued by two threads.
 
-    The S thread issues S(j) into buffer j % s_bufs once P V(j - s_bufs), which
-    read P out of that buffer, has completed (its per-buffer P V-done barrier,
-    committed by the P V thread) and K(j) has landed; it frees the K stage by a
-    commit.  The P V thread waits for P(j) and V(j), issues P V(j) and commits
+    The S thread issues S(j) into buffer j % s_bufs once K(j) has landed and
+    P V(j - s_bufs), which read P out of that buffer, has completed (its
+    per-buffer P V-done barrier, committed by the P V thread); it frees the K
+    stage by a commit.  The P V thread waits for V(j) and P(j), issues P V(j) and commits
     the V stage's empty barrier, o_done, the buffer's P V-done barrier and, after
     the last tile, the drain barrier.  Each thread's MMAs and commits run in its
     own in-order queue, and the two queues progress independently (no order
@@ -515,12 +515,13 @@ def explore_two_issuers(n_tiles, warps=2, s_bufs=2, mistake=None):
     last, k_stages, v_stages = n_tiles - 1, 2, 2
     s_prog = []
     for j in range(n_tiles):
+        s_prog.append(("wait_k", j))
         if j >= s_bufs and mistake != "no_pv_done_wait":
             s_prog.append(("wait_pvd", j))
-        s_prog += [("wait_k", j), ("issue_s", j)]
+        s_prog.append(("issue_s", j))
     pv_prog = []
     for j in range(n_tiles):
-        pv_prog += [("wait_p", j), ("wait_v", j), ("issue_pv", j)]
+        pv_prog += [("wait_v", j), ("wait_p", j), ("issue_pv", j)]
     pv_prog.append(("commit_drain", None))
     soft = []
     for j in range(n_tiles):
