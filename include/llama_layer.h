@@ -43,10 +43,14 @@
  *     llama_workspace_size() returns.
  *   - Work is enqueued on `stream` and runs asynchronously; nothing
  *     synchronises the host.  Results are valid once the stream reaches them.
- *     The first kernel of a call starts after everything queued before it on
- *     the stream has completed; each later kernel of the call may start its
- *     prologue while the one before it finishes (programmatic dependent
- *     launch) and reads that kernel's results only after it has completed.
+ *     Each kernel of a call may start its prologue while the kernel before
+ *     it on the stream finishes (programmatic dependent launch) and reads
+ *     that kernel's results only after it has completed.  The first kernel
+ *     of llama_layer_forward, llama_stack_forward and llama_moe_layer_forward
+ *     (an embedding gather or a norm) reads nothing before then, so work
+ *     queued before the call is complete before any of its data is read;
+ *     the other entry points' first kernels start only after everything
+ *     queued before them has completed.
  *   - A workspace belongs to one call at a time: calls that may overlap on the
  *     GPU need separate workspaces.  Its contents need not be initialised.
  *   - A call returns LLAMA_OK, or a status code without launching anything

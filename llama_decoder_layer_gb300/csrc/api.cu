@@ -225,9 +225,9 @@ AttnArgs attn_args(const LlamaLayerConfig& c, const LlamaBatch& b, const void* q
   return a;
 }
 
-// The kernels of one layer, in order.  chain: the first kernel may overlap the
-// kernel before it on the stream (one of this library's, inside a stack call);
-// every later kernel overlaps its predecessor in the layer.
+// The kernels of one layer, in order.  chain: the first kernel (the input
+// norm, which reads nothing before it waits) may overlap the kernel before it
+// on the stream; every later kernel overlaps its predecessor in the layer.
 // The MLP of a Qwen3-MoE layer: the sparse block's config, weights and
 // workspace, and where the chosen experts go (or null).
 struct MoeMlp {
@@ -395,7 +395,7 @@ int llama_layer_forward(const LlamaLayerConfig* cfg, const LlamaLayerWeights* we
   const Layout L = make_layout(*cfg, batch->num_tokens, batch->num_seqs, batch->max_seq_len, 0);
   if (workspace == nullptr || workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
   return layer_impl(*cfg, *weights, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache,
-                    ws_base(workspace), L, false, reinterpret_cast<cudaStream_t>(stream));
+                    ws_base(workspace), L, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const LlamaLayerWeights* layers,
@@ -427,12 +427,12 @@ int llama_stack_forward(const LlamaLayerConfig* cfg, int num_layers, const Llama
   const int T = batch->num_tokens, B = batch->num_seqs, H = cfg->hidden;
   int e;
   if (embed_w) {
-    e = embed_launch(embed_w, input_ids, T, H, vocab, hidden_states, err, false, s);
+    e = embed_launch(embed_w, input_ids, T, H, vocab, hidden_states, err, true, s);
     if (e) return LLAMA_ERR_CUDA;
   }
   for (int l = 0; l < num_layers; ++l) {
     st = layer_impl(*cfg, layers[l], *batch, hidden_states, l == 0 ? nullptr : residual, residual, k_caches[l],
-                    v_caches[l], ws, L, l > 0 || embed_w != nullptr, s);
+                    v_caches[l], ws, L, true, s);
     if (st) return st;
   }
   // final norm over the last token of every sequence
@@ -667,7 +667,7 @@ int llama_moe_layer_forward(const LlamaLayerConfig* cfg, const LlamaMoeConfig* m
   w.w_o = weights->w_o;
   w.ln2_w = weights->ln2_w;
   MoeMlp mm{moe, weights->w_router, weights->w13, weights->w2, base + layer_bytes, out_expert_ids};
-  return layer_impl(*cfg, w, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache, base, L, false,
+  return layer_impl(*cfg, w, *batch, hidden_states, residual_in, residual_out, k_cache, v_cache, base, L, true,
                     reinterpret_cast<cudaStream_t>(stream), &mm);
 }
 
