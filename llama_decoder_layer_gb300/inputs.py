@@ -19,6 +19,11 @@ Workloads (all sizes as the layer sees them):
 * ``stack_70b``   8 layers of the 70B shape + final norm + lm_head (vocab
                   128256) + greedy argmax; 32 decode sequences (context uniform
                   in [1024, 16384]) then 2 prefill chunks of 2048 tokens.
+* ``small_mixed`` hidden 1024, 8 q heads x 128, 2 kv heads, intermediate
+                  2048, llama3 scaling; 3 decode sequences (context uniform in
+                  [1500, 2100], one or two split-KV chunks) and one 80-token
+                  prefill chunk after a 32-token cached prefix: the head_dim-128
+                  kernels of every path at a size the oracle runs in seconds.
 
 Value recipe: projection, lm_head weights ~N(0, 0.02) in bf16; norm weights
 1 + N(0, 0.02) (the reading that keeps the norms' scale); hidden states,
@@ -73,6 +78,8 @@ class Spec:
 SPECS = {
     "tiny": Spec("tiny", 512, 8, 2, 64, 1376, 1e-5, 10000.0, None,
                  groups=(("prefill", 2, 32, 0, 0),), residual_none=True),
+    "small_mixed": Spec("small_mixed", 1024, 8, 2, 128, 2048, 1e-5, 500000.0, LLAMA3_SCALING,
+                        groups=(("decode", 3, 1, 1500, 2100), ("prefill", 1, 80, 32, 32))),
     "decode_8b": Spec("decode_8b", 4096, 32, 8, 128, 14336, 1e-5, 500000.0, None,
                       groups=(("decode", 64, 1, 2048, 2048),)),
     "decode_70b": Spec("decode_70b", 8192, 64, 8, 128, 28672, 1e-5, 500000.0, LLAMA3_SCALING,
